@@ -1,0 +1,158 @@
+"""fp64 CPU oracle for the DDTree verify step -- test infrastructure only.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline leg may import this package.  It shares nothing with the CUDA path.
+The arithmetic lives in ``lucetree_oracle.c`` (plain C, fp64); this module
+builds it with gcc and marshals numpy arrays.  Every function below states the
+rule it follows; the C file carries the citations and the pins are in
+``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sysconfig
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lucetree_oracle.c")
+_LIB = os.path.join(_HERE, "liblucetree_oracle.so")
+_lib = None
+
+F16, BF16 = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (portable flags only)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int, ctypes.c_long, ctypes.c_double
+        lib.oracle_verify_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, i32, P, i32,
+                                           P, P, P, P, P, i64, P, P, i32]
+        lib.oracle_verify_attn.restype = i32
+        lib.oracle_argmax.argtypes = [P, i64, i64, i64, P]
+        lib.oracle_argmax.restype = None
+        lib.oracle_accept.argtypes = [i32, i32, P, P, P, P, P, P]
+        lib.oracle_accept.restype = i32
+        lib.oracle_commit.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, i32, i32, P, P, P]
+        lib.oracle_commit.restype = i32
+        lib.oracle_ancestor_matrix.argtypes = [P, i32, P]
+        lib.oracle_ancestor_matrix.restype = None
+        lib.oracle_upcast.argtypes = [i32, ctypes.c_uint16]
+        lib.oracle_upcast.restype = f64
+        _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def upcast(dtype: int, bits: int) -> float:
+    """Exact value of one fp16 (dtype 0) or bf16 (dtype 1) bit pattern."""
+    return _load().oracle_upcast(dtype, bits)
+
+
+def ancestor_matrix(parent) -> np.ndarray:
+    """uint8 [N][N]: 1 iff node j is node i or an ancestor of i."""
+    parent = _c(parent, np.int32)
+    n = parent.shape[0]
+    out = np.zeros((n, n), dtype=np.uint8)
+    _load().oracle_ancestor_matrix(_p(parent), n, _p(out))
+    return out
+
+
+def verify_attn(inp: dict, dtype: int, scale: float | None = None, rows=None, threads: int | None = None):
+    """Tree-verify attention in fp64 with an explicit mask.
+
+    ``inp`` holds the generator's arrays.  ``rows`` (flat ids (b*N+i)*Hq+h)
+    selects a subset; default all rows.  Returns (out [rows][D] fp64,
+    lse [rows] natural log)."""
+    q = _c(inp["q"], np.uint16)
+    B, N, Hq, D = q.shape
+    k_pool = _c(inp["k_pool"], np.uint16)
+    v_pool = _c(inp["v_pool"], np.uint16)
+    num_pages, Hkv, P, _ = k_pool.shape
+    pt = _c(inp["page_table"], np.int32)
+    ctx = _c(inp["ctx_len"], np.int32)
+    kt = _c(inp["k_tree"], np.uint16)
+    vt = _c(inp["v_tree"], np.uint16)
+    par = _c(inp["parent"], np.int32)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    if rows is None:
+        rows_arr = None
+        n_rows = B * N * Hq
+    else:
+        rows_arr = _c(rows, np.int32)
+        n_rows = rows_arr.shape[0]
+    out = np.zeros((n_rows, D), dtype=np.float64)
+    lse = np.zeros(n_rows, dtype=np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = _load().oracle_verify_attn(dtype, B, N, Hq, Hkv, D, P, float(scale), _p(q), _p(k_pool), _p(v_pool),
+                                    num_pages, _p(pt), pt.shape[1], _p(ctx), _p(kt), _p(vt), _p(par),
+                                    None if rows_arr is None else _p(rows_arr), n_rows, _p(out), _p(lse),
+                                    int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_verify_attn failed ({rc})")
+    return out, lse
+
+
+def argmax(logits) -> np.ndarray:
+    """First index of the maximum of each row of a 2-D float32 array."""
+    x = _c(logits, np.float32)
+    x2 = x.reshape(-1, x.shape[-1])
+    out = np.empty(x2.shape[0], dtype=np.int32)
+    _load().oracle_argmax(_p(x2), x2.shape[0], x2.shape[1], x2.shape[1], _p(out))
+    return out.reshape(x.shape[:-1])
+
+
+def accept(parent, draft, argmax_idx):
+    """Greedy acceptance; returns (acc_nodes [B][N] (-1 padded), acc_len [B], bonus [B])."""
+    par = _c(parent, np.int32)
+    dr = _c(draft, np.int32)
+    am = _c(argmax_idx, np.int32)
+    B, N = par.shape
+    acc = np.full((B, N), -1, dtype=np.int32)
+    alen = np.zeros(B, dtype=np.int32)
+    bonus = np.zeros(B, dtype=np.int32)
+    rc = _load().oracle_accept(B, N, _p(par), _p(dr), _p(am), _p(acc), _p(alen), _p(bonus))
+    if rc != 0:
+        raise ValueError("parent array is not in topological order")
+    return acc, alen, bonus
+
+
+def commit(inp: dict, acc_nodes, acc_len):
+    """Returns (k_pool, v_pool, ctx_len) after committing, on copies."""
+    k_pool = np.array(inp["k_pool"], dtype=np.uint16, copy=True)
+    v_pool = np.array(inp["v_pool"], dtype=np.uint16, copy=True)
+    ctx = np.array(inp["ctx_len"], dtype=np.int32, copy=True)
+    kt = _c(inp["k_tree"], np.uint16)
+    vt = _c(inp["v_tree"], np.uint16)
+    pt = _c(inp["page_table"], np.int32)
+    acc = _c(acc_nodes, np.int32)
+    alen = _c(acc_len, np.int32)
+    B, N, Hkv, D = kt.shape
+    rc = _load().oracle_commit(B, N, Hkv, D, k_pool.shape[2], _p(kt), _p(vt), _p(acc), _p(alen), _p(pt),
+                               pt.shape[1], k_pool.shape[0], _p(ctx), _p(k_pool), _p(v_pool))
+    if rc != 0:
+        raise ValueError("commit touched a page outside the pool")
+    return k_pool, v_pool, ctx

@@ -1,0 +1,369 @@
+"""Pins for the fp64 oracle against facts it does not compute itself: values
+worked by hand, closed forms, independent textbook routines (numpy / torch
+CPU), exhaustive checks of the 16-bit upcasts, and brute-force enumeration of
+root paths.  Each pin targets a mistake that could plausibly hide in the
+oracle (a dropped mask term, a wrong GQA head, a wrong page index, a reversed
+path, a wrong tie rule)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+
+# ---------------------------------------------------------------- helpers
+
+def _bits(vals, dtype):
+    a = np.asarray(vals, dtype=np.float32)
+    return W.f32_to_bf16_bits(a) if dtype == W.BF16 else W.f32_to_f16_bits(a)
+
+
+def _hand_tree_inputs(dtype=W.F16):
+    """Hand example: D=1, one head, q=1, one committed key k=0 (v=0), tree
+    parent=[-1,0,0], tree keys [1, 0, 2], tree values [4, 8, -4], scale ln 2,
+    so each visible key's weight is 2**k."""
+    q = np.array([[[[1.0]], [[1.0]], [[1.0]]]], dtype=np.float32)  # [1][3][1][1]
+    kp = np.zeros((1, 1, 64, 1), np.float32)
+    vp = np.zeros((1, 1, 64, 1), np.float32)
+    return dict(q=_bits(q, dtype), k_pool=_bits(kp, dtype), v_pool=_bits(vp, dtype),
+                page_table=np.array([[0]], np.int32), ctx_len=np.array([1], np.int32),
+                k_tree=_bits(np.array([1.0, 0.0, 2.0]).reshape(1, 3, 1, 1), dtype),
+                v_tree=_bits(np.array([4.0, 8.0, -4.0]).reshape(1, 3, 1, 1), dtype),
+                parent=np.array([[-1, 0, 0]], np.int32))
+
+
+def _gather_logical(inp, b, g, dtype_id):
+    """K, V of sequence b / kv-head g in logical order, fp64, via numpy indexing."""
+    L = int(inp["ctx_len"][b])
+    pos = np.arange(L)
+    pages = inp["page_table"][b][pos // 64]
+    slots = pos % 64
+    k = inp["k_pool"][pages, g, slots, :]
+    v = inp["v_pool"][pages, g, slots, :]
+    return _to64(k, dtype_id), _to64(v, dtype_id)
+
+
+def _to64(bits, dtype_id):
+    bits = np.asarray(bits, dtype=np.uint16)
+    if dtype_id == oracle.BF16:
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return bits.view(np.float16).astype(np.float64)
+
+
+# ---------------------------------------------------------------- upcasts
+
+def test_upcast_bf16_exhaustive():
+    lib_vals = np.array([oracle.upcast(oracle.BF16, b) for b in range(65536)])
+    ref = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(lib_vals), nan)
+    assert np.array_equal(lib_vals[~nan], ref[~nan])
+
+
+def test_upcast_f16_exhaustive():
+    lib_vals = np.array([oracle.upcast(oracle.F16, b) for b in range(65536)])
+    ref = np.arange(65536, dtype=np.uint16).view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(lib_vals), nan)
+    assert np.array_equal(lib_vals[~nan], ref[~nan])
+    assert oracle.upcast(oracle.F16, 0x0001) == 2.0 ** -24
+    assert oracle.upcast(oracle.F16, 0x7BFF) == 65504.0
+
+
+# ---------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+def test_attention_hand_example(dtype):
+    inp = _hand_tree_inputs(dtype)
+    did = oracle.BF16 if dtype == W.BF16 else oracle.F16
+    out, lse = oracle.verify_attn(inp, did, scale=math.log(2.0), threads=1)
+    # node 0 sees {prefix 1, n0 2}: 8/3; node 1 sees {1, 2, 1}: 16/4;
+    # node 2 sees {1, 2, 4}: (8 - 16)/7
+    np.testing.assert_allclose(out[:, 0], [8.0 / 3.0, 4.0, -8.0 / 7.0], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(lse, [math.log(3.0), math.log(4.0), math.log(7.0)], rtol=1e-13)
+
+
+def test_attention_equal_keys_is_mean_of_visible_values():
+    cfg = W.TINY.replace(ctx=(200,), N=6, Hq=4, Hkv=2, D=16)
+    inp = W.generate(cfg, seed=3, fill_unused="nan")
+    inp["k_pool"][:] = W.f32_to_f16_bits(np.full(1, 0.5))[0]
+    inp["k_tree"][:] = inp["k_pool"].flat[0]
+    out, _ = oracle.verify_attn(inp, oracle.F16, threads=2)
+    out = out.reshape(1, cfg.N, cfg.Hq, cfg.D)
+    for h in range(cfg.Hq):
+        g = h // (cfg.Hq // cfg.Hkv)
+        _, vpre = _gather_logical(inp, 0, g, oracle.F16)
+        vt = _to64(inp["v_tree"][0, :, g, :], oracle.F16)
+        for i in range(cfg.N):
+            path, c = [], i
+            while c >= 0:
+                path.append(c)
+                c = int(inp["parent"][0, c])
+            vis = np.concatenate([vpre, vt[path]], axis=0)
+            np.testing.assert_allclose(out[0, i, h], vis.mean(axis=0), rtol=1e-11, atol=1e-13)
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+def test_one_node_tree_is_plain_decode(dtype):
+    cfg = W.VerifyConfig("decode", ctx=(300, 77), Hq=6, Hkv=2, D=32, dtype=dtype, N=1,
+                         paged="permuted", spare_pages=5, vocab=64)
+    inp = W.generate(cfg, seed=11)
+    did = oracle.BF16 if dtype == W.BF16 else oracle.F16
+    scale = 1.0 / math.sqrt(cfg.D)
+    out, lse = oracle.verify_attn(inp, did, threads=2)
+    out = out.reshape(cfg.B, cfg.Hq, cfg.D)
+    for b in range(cfg.B):
+        for h in range(cfg.Hq):
+            g = h // cfg.G
+            k, v = _gather_logical(inp, b, g, did)
+            k = np.vstack([k, _to64(inp["k_tree"][b, 0, g], did)[None]])
+            v = np.vstack([v, _to64(inp["v_tree"][b, 0, g], did)[None]])
+            q = _to64(inp["q"][b, 0, h], did)
+            logits = (k @ q) * scale
+            w = np.exp(logits - logits.max())
+            ref = (w / w.sum()) @ v
+            np.testing.assert_allclose(out[b, h], ref, rtol=1e-11, atol=1e-14)
+            assert abs(lse[b * cfg.Hq + h] - (logits.max() + np.log(w.sum()))) < 1e-11
+
+
+def test_chain_tree_is_causal_attention():
+    torch = pytest.importorskip("torch")
+    cfg = W.VerifyConfig("chain", ctx=(130,), Hq=4, Hkv=1, D=16, dtype=W.BF16, N=9, tree="chain",
+                         vocab=64, paged="permuted", spare_pages=3)
+    inp = W.generate(cfg, seed=5)
+    out, _ = oracle.verify_attn(inp, oracle.BF16, threads=2)
+    out = out.reshape(cfg.N, cfg.Hq, cfg.D)
+    k, v = _gather_logical(inp, 0, 0, oracle.BF16)
+    kt = _to64(inp["k_tree"][0, :, 0, :], oracle.BF16)
+    vt = _to64(inp["v_tree"][0, :, 0, :], oracle.BF16)
+    K = torch.from_numpy(np.vstack([k, kt]))[None, None].expand(1, cfg.Hq, -1, -1)
+    V = torch.from_numpy(np.vstack([v, vt]))[None, None].expand(1, cfg.Hq, -1, -1)
+    Q = torch.from_numpy(_to64(inp["q"][0], oracle.BF16)).permute(1, 0, 2)[None]  # [1][Hq][N][D]
+    L = cfg.ctx[0]
+    mask = torch.ones(cfg.N, L + cfg.N, dtype=torch.bool)
+    mask[:, L:] = torch.tril(torch.ones(cfg.N, cfg.N, dtype=torch.bool))
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask)[0].permute(1, 0, 2)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-10, atol=1e-13)
+
+
+def test_non_ancestor_tree_kv_does_not_change_output():
+    cfg = W.TINY.replace(ctx=(150,), N=10, D=16)
+    inp = W.generate(cfg, seed=8)
+    base, _ = oracle.verify_attn(inp, oracle.F16, threads=2)
+    anc = oracle.ancestor_matrix(inp["parent"][0])
+    rng = np.random.default_rng(0)
+    i = 7
+    non = [j for j in range(cfg.N) if not anc[i, j]]
+    assert non, "test tree should have non-ancestors of node 7"
+    pert = {k: v.copy() for k, v in inp.items()}
+    pert["k_tree"][0, non] = rng.integers(0, 0x3C00, size=pert["k_tree"][0, non].shape, dtype=np.uint16)
+    pert["v_tree"][0, non] = rng.integers(0, 0x3C00, size=pert["v_tree"][0, non].shape, dtype=np.uint16)
+    out, _ = oracle.verify_attn(pert, oracle.F16, threads=2)
+    rows = slice(i * cfg.Hq, (i + 1) * cfg.Hq)
+    assert np.array_equal(out[rows], base[rows])
+    # and nodes that do see a perturbed node change
+    seen = [r for r in range(cfg.N) if any(anc[r, j] for j in non)]
+    assert any(not np.array_equal(out[r * cfg.Hq:(r + 1) * cfg.Hq], base[r * cfg.Hq:(r + 1) * cfg.Hq])
+               for r in seen)
+
+
+def test_page_relabelling_is_invisible():
+    cfg = W.TINY.replace(ctx=(333, 64, 5), N=5, D=16, paged="permuted", spare_pages=4)
+    inp = W.generate(cfg, seed=9, fill_unused="random")
+    base, _ = oracle.verify_attn(inp, oracle.F16, threads=2)
+    perm = np.random.default_rng(1).permutation(inp["k_pool"].shape[0])
+    moved = dict(inp)
+    moved["k_pool"] = np.empty_like(inp["k_pool"])
+    moved["v_pool"] = np.empty_like(inp["v_pool"])
+    moved["k_pool"][perm] = inp["k_pool"]
+    moved["v_pool"][perm] = inp["v_pool"]
+    pt = inp["page_table"].copy()
+    pt[pt >= 0] = perm[pt[pt >= 0]]
+    moved["page_table"] = pt
+    out, _ = oracle.verify_attn(moved, oracle.F16, threads=2)
+    assert np.array_equal(out, base)
+
+
+def test_empty_prefix_sees_only_tree():
+    inp = _hand_tree_inputs()
+    inp["ctx_len"] = np.array([0], np.int32)
+    out, _ = oracle.verify_attn(inp, oracle.F16, scale=math.log(2.0), threads=1)
+    # node 0 sees only itself: 4; node 1 {2,1}: (8+8)/3; node 2 {2,4}: (8-16)/6
+    np.testing.assert_allclose(out[:, 0], [4.0, 16.0 / 3.0, -8.0 / 6.0], rtol=1e-13)
+
+
+def test_ancestor_matrix_hand():
+    anc = oracle.ancestor_matrix(np.array([-1, 0, 0, 1, 3], np.int32))
+    exp = np.array([[1, 0, 0, 0, 0],
+                    [1, 1, 0, 0, 0],
+                    [1, 0, 1, 0, 0],
+                    [1, 1, 0, 1, 0],
+                    [1, 1, 0, 1, 1]], np.uint8)
+    assert np.array_equal(anc, exp)
+
+
+# ---------------------------------------------------------------- argmax
+
+def test_argmax_matches_numpy_first_index_with_ties_and_zeros():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((64, 1000)).astype(np.float32)
+    x[1, 10] = x[1, 500] = 99.0            # tie: lowest index wins
+    x[2, :] = 0.0
+    x[2, 3] = -0.0                         # -0.0 ties +0.0
+    x[3, :] = -0.0
+    x[3, 7] = 0.0
+    x[4, -1] = 50.0                        # maximum at the last index
+    x[5, :] = -np.inf
+    x[6, :] = 7.0
+    assert np.array_equal(oracle.argmax(x), np.argmax(x, axis=1).astype(np.int32))
+    assert oracle.argmax(x)[1] == 10
+    assert oracle.argmax(x)[2] == 0
+
+
+# ---------------------------------------------------------------- acceptance
+
+def _paths_top_down(parent):
+    """Every root path, built from the root downward over child lists."""
+    n = len(parent)
+    kids = {-1: []}
+    for i in range(n):
+        kids.setdefault(int(parent[i]), []).append(i)
+    out, stack = [], [[]]
+    while stack:
+        path = stack.pop()
+        last = path[-1] if path else -1
+        for c in kids.get(last, []):
+            stack.append(path + [c])
+            out.append(path + [c])
+    return out
+
+
+def _brute_accept(parent, draft, am):
+    best = []
+    for path in _paths_top_down(parent):
+        rows = [0] + [c + 1 for c in path[:-1]]
+        if all(draft[c] == am[r] for c, r in zip(path, rows)):
+            if len(path) > len(best) or (len(path) == len(best) and path[-1] < best[-1]):
+                best = path
+    bonus = am[best[-1] + 1] if best else am[0]
+    return best, bonus
+
+
+def test_accept_hand_example():
+    acc, alen, bonus = oracle.accept(np.array([[-1, 0, 0]]), np.array([[5, 7, 9]]), np.array([[5, 9, 3, 4]]))
+    assert alen[0] == 2 and list(acc[0, :2]) == [0, 2] and bonus[0] == 4
+    assert acc[0, 2] == -1
+    acc, alen, bonus = oracle.accept(np.array([[-1, 0, 0]]), np.array([[6, 7, 9]]), np.array([[5, 9, 3, 4]]))
+    assert alen[0] == 0 and bonus[0] == 5
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7])
+def test_accept_brute_force_random_trees(n):
+    rng = np.random.default_rng(100 + n)
+    B = 10000
+    vocab = 3  # tiny vocabulary: many matches, duplicate sibling tokens included
+    parent = np.zeros((B, n), np.int32)
+    for b in range(B):
+        parent[b, 0] = -1 if rng.random() < 0.8 else -1
+        for i in range(1, n):
+            parent[b, i] = rng.integers(-1, i)
+    draft = rng.integers(0, vocab, size=(B, n)).astype(np.int32)
+    am = rng.integers(0, vocab, size=(B, n + 1)).astype(np.int32)
+    acc, alen, bonus = oracle.accept(parent, draft, am)
+    for b in range(0, B, 7 if n > 5 else 1):
+        path, bo = _brute_accept(parent[b], draft[b], am[b])
+        assert alen[b] == len(path)
+        assert list(acc[b, :alen[b]]) == path
+        assert bonus[b] == bo
+
+
+def test_accept_greedy_walk_for_distinct_siblings():
+    """With distinct sibling tokens the deepest matching path is the greedy walk
+    down from the root."""
+    cfg = W.GQA27B_32K.replace(ctx=(64,), vocab=50, N=22)
+    for seed in range(200):
+        rng = np.random.default_rng(seed)
+        par = W.random_parents(rng, cfg.N, "random", 4)
+        dr = W.draft_tokens(rng, par, cfg.vocab)
+        lg = W.planted_logits(rng, par, dr, cfg.vocab, 0.9)
+        am = np.argmax(lg, axis=1).astype(np.int32)
+        acc, alen, bonus = oracle.accept(par[None], dr[None], am[None])
+        walk, cur = [], -1
+        while True:
+            t = am[cur + 1]
+            nxt = [c for c in range(cfg.N) if par[c] == cur and dr[c] == t]
+            if not nxt:
+                break
+            cur = nxt[0]
+            walk.append(cur)
+        assert list(acc[0, :alen[0]]) == walk
+        assert bonus[0] == am[walk[-1] + 1 if walk else 0]
+
+
+def test_accept_chain_full_plant_accepts_everything():
+    n = 12
+    par = np.arange(-1, n - 1, dtype=np.int32)[None]
+    dr = np.arange(100, 100 + n, dtype=np.int32)[None]
+    am = np.concatenate([dr[0], [7]]).astype(np.int32)[None]
+    acc, alen, bonus = oracle.accept(par, dr, am)
+    assert alen[0] == n and list(acc[0]) == list(range(n)) and bonus[0] == 7
+
+
+def test_accept_result_is_prefix_closed_root_path():
+    rng = np.random.default_rng(4)
+    for _ in range(300):
+        n = int(rng.integers(1, 40))
+        par = W.random_parents(rng, n, "random", 4)
+        dr = W.draft_tokens(rng, par, 6)
+        am = rng.integers(0, 6, size=n + 1).astype(np.int32)
+        acc, alen, _ = oracle.accept(par[None], dr[None], am[None])
+        path = list(acc[0, :alen[0]])
+        prev = -1
+        for c in path:
+            assert par[c] == prev
+            prev = c
+        assert all(x == -1 for x in acc[0, alen[0]:])
+
+
+def test_accept_rejects_non_topological_parent():
+    with pytest.raises(ValueError):
+        oracle.accept(np.array([[-1, 2, 0]]), np.array([[1, 2, 3]]), np.array([[1, 2, 3, 4]]))
+
+
+# ---------------------------------------------------------------- commit
+
+def test_commit_hand_example():
+    cfg = W.TINY.replace(ctx=(64,), N=3, Hq=2, Hkv=1, D=8, paged="permuted", spare_pages=2)
+    inp = W.generate(cfg, seed=1)
+    acc = np.array([[0, 2, -1]], np.int32)
+    kp, vp, ctx = oracle.commit(inp, acc, np.array([2], np.int32))
+    page = inp["page_table"][0, 1]
+    assert ctx[0] == 66
+    assert np.array_equal(kp[page, 0, 0], inp["k_tree"][0, 0, 0])
+    assert np.array_equal(kp[page, 0, 1], inp["k_tree"][0, 2, 0])
+    assert np.array_equal(vp[page, 0, 1], inp["v_tree"][0, 2, 0])
+    # every other byte is unchanged
+    mask = np.ones(kp.shape[:3], bool)
+    mask[page, 0, 0:2] = False
+    assert np.array_equal(kp[mask], inp["k_pool"][mask])
+    assert np.array_equal(vp[mask], inp["v_pool"][mask])
+
+
+def test_commit_then_verify_equals_extended_prefix():
+    """After committing the accepted path, the committed prefix attends exactly
+    like a prefix that had those tokens all along."""
+    cfg = W.TINY.replace(ctx=(70, 128), N=6, D=16, paged="permuted", spare_pages=3)
+    inp = W.generate(cfg, seed=12)
+    acc = np.full((2, 6), -1, np.int32)
+    acc[0, :2] = [0, 3]
+    acc[1, :1] = [0]
+    kp, vp, ctx = oracle.commit(inp, acc, np.array([2, 1], np.int32))
+    for b in range(2):
+        L = int(inp["ctx_len"][b])
+        pos = np.arange(L, int(ctx[b]))
+        pages = inp["page_table"][b][pos // 64]
+        got = kp[pages, :, pos % 64, :]
+        want = inp["k_tree"][b, acc[b, :len(pos)]]
+        assert np.array_equal(got, want)

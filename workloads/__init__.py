@@ -1,0 +1,284 @@
+"""Seeded synthetic inputs for the DDTree verify step.
+
+This module only draws random numbers and lays them out; it holds none of the
+verify step's arithmetic (no masks, softmax, argmax, acceptance or copies).
+Both the CUDA path and the fp64 oracle consume exactly what it returns.
+
+Workloads follow the shapes the Lucebox pages describe for DDTree verification
+("Lucebox Hub", section "Speculative decoding layer (DFlash / DDTree / DSpark)";
+"Paged attention + continuous batching" for D=256 GQA; the pytorch.kr Lucebox
+introduction, section "Installation and running", for budgets 22 / 40 and
+temperature 0; section "Lucebox optimization components" for 64-token KV
+chunks).  Every tensor is synthetic:
+
+* Q, committed K/V and tree K/V are N(0, 1) rounded to fp16 or bf16 (RNE).
+* The tree: node 0's parent is the root (-1); node i > 0 takes its parent
+  uniformly among earlier nodes (optionally only those with fewer than
+  ``branch_cap`` children).  A "chain" tree has parent[i] = i - 1.
+* Draft tokens are uniform in [0, V), resampled so siblings are distinct.
+* Logits are N(0, 1) fp32 with shape [B][N + 1][V]; row 0 belongs to the
+  root (the last committed token), row j + 1 to node j.  For each parent row
+  with at least one child, with probability ``p_plant`` one uniformly chosen
+  child c gets ``logits[row][draft[c]] = row.max() + 1``.
+* The K/V pool is [num_pages][Hkv][64][D]; a sequence owns
+  ceil((L_b + N) / 64) pages, the tail ones pre-reserved ("newly allocated")
+  for the tree positions.  Pages are either laid out in order (identity page
+  table) or placed by a seeded random permutation of the whole pool, which also
+  holds ``spare_pages`` unused pages.  Pool slots that hold no committed token
+  are filled per ``fill_unused`` ('nan' makes any stray read visible).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import numpy as np
+
+PAGE = 64
+
+F16 = "f16"
+BF16 = "bf16"
+
+
+@dataclasses.dataclass(frozen=True)
+class VerifyConfig:
+    name: str
+    ctx: tuple                # committed length L_b per sequence
+    Hq: int
+    Hkv: int
+    D: int
+    dtype: str                # 'f16' | 'bf16'
+    N: int                    # tree budget (nodes)
+    tree: str = "random"      # 'random' | 'chain'
+    branch_cap: Optional[int] = None
+    vocab: int = 4096
+    p_plant: float = 0.7
+    paged: str = "identity"   # 'identity' | 'permuted'
+    spare_pages: int = 0
+
+    @property
+    def B(self) -> int:
+        return len(self.ctx)
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    def kv_bytes(self) -> int:
+        """Bytes of committed K and V one verify pass must stream."""
+        return sum(self.ctx) * self.Hkv * self.D * 2 * 2
+
+    def replace(self, **kw) -> "VerifyConfig":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads, in order: tiny, 27B-class 32K / budget 22, 128K / budget
+# 40, 256K paged / budget 22, and the concurrent sweep (see ``sweep_points``).
+TINY = VerifyConfig("tiny-1k-b8", ctx=(1024,), Hq=8, Hkv=2, D=128, dtype=F16, N=8,
+                    tree="random", branch_cap=None, vocab=4096, p_plant=0.7)
+GQA27B_32K = VerifyConfig("gqa27b-32k-b22", ctx=(32768,), Hq=24, Hkv=4, D=256, dtype=BF16,
+                          N=22, tree="random", branch_cap=4, vocab=151936, p_plant=0.7)
+LONG_128K = VerifyConfig("long-128k-b40", ctx=(131072,), Hq=24, Hkv=4, D=256, dtype=BF16,
+                         N=40, tree="random", branch_cap=4, vocab=151936, p_plant=0.6)
+PAGED_256K = VerifyConfig("paged-256k-b22", ctx=(262144,), Hq=24, Hkv=4, D=256, dtype=BF16,
+                          N=22, tree="random", branch_cap=4, vocab=151936, p_plant=0.7,
+                          paged="permuted", spare_pages=64)
+# Headline workload: one sequence of the concurrent sweep, 131,072 committed
+# tokens at budget 22 in a permuted paged pool.
+HEADLINE_128K_B22 = VerifyConfig("verify-128k-b22", ctx=(131072,), Hq=24, Hkv=4, D=256,
+                                 dtype=BF16, N=22, tree="random", branch_cap=4,
+                                 vocab=151936, p_plant=0.7, paged="permuted",
+                                 spare_pages=64)
+
+SWEEP_CTX = (4096, 32768, 131072, 262144)
+SWEEP_BUDGETS = (1, 8, 22, 40, 64)
+SWEEP_P = (0.3, 0.7, 0.95)
+
+
+def sweep_points():
+    """The concurrent sweep: 4 sequences in one permuted pool; budgets x tree
+    shapes x planting probabilities (budget 1 is plain decode: chain == tree)."""
+    pts = []
+    for n in SWEEP_BUDGETS:
+        for shape in (("chain",) if n == 1 else ("chain", "random")):
+            for p in SWEEP_P:
+                pts.append(VerifyConfig(f"sweep-b{n}-{shape}-p{p}", ctx=SWEEP_CTX, Hq=24, Hkv=4,
+                                        D=256, dtype=BF16, N=n, tree=shape, branch_cap=4,
+                                        vocab=151936, p_plant=p, paged="permuted",
+                                        spare_pages=64))
+    return pts
+
+
+CONFIGS = {c.name: c for c in (TINY, GQA27B_32K, LONG_128K, PAGED_256K, HEADLINE_128K_B22)}
+
+
+# ----------------------------------------------------------------------------
+# rounding of random draws to the storage dtype (input preparation only)
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest even); return raw bits."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    return ((b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def _normal_bits(rng: np.random.Generator, shape, dtype: str, chunk: int = 1 << 24) -> np.ndarray:
+    total = int(np.prod(shape))
+    out = np.empty(total, dtype=np.uint16)
+    conv = f32_to_bf16_bits if dtype == BF16 else f32_to_f16_bits
+    for s in range(0, total, chunk):
+        e = min(total, s + chunk)
+        out[s:e] = conv(rng.standard_normal(e - s, dtype=np.float32))
+    return out.reshape(shape)
+
+
+NAN_BITS = {BF16: 0x7FC0, F16: 0x7E00}
+
+
+# ----------------------------------------------------------------------------
+# trees, draft tokens and logits
+
+def random_parents(rng: np.random.Generator, n: int, shape: str, cap: Optional[int]) -> np.ndarray:
+    parent = np.empty(n, dtype=np.int32)
+    if n == 0:
+        return parent
+    parent[0] = -1
+    if shape == "chain":
+        parent[1:] = np.arange(n - 1, dtype=np.int32)
+        return parent
+    children = np.zeros(n, dtype=np.int64)
+    for i in range(1, n):
+        if cap is None:
+            cand = np.arange(i)
+        else:
+            cand = np.nonzero(children[:i] < cap)[0]
+        p = int(cand[rng.integers(0, len(cand))])
+        parent[i] = p
+        children[p] += 1
+    return parent
+
+
+def draft_tokens(rng: np.random.Generator, parent: np.ndarray, vocab: int) -> np.ndarray:
+    n = len(parent)
+    draft = np.empty(n, dtype=np.int32)
+    used = {}
+    for i in range(n):
+        sib = used.setdefault(int(parent[i]), set())
+        t = int(rng.integers(0, vocab))
+        while t in sib:
+            t = int(rng.integers(0, vocab))
+        sib.add(t)
+        draft[i] = t
+    return draft
+
+
+def planted_logits(rng: np.random.Generator, parent: np.ndarray, draft: np.ndarray,
+                   vocab: int, p: float) -> np.ndarray:
+    n = len(parent)
+    logits = rng.standard_normal((n + 1, vocab), dtype=np.float32)
+    kids = {}
+    for i in range(n):
+        kids.setdefault(int(parent[i]), []).append(i)
+    for par in sorted(kids):
+        row = par + 1
+        if rng.random() < p:
+            c = kids[par][int(rng.integers(0, len(kids[par])))]
+            logits[row, draft[c]] = logits[row].max() + np.float32(1.0)
+    return logits
+
+
+# ----------------------------------------------------------------------------
+# the whole input set
+
+def pages_needed(L: int, N: int) -> int:
+    return -(-(L + N) // PAGE)
+
+
+def generate(cfg: VerifyConfig, seed: int = 0, fill_unused: str = "nan",
+             with_logits: bool = True) -> dict:
+    """Draw one verify step's inputs for ``cfg``.
+
+    Returns numpy arrays (16-bit payloads as raw uint16 bits):
+      q [B][N][Hq][D], k_pool / v_pool [num_pages][Hkv][64][D],
+      page_table int32 [B][max_pages] (-1 = unassigned), ctx_len int32 [B],
+      k_tree / v_tree [B][N][Hkv][D], parent / draft int32 [B][N],
+      logits float32 [B][N + 1][V].
+    """
+    rng = np.random.default_rng(np.random.SeedSequence([seed, _name_key(cfg.name)]))
+    B, N, Hq, Hkv, D = cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D
+    need = [pages_needed(L, N) for L in cfg.ctx]
+    num_pages = sum(need) + cfg.spare_pages
+    max_pages = max(need)
+    if cfg.paged == "permuted":
+        order = rng.permutation(num_pages).astype(np.int32)
+    else:
+        order = np.arange(num_pages, dtype=np.int32)
+    page_table = np.full((B, max_pages), -1, dtype=np.int32)
+    at = 0
+    for b in range(B):
+        page_table[b, :need[b]] = order[at:at + need[b]]
+        at += need[b]
+
+    q = _normal_bits(rng, (B, N, Hq, D), cfg.dtype)
+    k_tree = _normal_bits(rng, (B, N, Hkv, D), cfg.dtype)
+    v_tree = _normal_bits(rng, (B, N, Hkv, D), cfg.dtype)
+
+    k_pool = np.empty((num_pages, Hkv, PAGE, D), dtype=np.uint16)
+    v_pool = np.empty((num_pages, Hkv, PAGE, D), dtype=np.uint16)
+    if fill_unused == "nan":
+        k_pool.fill(NAN_BITS[cfg.dtype])
+        v_pool.fill(NAN_BITS[cfg.dtype])
+    elif fill_unused == "zero":
+        k_pool.fill(0)
+        v_pool.fill(0)
+    elif fill_unused != "random":
+        raise ValueError(fill_unused)
+    for b, L in enumerate(cfg.ctx):
+        full = L // PAGE
+        for which in (k_pool, v_pool):
+            if fill_unused == "random":
+                which[page_table[b, :need[b]]] = _normal_bits(rng, (need[b], Hkv, PAGE, D), cfg.dtype)
+            if full:
+                which[page_table[b, :full]] = _normal_bits(rng, (full, Hkv, PAGE, D), cfg.dtype)
+            rem = L - full * PAGE
+            if rem:
+                which[page_table[b, full], :, :rem, :] = _normal_bits(rng, (Hkv, rem, D), cfg.dtype)
+    if fill_unused == "random":
+        spare = order[at:]
+        for which in (k_pool, v_pool):
+            which[spare] = _normal_bits(rng, (len(spare), Hkv, PAGE, D), cfg.dtype)
+
+    parent = np.empty((B, N), dtype=np.int32)
+    draft = np.empty((B, N), dtype=np.int32)
+    logits = np.empty((B, N + 1, cfg.vocab), dtype=np.float32) if with_logits else None
+    for b in range(B):
+        parent[b] = random_parents(rng, N, cfg.tree, cfg.branch_cap)
+        draft[b] = draft_tokens(rng, parent[b], cfg.vocab)
+        if with_logits:
+            logits[b] = planted_logits(rng, parent[b], draft[b], cfg.vocab, cfg.p_plant)
+    return dict(q=q, k_pool=k_pool, v_pool=v_pool, page_table=page_table,
+                ctx_len=np.asarray(cfg.ctx, dtype=np.int32), k_tree=k_tree, v_tree=v_tree,
+                parent=parent, draft=draft, logits=logits)
+
+
+def _name_key(name: str) -> int:
+    h = 0
+    for ch in name.encode():
+        h = (h * 131 + ch) % (1 << 31)
+    return h
+
+
+def sample_rows(cfg: VerifyConfig, count: int, seed: int = 1) -> np.ndarray:
+    """Seeded sample of flat output rows (b * N + i) * Hq + h, always including
+    the first and last row."""
+    total = cfg.B * cfg.N * cfg.Hq
+    rng = np.random.default_rng(seed)
+    if count >= total:
+        return np.arange(total, dtype=np.int32)
+    pick = set(rng.choice(total, size=max(0, count - 2), replace=False).tolist())
+    pick.update({0, total - 1})
+    return np.array(sorted(pick), dtype=np.int32)
