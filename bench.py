@@ -1,0 +1,400 @@
+#!/usr/bin/env python
+"""Benchmark of the DDTree verify step on GB300.
+
+One step = the whole hot path over one batch: ancestor masks, tree-verify
+attention over the paged committed prefix, per-node vocab argmax, greedy
+acceptance and the commit copy, all through the C-ABI library.  Default
+workload: one sequence with 131,072 committed tokens, 24 query / 4 KV heads,
+head dim 256, bf16, a 22-node random tree (branching <= 4), 151,936-entry
+vocabulary, 64-token pages placed by a random permutation.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  ``value`` is algorithmic bytes of the step
+(committed K/V, queries, tree K/V, outputs, page table, logits, commit copy)
+per second; under torchrun every rank runs its own sequence (weak scaling)
+and the time is the maximum over ranks.  ``--impl reference`` times the fp64
+CPU oracle on the host cores on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "tree-verify HBM GB/s (% of peak) and verify steps/s, budget 22 @128K ctx"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+KERNELS_PER_STEP = 6  # anc mask, prefix attention, merge, argmax, accept, commit
+
+
+# ----------------------------------------------------------------------------- bytes
+
+def attn_bytes(cfg: W.VerifyConfig) -> int:
+    """Algorithmic bytes of one lucetree_verify_attn call."""
+    s = 2
+    kv = sum(cfg.ctx) * cfg.Hkv * cfg.D * 2 * s
+    q = cfg.B * cfg.N * cfg.Hq * cfg.D * s
+    out = cfg.B * cfg.N * cfg.Hq * (cfg.D + 1) * 4
+    tree = cfg.B * cfg.N * cfg.Hkv * cfg.D * 2 * s
+    pt = sum(-(-L // 64) for L in cfg.ctx) * 4
+    anc = cfg.B * cfg.N * 8
+    return kv + q + out + tree + pt + anc
+
+
+def step_bytes(cfg: W.VerifyConfig, accepted_total: int) -> int:
+    logits = cfg.B * (cfg.N + 1) * cfg.vocab * 4
+    commit = 2 * accepted_total * cfg.Hkv * cfg.D * 2 * 2
+    small = cfg.B * cfg.N * 4 * 6
+    return attn_bytes(cfg) + logits + commit + small
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def prefix_kernel_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_tree_ddtree_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.startswith("attn_prefix") or fn == "internal.cuh":
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch of the prefix kernel from the committed ncu summary,
+    or None when the kernel source changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "attn_prefix_verify-128k-b22.md")
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s*\(source sha\s*([0-9a-f]+)\)", txt)
+    if not m or m.group(2) != prefix_kernel_sha():
+        return None
+    return int(m.group(1))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a scalar over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_step_sample(inp, cfg, rows, threads):
+    """One bounded oracle step: sampled attention rows, then argmax, acceptance
+    and commit of the whole batch.  Returns (attention seconds, rest seconds)."""
+    import oracle
+    did = oracle.BF16 if cfg.dtype == W.BF16 else oracle.F16
+    t0 = time.perf_counter()
+    oracle.verify_attn(inp, did, rows=rows, threads=threads)
+    t1 = time.perf_counter()
+    am = oracle.argmax(inp["logits"])
+    acc, alen, _ = oracle.accept(inp["parent"], inp["draft"], am)
+    oracle.commit(inp, acc, alen, inplace=True)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def cpu_baseline(inp, cfg, acc_total, budget_s=15.0):
+    threads = os.cpu_count() or 1
+    total_rows = cfg.B * cfg.N * cfg.Hq
+    # calibrate on one row per thread, then size the sample to the budget
+    rows = W.sample_rows(cfg, threads, seed=7)
+    ta, tr = oracle_step_sample(inp, cfg, rows, threads)
+    per_row = ta / len(rows)
+    n = int(min(total_rows, max(len(rows), (budget_s - ta) / max(per_row, 1e-9))))
+    rows = W.sample_rows(cfg, n, seed=8)
+    ta, tr = oracle_step_sample(inp, cfg, rows, threads)
+    step_s = ta * total_rows / len(rows) + tr
+    return {"value": step_bytes(cfg, acc_total) / step_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} of {total_rows} attention rows (fp64 C, {threads} threads) scaled to the "
+                      f"full step, plus argmax/accept/commit of the whole batch",
+            "ms_per_step": step_s * 1e3}
+
+
+def run_reference(args, cfg):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = W.generate(cfg, seed=0)
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    total_rows = cfg.B * cfg.N * cfg.Hq
+    am = oracle.argmax(inp["logits"])
+    _, alen, _ = oracle.accept(inp["parent"], inp["draft"], am)
+    acc_total = int(alen.sum())
+    # size each step's row sample so warmup + steps stay within ~150 s
+    rows = W.sample_rows(cfg, threads, seed=7)
+    ta, _ = oracle_step_sample(inp, cfg, rows, threads)
+    per_row = ta / len(rows)
+    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(total_rows, per_step_budget / max(per_row, 1e-9))))
+    rows = W.sample_rows(cfg, n, seed=9)
+    for _ in range(args.warmup):
+        oracle_step_sample(inp, cfg, rows, threads)
+    equiv = []
+    for _ in range(args.steps):
+        ta, tr = oracle_step_sample(inp, cfg, rows, threads)
+        equiv.append(ta * total_rows / len(rows) + tr)
+    step_s = float(np.mean(equiv))
+    value = step_bytes(cfg, acc_total) / step_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_dict(cfg),
+        "verify_steps_per_s": 1.0 / step_s,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{len(rows)} of {total_rows} attention rows per step (fp64 C, {threads} "
+                                   f"threads) scaled to the full step, plus argmax/accept/commit of the batch"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(cfg):
+    return {"workload": f"{cfg.name}: {cfg.B} seq x {','.join(str(x) for x in cfg.ctx)} committed tokens, "
+                        f"{cfg.Hq}q/{cfg.Hkv}kv heads, D={cfg.D}, {cfg.dtype}, {cfg.N}-node {cfg.tree} tree, "
+                        f"vocab {cfg.vocab}, 64-token pages ({cfg.paged})",
+            "global_batch": cfg.B, "seq_len": cfg.ctx[0], "tree_budget": cfg.N, "heads_q": cfg.Hq,
+            "heads_kv": cfg.Hkv, "head_dim": cfg.D, "vocab": cfg.vocab, "page_size": 64,
+            "parallelism": "replicas (one sequence per rank)",
+            "l2": "inputs larger than L2: committed K/V %d MiB > 129 MB L2" % (cfg.kv_bytes() >> 20)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, cfg):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    from speculative_decoding_tree_ddtree_gb300.build import build
+    build()
+    LT.load()
+
+    inp = W.generate(cfg, seed=rank)
+    tdt = torch.bfloat16 if cfg.dtype == W.BF16 else torch.float16
+
+    def h16(a, pin=False):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(tdt)
+        return t.pin_memory() if pin else t.to(dev)
+
+    d = dict(q=h16(inp["q"]), k_pool=h16(inp["k_pool"]), v_pool=h16(inp["v_pool"]), k_tree=h16(inp["k_tree"]),
+             v_tree=h16(inp["v_tree"]), page_table=torch.from_numpy(inp["page_table"]).to(dev),
+             ctx_len=torch.from_numpy(inp["ctx_len"]).to(dev), parent=torch.from_numpy(inp["parent"]).to(dev),
+             draft=torch.from_numpy(inp["draft"]).to(dev), logits=torch.from_numpy(inp["logits"]).to(dev))
+    stream = torch.cuda.Stream(device=dev)
+    step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, device=dev)
+
+    def one(ev=None):
+        LT.lucetree_build_anc_mask(d["parent"], step.anc, step.status, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        LT.lucetree_verify_attn(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"],
+                                d["v_tree"], step.anc, step.out, step.status, step.ws_attn, lse=step.lse,
+                                stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        LT.lucetree_argmax(d["logits"], step.argmax, step.ws_argmax, stream)
+        LT.lucetree_accept(d["parent"], d["draft"], step.argmax, cfg.vocab, step.acc_nodes, step.acc_len,
+                           step.bonus, step.status, stream)
+        LT.lucetree_commit(d["k_tree"], d["v_tree"], step.acc_nodes, step.acc_len, d["page_table"], d["ctx_len"],
+                           step.ctx_out, d["k_pool"], d["v_pool"], step.status, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            one()
+    stream.synchronize()
+    status = int(step.status.item())
+    acc_total = int(step.acc_len.sum().item())
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for k in range(args.steps):
+        one(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+    ms_per_step = elapsed_ms / args.steps
+
+    # end to end: pinned host inputs -> device, the step, results -> host, every step
+    host = dict(q=h16(inp["q"], True), k_tree=h16(inp["k_tree"], True), v_tree=h16(inp["v_tree"], True),
+                parent=torch.from_numpy(inp["parent"]).pin_memory(), draft=torch.from_numpy(inp["draft"]).pin_memory(),
+                logits=torch.from_numpy(inp["logits"]).pin_memory())
+    res = dict(acc_nodes=torch.empty_like(step.acc_nodes, device="cpu").pin_memory(),
+               acc_len=torch.empty_like(step.acc_len, device="cpu").pin_memory(),
+               bonus=torch.empty_like(step.bonus, device="cpu").pin_memory())
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in res.values())
+    e2e_steps = min(args.steps, 500)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            for k, t in host.items():
+                d[k].copy_(t, non_blocking=True)
+            one()
+            res["acc_nodes"].copy_(step.acc_nodes, non_blocking=True)
+            res["acc_len"].copy_(step.acc_len, non_blocking=True)
+            res["bonus"].copy_(step.bonus, non_blocking=True)
+            stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev) / e2e_steps
+    barrier()
+
+    sb = step_bytes(cfg, acc_total)
+    value = world * sb / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = peak_hbm()
+    achieved = attn_bytes(cfg) / (attn_ms * 1e-3) / 1e9
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic", "config": config_dict(cfg),
+        "verify_steps_per_s": world * 1e3 / ms_per_step,
+        "hbm_pct_of_peak": 100.0 * (sb / (ms_per_step * 1e-3) / 1e9) / peak,
+        "attn_ms_per_call": attn_ms,
+        "accepted_per_step": acc_total, "device_status": status,
+        "clocks": clocks,
+        "e2e": {"value": world * sb / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "lucetree_verify_attn (split-K prefix + tree/merge launch)",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": attn_bytes(cfg)},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, cfg, acc_total)
+    print(json.dumps(line), flush=True)
+    if dist.is_initialized():
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default=W.HEADLINE_128K_B22.name, choices=sorted(W.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    cfg = W.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,205 @@
+/*
+ * lucetree.h -- C ABI of the DDTree verify step on one GB300 (sm_103a).
+ *
+ * One speculative-decoding verify step, as the Lucebox pages describe it:
+ * the target checks a whole tree of draft candidates in one forward pass
+ * instead of a chain ("Lucebox Hub" (Donggyun's knowledge base), section
+ * "Speculative decoding 계층 (DFlash / DDTree / DSpark)"), decoding is greedy at
+ * temperature 0 (PyTorch Korea forum post "Lucebox: 추측 디코딩과 전용 커널로 ...",
+ * section "Lucebox 설치 및 실행", which also gives the budgets 22 and 40), the
+ * KV of rejected tokens is rolled back (the DFlashTarget duties in the
+ * "Lucebox Hub" section above), and KV lives in 64-token chunks (forum post,
+ * section "Lucebox의 최적화 구성요소"; "Lucebox Hub", section "KVFlash") of a
+ * paged pool with a per-sequence block table and D=256 GQA heads ("Lucebox
+ * Hub", section "Paged attention + continuous batching").
+ *
+ * The step is four calls, all asynchronous on the caller's CUDA stream:
+ *   lucetree_verify_attn  tree attention: committed prefix + ancestor block
+ *   lucetree_argmax       per-node argmax over the vocabulary
+ *   lucetree_accept       longest matching root path, greedy
+ *   lucetree_commit       copy accepted K/V into the pool, advance lengths
+ * plus lucetree_build_anc_mask, which turns a parent array into the ancestor
+ * bitmasks verify_attn consumes.
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers unless a parameter says "host".
+ *     The caller owns every buffer; the library allocates no device memory
+ *     and keeps no state beyond cached device properties and TMA descriptors
+ *     built inside the call.  Calls on different streams do not interfere
+ *     as long as their buffers do not overlap.
+ *   - Host-detectable errors (null pointers, unsupported sizes, a workspace
+ *     that is too small) return an error code before anything is launched.
+ *   - Data-dependent errors found by the kernels are OR-ed into the caller's
+ *     device status word (uint32_t, LUCETREE_DEV_* flags); kernels never
+ *     trap.  A call whose inputs raise a flag still completes; outputs that
+ *     depended on the bad input are unspecified.  Clear the word before a
+ *     step and read it whenever convenient.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ */
+#ifndef LUCETREE_H
+#define LUCETREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LUCETREE_API __attribute__((visibility("default")))
+#else
+#define LUCETREE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lucetree_status {
+    LUCETREE_OK = 0,
+    LUCETREE_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size */
+    LUCETREE_ERR_UNSUPPORTED = 2,  /* shape outside what the kernels implement */
+    LUCETREE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    LUCETREE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    LUCETREE_ERR_DEVICE_CHECK = 5, /* reserved: a device status word was non-zero */
+    LUCETREE_ERR_TIMEOUT = 6       /* reserved: a bounded device wait gave up */
+} lucetree_status;
+
+typedef enum lucetree_dtype {
+    LUCETREE_F16 = 0,  /* IEEE binary16 */
+    LUCETREE_BF16 = 1  /* bfloat16 */
+} lucetree_dtype;
+
+/* Flags kernels OR into the device status word. */
+#define LUCETREE_DEV_BAD_PARENT 0x1u /* parent[i] not in [-1, i) */
+#define LUCETREE_DEV_BAD_PAGE 0x2u   /* page id outside [0, num_pages) or page index past the table */
+#define LUCETREE_DEV_BAD_CTX 0x4u    /* ctx_len outside [0, max_pages_per_seq * 64] */
+#define LUCETREE_DEV_BAD_TOKEN 0x8u  /* draft token outside [0, vocab) */
+#define LUCETREE_DEV_BAD_NODE 0x10u  /* accepted node id / count out of range, or a mask without self */
+#define LUCETREE_DEV_TIMEOUT 0x20u   /* a bounded wait inside a kernel gave up */
+
+#define LUCETREE_PAGE_SIZE 64 /* tokens per KV page */
+#define LUCETREE_MAX_NODES 64 /* tree budget limit (one 64-bit ancestor mask per node) */
+
+/*
+ * Arguments of lucetree_verify_attn.  Sizes: B sequences, N tree nodes
+ * (1..64), Hq query heads, Hkv KV heads (Hq % Hkv == 0; query head h reads KV
+ * head h / (Hq / Hkv)), D head dim (128 or 256).
+ */
+typedef struct lucetree_attn_args {
+    int dtype;             /* lucetree_dtype of q, pools and tree K/V */
+    int B, N, Hq, Hkv, D;
+    int page_size;         /* must be LUCETREE_PAGE_SIZE */
+    float scale;           /* softmax scale applied to q.k (1/sqrt(D) in the usual case) */
+    const void* q;         /* [B][N][Hq][D], post-RoPE queries of the tree nodes */
+    const void* k_pool;    /* [num_pages][Hkv][page_size][D] committed keys */
+    const void* v_pool;    /* [num_pages][Hkv][page_size][D] committed values */
+    int num_pages;
+    const int32_t* page_table; /* [B][max_pages_per_seq]: logical page -> pool page */
+    int max_pages_per_seq;
+    const int32_t* ctx_len;    /* [B] committed length L_b; positions [0, L_b) are visible */
+    const void* k_tree;        /* [B][N][Hkv][D] keys of the tree nodes */
+    const void* v_tree;        /* [B][N][Hkv][D] values of the tree nodes */
+    const uint64_t* anc_mask;  /* [B][N]: bit j of node i set iff j is i or an ancestor of i */
+    float* out;                /* [B][N][Hq][D] fp32 attention output */
+    float* lse;                /* [B][N][Hq] natural-log log-sum-exp of the scores, or NULL */
+    uint32_t* status;          /* device status word (LUCETREE_DEV_* flags), required */
+} lucetree_attn_args;
+
+/*
+ * Workspace bytes lucetree_verify_attn needs for these sizes on the CURRENT
+ * device (the split plan is sized to its SM count).  The workspace holds
+ * per-split partial (O, max, sum) triples; it needs no initialisation and
+ * must be 256-byte aligned.  Returns LUCETREE_ERR_UNSUPPORTED for shapes the
+ * kernels do not implement.
+ */
+LUCETREE_API lucetree_status lucetree_verify_attn_workspace(int B, int N, int Hq, int Hkv, int D, size_t* bytes);
+
+/*
+ * Tree-verify attention.  For sequence b, node i and query head h:
+ *   out[b][i][h] = softmax_j(scale * q.k_j) . v_j
+ * over j = every committed position of sequence b (read through the page
+ * table) and every tree node j with bit j of anc_mask[b][i] set.  Split-K over
+ * the committed prefix on the tensor cores, then one merge launch that adds
+ * the tree block and combines the splits by log-sum-exp.
+ * Device checks: ctx_len outside [0, max_pages_per_seq*64] -> BAD_CTX (the
+ * sequence is treated as empty); page id out of range -> BAD_PAGE (those keys
+ * are skipped); a mask without its own bit -> BAD_NODE.
+ */
+LUCETREE_API lucetree_status lucetree_verify_attn(const lucetree_attn_args* args, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
+ * anc[b][i] = bit i | anc[b][parent[b][i]] (parent -1 = the root, which holds
+ * no bit).  Requires parent[b][i] in [-1, i) (topological order); otherwise
+ * BAD_PARENT is raised and anc[b][i] holds bit i only.  parent [B][N],
+ * anc [B][N].  N <= 64.
+ */
+LUCETREE_API lucetree_status lucetree_build_anc_mask(const int32_t* parent, int B, int N, uint64_t* anc, uint32_t* status,
+                                        void* stream);
+
+/* Workspace bytes lucetree_argmax needs for `rows` rows of `vocab` entries. */
+LUCETREE_API lucetree_status lucetree_argmax_workspace(int rows, int vocab, size_t* bytes);
+
+/*
+ * out_idx[r] = the lowest index k with logits[r*row_stride + k] maximal over
+ * k in [0, vocab) (ties, including -0.0 vs +0.0, go to the lower index; NaN
+ * is outside the contract).  logits fp32, row_stride >= vocab elements.  The
+ * workspace (see lucetree_argmax_workspace, 256-byte aligned) needs no
+ * initialisation.
+ */
+LUCETREE_API lucetree_status lucetree_argmax(const float* logits, int rows, int vocab, long long row_stride, int32_t* out_idx,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Greedy acceptance at temperature 0.  parent, draft [B][N]; argmax
+ * [B][N + 1] where row 0 is the root (last committed token) and row j + 1
+ * is node j.  Node c matches when draft[c] == argmax row of parent(c).  The
+ * accepted path ends at the deepest node whose whole root path matches (the
+ * lowest node id among equally deep ones).  Outputs: acc_nodes [B][N] the
+ * path root-to-leaf, padded with -1; acc_len [B]; bonus [B] = argmax row of
+ * the last accepted node (the root's row when none is accepted).
+ * Device checks: BAD_PARENT (the sequence then accepts nothing), BAD_TOKEN
+ * (draft outside [0, vocab): never matches).
+ */
+LUCETREE_API lucetree_status lucetree_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int B, int N,
+                                int vocab, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus, uint32_t* status,
+                                void* stream);
+
+/* Arguments of lucetree_commit (sizes as in lucetree_attn_args). */
+typedef struct lucetree_commit_args {
+    int dtype;
+    int B, N, Hkv, D;
+    int page_size;             /* must be LUCETREE_PAGE_SIZE */
+    const void* k_tree;        /* [B][N][Hkv][D] */
+    const void* v_tree;        /* [B][N][Hkv][D] */
+    const int32_t* acc_nodes;  /* [B][N] from lucetree_accept */
+    const int32_t* acc_len;    /* [B] */
+    const int32_t* page_table; /* [B][max_pages_per_seq]; must already map positions [L_b, L_b + N) */
+    int max_pages_per_seq;
+    int num_pages;
+    const int32_t* ctx_len_in; /* [B] L_b before the step */
+    int32_t* ctx_len_out;      /* [B] L_b + accepted count; may alias ctx_len_in */
+    void* k_pool;              /* [num_pages][Hkv][page_size][D], updated in place */
+    void* v_pool;
+    uint32_t* status;
+} lucetree_commit_args;
+
+/*
+ * Commit / rollback.  The k-th accepted node's K and V rows (every KV head)
+ * are copied to logical position L_b + k: pool page page_table[b][(L_b+k)/64],
+ * slot (L_b+k) % 64.  Rejected nodes are never written, which is the
+ * rollback.  No other pool byte changes.  ctx_len_out[b] = L_b + count
+ * copied.  Device checks: BAD_NODE (count outside [0, N] or node id outside
+ * [0, N)), BAD_PAGE, BAD_CTX; copying stops at the first bad entry.
+ */
+LUCETREE_API lucetree_status lucetree_commit(const lucetree_commit_args* args, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+LUCETREE_API const char* lucetree_status_string(lucetree_status status);
+
+/* ABI version of this header: 1. */
+LUCETREE_API int lucetree_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LUCETREE_H */

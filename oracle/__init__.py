@@ -140,10 +140,15 @@ def accept(parent, draft, argmax_idx):
     return acc, alen, bonus
 
 
-def commit(inp: dict, acc_nodes, acc_len):
-    """Returns (k_pool, v_pool, ctx_len) after committing, on copies."""
-    k_pool = np.array(inp["k_pool"], dtype=np.uint16, copy=True)
-    v_pool = np.array(inp["v_pool"], dtype=np.uint16, copy=True)
+def commit(inp: dict, acc_nodes, acc_len, inplace: bool = False):
+    """Returns (k_pool, v_pool, ctx_len) after committing, on copies (or, with
+    ``inplace``, writing into the given pools; ctx_len is always a copy)."""
+    if inplace:
+        k_pool, v_pool = inp["k_pool"], inp["v_pool"]
+        assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous and k_pool.dtype == np.uint16
+    else:
+        k_pool = np.array(inp["k_pool"], dtype=np.uint16, copy=True)
+        v_pool = np.array(inp["v_pool"], dtype=np.uint16, copy=True)
     ctx = np.array(inp["ctx_len"], dtype=np.int32, copy=True)
     kt = _c(inp["k_tree"], np.uint16)
     vt = _c(inp["v_tree"], np.uint16)

@@ -1,0 +1,192 @@
+// internal.cuh -- shared definitions of the lucetree CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lucetree.h"
+
+namespace lucetree {
+
+// ---------------------------------------------------------------------------
+// Split plan of the committed-prefix attention.
+//
+// Query rows of one (sequence b, KV head g) are the N*G pairs (node i, head
+// h' in the group).  They are cut into NG row groups of NPG consecutive nodes
+// so a group has at most kRowsMax rows (the tensor-core tile's N extent).
+// A "segment" is one (b, g, row group); segments are numbered
+//   s = (b * Hkv + g) * NG + rg
+// and each owns ceil(L_b / kTileKeys) key tiles.  Concatenating all segments'
+// tiles gives a flat list of T tiles; CTA c of a C-CTA persistent grid takes
+// tiles [floor(c*T/C), floor((c+1)*T/C)).  A CTA writes one partial
+// (O, max, sum) per segment its range touches, into workspace slot c + s; the
+// pair (c, s) is unique because both partitions are ordered, so C + S - 1
+// slots always suffice.
+// ---------------------------------------------------------------------------
+constexpr int kTileKeys = 128;  // keys per tile: two 64-token pages
+constexpr int kRowsMax = 144;   // rows per CTA (multiple of 16)
+constexpr int kPage = LUCETREE_PAGE_SIZE;
+
+struct RowGroups {
+    int NG;   // number of row groups
+    int NPG;  // nodes per group (the last group may hold fewer)
+    int RG;   // rows per group = NPG * G
+};
+
+__host__ __device__ inline RowGroups make_row_groups(int N, int G) {
+    RowGroups r;
+    r.NG = (N * G + kRowsMax - 1) / kRowsMax;
+    if (r.NG < 1) r.NG = 1;
+    r.NPG = (N + r.NG - 1) / r.NG;
+    while (r.NPG * G > kRowsMax && r.NPG > 1) {
+        r.NG += 1;
+        r.NPG = (N + r.NG - 1) / r.NG;
+    }
+    r.RG = r.NPG * G;
+    return r;
+}
+
+struct PlanDims {
+    int B, N, Hq, Hkv, D, G;
+    RowGroups rg;
+    int S;         // segments
+    int C;         // CTAs of the prefix grid
+    int max_pages; // page-table row length
+};
+
+__host__ __device__ inline PlanDims make_plan(int B, int N, int Hq, int Hkv, int D, int C, int max_pages) {
+    PlanDims p;
+    p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
+    p.rg = make_row_groups(N, p.G);
+    p.S = B * Hkv * p.rg.NG;
+    p.C = C;
+    p.max_pages = max_pages;
+    return p;
+}
+
+// floats per workspace slot: O [RG][D], then max [RG], then sum [RG]
+__host__ __device__ inline size_t slot_floats(const PlanDims& p) {
+    return (size_t)p.rg.RG * (p.D + 2);
+}
+
+__host__ __device__ inline size_t attn_workspace_bytes(const PlanDims& p) {
+    size_t slots = (size_t)p.C + p.S - 1;
+    return slots * slot_floats(p) * sizeof(float);
+}
+
+// Committed length used by the kernels: out-of-range values count as 0.
+__device__ inline int seq_len(const int32_t* ctx_len, int b, int max_pages, uint32_t* status) {
+    int L = ctx_len[b];
+    if (L < 0 || (long long)L > (long long)max_pages * kPage) {
+        if (status) atomicOr(status, LUCETREE_DEV_BAD_CTX);
+        return 0;
+    }
+    return L;
+}
+
+__device__ inline int seq_len_quiet(const int32_t* ctx_len, int b, int max_pages) {
+    int L = ctx_len[b];
+    if (L < 0 || (long long)L > (long long)max_pages * kPage) return 0;
+    return L;
+}
+
+__device__ inline long long tiles_of(int L) { return (L + kTileKeys - 1) / kTileKeys; }
+
+// Total flat tiles over all segments.
+__device__ inline long long total_tiles(const PlanDims& p, const int32_t* ctx_len) {
+    long long t = 0;
+    for (int b = 0; b < p.B; ++b) t += tiles_of(seq_len_quiet(ctx_len, b, p.max_pages));
+    return t * p.Hkv * p.rg.NG;
+}
+
+// Flat offset of segment s's first tile.
+__device__ inline long long segment_offset(const PlanDims& p, const int32_t* ctx_len, int s) {
+    int per_seq = p.Hkv * p.rg.NG;
+    int b = s / per_seq, within = s % per_seq;
+    long long off = 0;
+    for (int bb = 0; bb < b; ++bb) off += tiles_of(seq_len_quiet(ctx_len, bb, p.max_pages)) * per_seq;
+    return off + (long long)within * tiles_of(seq_len_quiet(ctx_len, b, p.max_pages));
+}
+
+__device__ inline long long cta_begin(long long c, long long T, int C) { return c * T / C; }
+
+// The CTA whose range holds flat tile t (largest c with cta_begin(c) <= t).
+__device__ inline int cta_of_tile(long long t, long long T, int C) {
+    return (int)(((t + 1) * (long long)C - 1) / T);
+}
+
+// ---------------------------------------------------------------------------
+// 16-bit element helpers
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ inline float to_f32(T x);
+template <>
+__device__ inline float to_f32<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ inline float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 8 consecutive 16-bit elements (16 bytes) to fp32
+template <typename T>
+__device__ inline void load8_f32(const T* p, float* out);
+template <>
+__device__ inline void load8_f32<__half>(const __half* p, float* out) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float2 f = __half22float2(h[k]);
+        out[2 * k] = f.x;
+        out[2 * k + 1] = f.y;
+    }
+}
+template <>
+__device__ inline void load8_f32<__nv_bfloat16>(const __nv_bfloat16* p, float* out) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float2 f = __bfloat1622float2(h[k]);
+        out[2 * k] = f.x;
+        out[2 * k + 1] = f.y;
+    }
+}
+
+template <typename T>
+__device__ inline void load4_f32(const T* p, float* out) {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) out[k] = to_f32<T>(e[k]);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------------------
+// launchers (each returns cudaGetLastError() of its launch)
+// ---------------------------------------------------------------------------
+struct AttnLaunch {
+    lucetree_attn_args a;
+    PlanDims plan;
+    float* ws;
+    float scale_log2;  // scale * log2(e)
+};
+
+int prefix_grid_ctas(int device);  // persistent grid size of the prefix kernel
+cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_attn_merge(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_build_anc(const int32_t* parent, int B, int N, uint64_t* anc, uint32_t* status,
+                             cudaStream_t stream);
+cudaError_t launch_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int B, int N,
+                          int vocab, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus, uint32_t* status,
+                          cudaStream_t stream);
+cudaError_t launch_commit(const lucetree_commit_args& c, cudaStream_t stream);
+size_t argmax_workspace_bytes(int rows, int vocab, int device);
+cudaError_t launch_argmax(const float* logits, int rows, int vocab, long long row_stride, int32_t* out_idx,
+                          void* ws, int device, cudaStream_t stream);
+
+int device_sm_count(int device);
+
+}  // namespace lucetree

@@ -1,0 +1,154 @@
+// lucetree_abi.cu -- the extern "C" entry points: argument checks, workspace
+// sizing and kernel launches on the caller's stream.
+#include <cstring>
+
+#include "internal.cuh"
+
+namespace lucetree {
+
+int device_sm_count(int device) {
+    static int cache[128] = {0};
+    if (device < 0 || device >= 128) return 1;
+    if (cache[device] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) n = 1;
+        cache[device] = n;
+    }
+    return cache[device];
+}
+
+static int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return 0;
+    return d;
+}
+
+static bool attn_shape_ok(int B, int N, int Hq, int Hkv, int D) {
+    if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0) return false;
+    if (N > LUCETREE_MAX_NODES) return false;
+    if (Hq % Hkv != 0) return false;
+    if (D != 128 && D != 256) return false;
+    if (Hq / Hkv > kRowsMax) return false;
+    return true;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace lucetree
+
+using namespace lucetree;
+
+extern "C" {
+
+int lucetree_abi_version(void) { return 1; }
+
+const char* lucetree_status_string(lucetree_status s) {
+    switch (s) {
+        case LUCETREE_OK: return "ok";
+        case LUCETREE_ERR_INVALID_ARG: return "invalid argument";
+        case LUCETREE_ERR_UNSUPPORTED: return "unsupported shape";
+        case LUCETREE_ERR_WORKSPACE: return "workspace missing or too small";
+        case LUCETREE_ERR_CUDA: return "CUDA error";
+        case LUCETREE_ERR_DEVICE_CHECK: return "device check failed";
+        case LUCETREE_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+lucetree_status lucetree_verify_attn_workspace(int B, int N, int Hq, int Hkv, int D, size_t* bytes) {
+    if (!bytes) return LUCETREE_ERR_INVALID_ARG;
+    if (!attn_shape_ok(B, N, Hq, Hkv, D)) return LUCETREE_ERR_UNSUPPORTED;
+    PlanDims p = make_plan(B, N, Hq, Hkv, D, prefix_grid_ctas(current_device()), 1);
+    *bytes = attn_workspace_bytes(p);
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_verify_attn(const lucetree_attn_args* a, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+    if (!a) return LUCETREE_ERR_INVALID_ARG;
+    if (a->dtype != LUCETREE_F16 && a->dtype != LUCETREE_BF16) return LUCETREE_ERR_UNSUPPORTED;
+    if (a->page_size != LUCETREE_PAGE_SIZE) return LUCETREE_ERR_UNSUPPORTED;
+    if (!attn_shape_ok(a->B, a->N, a->Hq, a->Hkv, a->D)) return LUCETREE_ERR_UNSUPPORTED;
+    if (!a->q || !a->k_pool || !a->v_pool || !a->page_table || !a->ctx_len || !a->k_tree || !a->v_tree ||
+        !a->anc_mask || !a->out || !a->status)
+        return LUCETREE_ERR_INVALID_ARG;
+    if (a->num_pages <= 0 || a->max_pages_per_seq <= 0) return LUCETREE_ERR_INVALID_ARG;
+    if (!aligned16(a->q) || !aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->k_tree) ||
+        !aligned16(a->v_tree) || !aligned16(a->out))
+        return LUCETREE_ERR_INVALID_ARG;
+    if (!isfinite(a->scale)) return LUCETREE_ERR_INVALID_ARG;
+    const int dev = current_device();
+    AttnLaunch L;
+    L.a = *a;
+    L.plan = make_plan(a->B, a->N, a->Hq, a->Hkv, a->D, prefix_grid_ctas(dev), a->max_pages_per_seq);
+    if (!workspace || workspace_bytes < attn_workspace_bytes(L.plan) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return LUCETREE_ERR_WORKSPACE;
+    L.ws = reinterpret_cast<float*>(workspace);
+    L.scale_log2 = a->scale * kLog2e;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_attn_prefix(L, s) != cudaSuccess) return LUCETREE_ERR_CUDA;
+    if (launch_attn_merge(L, s) != cudaSuccess) return LUCETREE_ERR_CUDA;
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_build_anc_mask(const int32_t* parent, int B, int N, uint64_t* anc, uint32_t* status,
+                                        void* stream) {
+    if (!parent || !anc || !status || B <= 0 || N <= 0) return LUCETREE_ERR_INVALID_ARG;
+    if (N > LUCETREE_MAX_NODES) return LUCETREE_ERR_UNSUPPORTED;
+    if (launch_build_anc(parent, B, N, anc, status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LUCETREE_ERR_CUDA;
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_argmax_workspace(int rows, int vocab, size_t* bytes) {
+    if (!bytes || rows <= 0 || vocab <= 0) return LUCETREE_ERR_INVALID_ARG;
+    if (rows > 65535) return LUCETREE_ERR_UNSUPPORTED;
+    *bytes = argmax_workspace_bytes(rows, vocab, current_device());
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_argmax(const float* logits, int rows, int vocab, long long row_stride, int32_t* out_idx,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+    if (!logits || !out_idx || rows <= 0 || vocab <= 0 || row_stride < vocab) return LUCETREE_ERR_INVALID_ARG;
+    if (rows > 65535) return LUCETREE_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (!workspace || workspace_bytes < argmax_workspace_bytes(rows, vocab, dev) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return LUCETREE_ERR_WORKSPACE;
+    if (launch_argmax(logits, rows, vocab, row_stride, out_idx, workspace, dev,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LUCETREE_ERR_CUDA;
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int B, int N,
+                                int vocab, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus, uint32_t* status,
+                                void* stream) {
+    if (!parent || !draft || !argmax || !acc_nodes || !acc_len || !bonus || !status) return LUCETREE_ERR_INVALID_ARG;
+    if (B <= 0 || N <= 0 || vocab <= 0) return LUCETREE_ERR_INVALID_ARG;
+    if (N > LUCETREE_MAX_NODES) return LUCETREE_ERR_UNSUPPORTED;
+    if (launch_accept(parent, draft, argmax, B, N, vocab, acc_nodes, acc_len, bonus, status,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LUCETREE_ERR_CUDA;
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_commit(const lucetree_commit_args* c, void* stream) {
+    if (!c) return LUCETREE_ERR_INVALID_ARG;
+    if (c->dtype != LUCETREE_F16 && c->dtype != LUCETREE_BF16) return LUCETREE_ERR_UNSUPPORTED;
+    if (c->page_size != LUCETREE_PAGE_SIZE) return LUCETREE_ERR_UNSUPPORTED;
+    if (c->B <= 0 || c->N <= 0 || c->Hkv <= 0 || c->D <= 0 || c->num_pages <= 0 || c->max_pages_per_seq <= 0)
+        return LUCETREE_ERR_INVALID_ARG;
+    if (c->N > LUCETREE_MAX_NODES) return LUCETREE_ERR_UNSUPPORTED;
+    if ((c->D * 2) % 16 != 0) return LUCETREE_ERR_UNSUPPORTED;
+    if (!c->k_tree || !c->v_tree || !c->acc_nodes || !c->acc_len || !c->page_table || !c->ctx_len_in ||
+        !c->ctx_len_out || !c->k_pool || !c->v_pool || !c->status)
+        return LUCETREE_ERR_INVALID_ARG;
+    if (!aligned16(c->k_tree) || !aligned16(c->v_tree) || !aligned16(c->k_pool) || !aligned16(c->v_pool))
+        return LUCETREE_ERR_INVALID_ARG;
+    if (launch_commit(*c, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LUCETREE_ERR_CUDA;
+    return LUCETREE_OK;
+}
+
+}  // extern "C"

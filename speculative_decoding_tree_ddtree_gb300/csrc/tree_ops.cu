@@ -1,0 +1,165 @@
+// tree_ops.cu -- ancestor masks, greedy acceptance and the commit copy.
+//
+// Acceptance follows the greedy (temperature 0) rule: a draft node is right
+// when its token equals the argmax of its parent's logits, and the step keeps
+// the longest root path of right nodes (PyTorch Korea forum post "Lucebox:
+// 추측 디코딩과 전용 커널로 ...", section "Lucebox 설치 및 실행").  Commit copies
+// the kept nodes' K/V into the 64-token pages after the committed prefix and
+// leaves rejected nodes unwritten, which is the KV rollback of the
+// DFlashTarget interface ("Lucebox Hub", section "Speculative decoding 계층").
+#include "internal.cuh"
+
+namespace lucetree {
+
+namespace {
+
+// One thread per sequence; N <= 64 so the masks fit one word per node.
+__global__ void build_anc_kernel(const int32_t* __restrict__ parent, int B, int N, uint64_t* __restrict__ anc,
+                                 uint32_t* status) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int32_t* par = parent + (size_t)b * N;
+    uint64_t* out = anc + (size_t)b * N;
+    uint64_t local[LUCETREE_MAX_NODES];
+    for (int i = 0; i < N; ++i) {
+        const int pi = par[i];
+        uint64_t m = 1ull << i;
+        if (pi >= 0 && pi < i) {
+            m |= local[pi];
+        } else if (pi != -1) {
+            atomicOr(status, LUCETREE_DEV_BAD_PARENT);
+        }
+        local[i] = m;
+        out[i] = m;
+    }
+}
+
+// One thread per sequence.  ok[i]: node i and all its ancestors match; the
+// deepest ok node (lowest id among equals, by scanning ids upward with a
+// strict comparison) ends the accepted path.
+__global__ void accept_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ draft,
+                              const int32_t* __restrict__ argmax, int B, int N, int vocab,
+                              int32_t* __restrict__ acc_nodes, int32_t* __restrict__ acc_len,
+                              int32_t* __restrict__ bonus, uint32_t* status) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int32_t* par = parent + (size_t)b * N;
+    const int32_t* dr = draft + (size_t)b * N;
+    const int32_t* am = argmax + (size_t)b * (N + 1);
+    int32_t* out = acc_nodes + (size_t)b * N;
+    int depth[LUCETREE_MAX_NODES];
+    uint64_t ok = 0;
+    int best = -1, best_depth = 0;
+    bool bad = false;
+    for (int i = 0; i < N; ++i) {
+        const int pi = par[i];
+        if (pi < -1 || pi >= i) {
+            bad = true;
+            break;
+        }
+        const int t = dr[i];
+        bool match = t == am[pi + 1];
+        if (t < 0 || t >= vocab) {
+            atomicOr(status, LUCETREE_DEV_BAD_TOKEN);
+            match = false;
+        }
+        const bool parent_ok = pi < 0 || ((ok >> pi) & 1ull);
+        depth[i] = (pi < 0 ? 0 : depth[pi]) + 1;
+        if (match && parent_ok) {
+            ok |= 1ull << i;
+            if (depth[i] > best_depth) {
+                best = i;
+                best_depth = depth[i];
+            }
+        }
+    }
+    if (bad) {
+        atomicOr(status, LUCETREE_DEV_BAD_PARENT);
+        best = -1;
+        best_depth = 0;
+    }
+    for (int k = best_depth; k < N; ++k) out[k] = -1;
+    int k = best_depth;
+    for (int c = best; c >= 0; c = par[c]) out[--k] = c;
+    acc_len[b] = best_depth;
+    bonus[b] = am[best + 1];
+}
+
+// One block per sequence: 16-byte vector copies of every accepted node's K and
+// V rows (all KV heads); the length update happens after the block has read
+// ctx_len_in, so ctx_len_out may alias it.
+__global__ void __launch_bounds__(256) commit_kernel(lucetree_commit_args c, int elem_bytes) {
+    const int b = blockIdx.x;
+    const int L = c.ctx_len_in[b];
+    const int a = c.acc_len[b];
+    __shared__ int s_good;
+    if (threadIdx.x == 0) s_good = 0x7fffffff;
+    __syncthreads();
+    const size_t row_bytes = (size_t)c.D * elem_bytes;
+    const int vec_per_row = (int)(row_bytes / 16);
+    const char* kt = reinterpret_cast<const char*>(c.k_tree);
+    const char* vt = reinterpret_cast<const char*>(c.v_tree);
+    char* kp = reinterpret_cast<char*>(c.k_pool);
+    char* vp = reinterpret_cast<char*>(c.v_pool);
+    int count = a;
+    if (a < 0 || a > c.N || L < 0) {
+        if (threadIdx.x == 0) atomicOr(c.status, a < 0 || a > c.N ? LUCETREE_DEV_BAD_NODE : LUCETREE_DEV_BAD_CTX);
+        count = 0;
+    }
+    // validate entries first so the copy stops at the first bad one
+    for (int k = threadIdx.x; k < count; k += blockDim.x) {
+        const int node = c.acc_nodes[(size_t)b * c.N + k];
+        const long long pos = (long long)L + k;
+        const long long pi = pos / kPage;
+        bool good = node >= 0 && node < c.N && pi < c.max_pages_per_seq;
+        uint32_t flag = (node >= 0 && node < c.N) ? LUCETREE_DEV_BAD_PAGE : LUCETREE_DEV_BAD_NODE;
+        if (good) {
+            const int page = c.page_table[(size_t)b * c.max_pages_per_seq + pi];
+            good = page >= 0 && page < c.num_pages;
+        }
+        if (!good) {
+            atomicOr(c.status, flag);
+            atomicMin(&s_good, k);
+        }
+    }
+    __syncthreads();
+    count = min(count, s_good);
+    const int units = count * c.Hkv * vec_per_row;
+    for (int u = threadIdx.x; u < units; u += blockDim.x) {
+        const int v = u % vec_per_row;
+        const int g = (u / vec_per_row) % c.Hkv;
+        const int k = u / (vec_per_row * c.Hkv);
+        const int node = c.acc_nodes[(size_t)b * c.N + k];
+        const long long pos = (long long)L + k;
+        const int page = c.page_table[(size_t)b * c.max_pages_per_seq + pos / kPage];
+        const size_t dst = ((((size_t)page * c.Hkv + g) * kPage + (size_t)(pos % kPage)) * row_bytes) + (size_t)v * 16;
+        const size_t src = ((((size_t)b * c.N + node) * c.Hkv + g) * row_bytes) + (size_t)v * 16;
+        *reinterpret_cast<uint4*>(kp + dst) = *reinterpret_cast<const uint4*>(kt + src);
+        *reinterpret_cast<uint4*>(vp + dst) = *reinterpret_cast<const uint4*>(vt + src);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) c.ctx_len_out[b] = L < 0 ? L : L + count;
+}
+
+}  // namespace
+
+cudaError_t launch_build_anc(const int32_t* parent, int B, int N, uint64_t* anc, uint32_t* status,
+                             cudaStream_t stream) {
+    build_anc_kernel<<<(B + 63) / 64, 64, 0, stream>>>(parent, B, N, anc, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int B, int N,
+                          int vocab, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus, uint32_t* status,
+                          cudaStream_t stream) {
+    accept_kernel<<<(B + 63) / 64, 64, 0, stream>>>(parent, draft, argmax, B, N, vocab, acc_nodes, acc_len, bonus,
+                                                    status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_commit(const lucetree_commit_args& c, cudaStream_t stream) {
+    commit_kernel<<<c.B, 256, 0, stream>>>(c, 2);
+    return cudaGetLastError();
+}
+
+}  // namespace lucetree

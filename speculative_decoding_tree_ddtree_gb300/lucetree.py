@@ -1,0 +1,234 @@
+"""Thin Python binding of liblucetree.so (include/lucetree.h).
+
+Argument marshalling only: torch tensors become raw device pointers and every
+step runs in the library's CUDA kernels.  The functions carry the C names.
+There is no fallback: if the shared library is missing or a call returns an
+error status, a ``LucetreeError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblucetree.so")
+
+LUCETREE_OK = 0
+LUCETREE_F16 = 0
+LUCETREE_BF16 = 1
+PAGE_SIZE = 64
+MAX_NODES = 64
+
+DEV_BAD_PARENT = 0x1
+DEV_BAD_PAGE = 0x2
+DEV_BAD_CTX = 0x4
+DEV_BAD_TOKEN = 0x8
+DEV_BAD_NODE = 0x10
+DEV_TIMEOUT = 0x20
+
+EXPORTED = (
+    "lucetree_verify_attn_workspace",
+    "lucetree_verify_attn",
+    "lucetree_build_anc_mask",
+    "lucetree_argmax_workspace",
+    "lucetree_argmax",
+    "lucetree_accept",
+    "lucetree_commit",
+    "lucetree_status_string",
+    "lucetree_abi_version",
+)
+
+
+class LucetreeError(RuntimeError):
+    pass
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int), ("B", ctypes.c_int), ("N", ctypes.c_int), ("Hq", ctypes.c_int),
+        ("Hkv", ctypes.c_int), ("D", ctypes.c_int), ("page_size", ctypes.c_int), ("scale", ctypes.c_float),
+        ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+        ("num_pages", ctypes.c_int), ("page_table", ctypes.c_void_p), ("max_pages_per_seq", ctypes.c_int),
+        ("ctx_len", ctypes.c_void_p), ("k_tree", ctypes.c_void_p), ("v_tree", ctypes.c_void_p),
+        ("anc_mask", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+    ]
+
+
+class CommitArgs(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int), ("B", ctypes.c_int), ("N", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("D", ctypes.c_int), ("page_size", ctypes.c_int), ("k_tree", ctypes.c_void_p), ("v_tree", ctypes.c_void_p),
+        ("acc_nodes", ctypes.c_void_p), ("acc_len", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+        ("max_pages_per_seq", ctypes.c_int), ("num_pages", ctypes.c_int), ("ctx_len_in", ctypes.c_void_p),
+        ("ctx_len_out", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load liblucetree.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise LucetreeError(f"{p} is missing: build it with speculative_decoding_tree_ddtree_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.lucetree_verify_attn_workspace.argtypes = [I, I, I, I, I, ctypes.POINTER(SZ)]
+    lib.lucetree_verify_attn.argtypes = [ctypes.POINTER(AttnArgs), P, SZ, P]
+    lib.lucetree_build_anc_mask.argtypes = [P, I, I, P, P, P]
+    lib.lucetree_argmax_workspace.argtypes = [I, I, ctypes.POINTER(SZ)]
+    lib.lucetree_argmax.argtypes = [P, I, I, ctypes.c_longlong, P, P, SZ, P]
+    lib.lucetree_accept.argtypes = [P, P, P, I, I, I, P, P, P, P, P]
+    lib.lucetree_commit.argtypes = [ctypes.POINTER(CommitArgs), P]
+    lib.lucetree_status_string.argtypes = [I]
+    lib.lucetree_status_string.restype = ctypes.c_char_p
+    lib.lucetree_abi_version.argtypes = []
+    for name in EXPORTED:
+        if name not in ("lucetree_status_string", "lucetree_abi_version"):
+            getattr(lib, name).restype = I
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != LUCETREE_OK:
+        msg = load().lucetree_status_string(rc).decode()
+        raise LucetreeError(f"lucetree error {rc}: {msg}")
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise LucetreeError("lucetree takes device tensors")
+    if not t.is_contiguous():
+        raise LucetreeError("lucetree takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return LUCETREE_BF16
+    if t.dtype == torch.float16:
+        return LUCETREE_F16
+    raise LucetreeError(f"unsupported dtype {t.dtype}")
+
+
+# ---------------------------------------------------------------- entry points
+
+def lucetree_verify_attn_workspace(B: int, N: int, Hq: int, Hkv: int, D: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().lucetree_verify_attn_workspace(B, N, Hq, Hkv, D, ctypes.byref(n)))
+    return int(n.value)
+
+
+def lucetree_verify_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status,
+                         workspace, lse=None, scale: float | None = None, stream=None):
+    """q [B][N][Hq][D]; pools [P][Hkv][64][D]; page_table int32 [B][max_pages];
+    ctx_len int32 [B]; tree K/V [B][N][Hkv][D]; anc_mask int64 [B][N];
+    out fp32 [B][N][Hq][D]; status int32 [1]; workspace uint8 (see
+    lucetree_verify_attn_workspace)."""
+    B, N, Hq, D = q.shape
+    Hkv = k_pool.shape[1]
+    a = AttnArgs()
+    a.dtype = dtype_code(q)
+    a.B, a.N, a.Hq, a.Hkv, a.D = B, N, Hq, Hkv, D
+    a.page_size = k_pool.shape[2]
+    a.scale = float(scale) if scale is not None else float(D) ** -0.5
+    a.q, a.k_pool, a.v_pool = _ptr(q), _ptr(k_pool), _ptr(v_pool)
+    a.num_pages = k_pool.shape[0]
+    a.page_table, a.max_pages_per_seq = _ptr(page_table), page_table.shape[1]
+    a.ctx_len, a.k_tree, a.v_tree, a.anc_mask = _ptr(ctx_len), _ptr(k_tree), _ptr(v_tree), _ptr(anc_mask)
+    a.out, a.lse, a.status = _ptr(out), _ptr(lse), _ptr(status)
+    _check(load().lucetree_verify_attn(ctypes.byref(a), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
+
+
+def lucetree_build_anc_mask(parent, anc, status, stream=None):
+    B, N = parent.shape
+    _check(load().lucetree_build_anc_mask(_ptr(parent), B, N, _ptr(anc), _ptr(status), _stream(stream)))
+
+
+def lucetree_argmax_workspace(rows: int, vocab: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().lucetree_argmax_workspace(rows, vocab, ctypes.byref(n)))
+    return int(n.value)
+
+
+def lucetree_argmax(logits, out_idx, workspace, stream=None):
+    """logits fp32 [..., V] (rows = all leading dims) -> out_idx int32 [...]."""
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    _check(load().lucetree_argmax(_ptr(logits), rows, V, V, _ptr(out_idx), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lucetree_accept(parent, draft, argmax_idx, vocab: int, acc_nodes, acc_len, bonus, status, stream=None):
+    B, N = parent.shape
+    _check(load().lucetree_accept(_ptr(parent), _ptr(draft), _ptr(argmax_idx), B, N, vocab, _ptr(acc_nodes),
+                                  _ptr(acc_len), _ptr(bonus), _ptr(status), _stream(stream)))
+
+
+def lucetree_commit(k_tree, v_tree, acc_nodes, acc_len, page_table, ctx_len_in, ctx_len_out, k_pool, v_pool,
+                    status, stream=None):
+    B, N, Hkv, D = k_tree.shape
+    c = CommitArgs()
+    c.dtype = dtype_code(k_tree)
+    c.B, c.N, c.Hkv, c.D = B, N, Hkv, D
+    c.page_size = k_pool.shape[2]
+    c.k_tree, c.v_tree = _ptr(k_tree), _ptr(v_tree)
+    c.acc_nodes, c.acc_len = _ptr(acc_nodes), _ptr(acc_len)
+    c.page_table, c.max_pages_per_seq = _ptr(page_table), page_table.shape[1]
+    c.num_pages = k_pool.shape[0]
+    c.ctx_len_in, c.ctx_len_out = _ptr(ctx_len_in), _ptr(ctx_len_out)
+    c.k_pool, c.v_pool, c.status = _ptr(k_pool), _ptr(v_pool), _ptr(status)
+    _check(load().lucetree_commit(ctypes.byref(c), _stream(stream)))
+
+
+# ---------------------------------------------------------------- one whole step
+
+class VerifyStep:
+    """Device buffers and workspaces for repeated verify steps of one shape.
+
+    ``run`` issues the whole step on one stream: ancestor masks, tree-verify
+    attention, argmax, acceptance and commit (all library kernels)."""
+
+    def __init__(self, B, N, Hq, Hkv, D, vocab, device="cuda"):
+        self.B, self.N, self.Hq, self.Hkv, self.D, self.vocab = B, N, Hq, Hkv, D, vocab
+        dev = torch.device(device)
+        self.ws_attn = torch.empty(lucetree_verify_attn_workspace(B, N, Hq, Hkv, D), dtype=torch.uint8, device=dev)
+        self.ws_argmax = torch.empty(lucetree_argmax_workspace(B * (N + 1), vocab), dtype=torch.uint8, device=dev)
+        self.anc = torch.empty(B, N, dtype=torch.int64, device=dev)
+        self.out = torch.empty(B, N, Hq, D, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(B, N, Hq, dtype=torch.float32, device=dev)
+        self.argmax = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+        self.acc_nodes = torch.empty(B, N, dtype=torch.int32, device=dev)
+        self.acc_len = torch.empty(B, dtype=torch.int32, device=dev)
+        self.bonus = torch.empty(B, dtype=torch.int32, device=dev)
+        self.ctx_out = torch.empty(B, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(self, q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, parent, draft, logits, stream=None):
+        lucetree_build_anc_mask(parent, self.anc, self.status, stream)
+        lucetree_verify_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, self.anc, self.out,
+                             self.status, self.ws_attn, lse=self.lse, stream=stream)
+        lucetree_argmax(logits, self.argmax, self.ws_argmax, stream)
+        lucetree_accept(parent, draft, self.argmax, self.vocab, self.acc_nodes, self.acc_len, self.bonus,
+                        self.status, stream)
+        lucetree_commit(k_tree, v_tree, self.acc_nodes, self.acc_len, page_table, ctx_len, self.ctx_out, k_pool,
+                        v_pool, self.status, stream)

@@ -1,0 +1,64 @@
+"""The C-ABI library loads without a GPU and exports every symbol the header
+declares; the binding refuses host tensors.  No compute calls here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_tree_ddtree_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names.update(re.findall(r"^LUCETREE_API\s+[\w\s\*]+?\b(lucetree_\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = B.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_four_calls():
+    d = _declared()
+    for name in ("lucetree_verify_attn", "lucetree_argmax", "lucetree_accept", "lucetree_commit"):
+        assert name in d
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_binding_lists_every_declared_symbol():
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    assert set(_declared()) <= set(LT.EXPORTED)
+
+
+def test_host_side_queries_without_gpu(lib):
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    lt = LT.load()
+    assert lt.lucetree_abi_version() == 1
+    assert lt.lucetree_status_string(3) == b"workspace missing or too small"
+    n = ctypes.c_size_t(0)
+    # unsupported head dim and budget are rejected before any device work
+    assert lt.lucetree_verify_attn_workspace(1, 22, 24, 4, 96, ctypes.byref(n)) == 2
+    assert lt.lucetree_verify_attn_workspace(1, 65, 24, 4, 256, ctypes.byref(n)) == 2
+    assert lt.lucetree_verify_attn_workspace(1, 22, 24, 5, 256, ctypes.byref(n)) == 2
+    assert lt.lucetree_accept(None, None, None, 1, 1, 1, None, None, None, None, None) == 1
+    assert lt.lucetree_verify_attn(None, None, 0, None) == 1
+    assert lt.lucetree_commit(None, None) == 1
+
+
+def test_binding_rejects_host_tensors():
+    torch = pytest.importorskip("torch")
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    with pytest.raises(LT.LucetreeError):
+        LT._ptr(torch.zeros(4))

@@ -199,7 +199,7 @@ def pages_needed(L: int, N: int) -> int:
 
 
 def generate(cfg: VerifyConfig, seed: int = 0, fill_unused: str = "nan",
-             with_logits: bool = True) -> dict:
+             with_logits: bool = True, with_pools: bool = True) -> dict:
     """Draw one verify step's inputs for ``cfg``.
 
     Returns numpy arrays (16-bit payloads as raw uint16 bits):
@@ -227,9 +227,11 @@ def generate(cfg: VerifyConfig, seed: int = 0, fill_unused: str = "nan",
     k_tree = _normal_bits(rng, (B, N, Hkv, D), cfg.dtype)
     v_tree = _normal_bits(rng, (B, N, Hkv, D), cfg.dtype)
 
-    k_pool = np.empty((num_pages, Hkv, PAGE, D), dtype=np.uint16)
-    v_pool = np.empty((num_pages, Hkv, PAGE, D), dtype=np.uint16)
-    if fill_unused == "nan":
+    k_pool = np.empty((num_pages if with_pools else 0, Hkv, PAGE, D), dtype=np.uint16)
+    v_pool = np.empty((num_pages if with_pools else 0, Hkv, PAGE, D), dtype=np.uint16)
+    if not with_pools:
+        pass
+    elif fill_unused == "nan":
         k_pool.fill(NAN_BITS[cfg.dtype])
         v_pool.fill(NAN_BITS[cfg.dtype])
     elif fill_unused == "zero":
@@ -237,7 +239,7 @@ def generate(cfg: VerifyConfig, seed: int = 0, fill_unused: str = "nan",
         v_pool.fill(0)
     elif fill_unused != "random":
         raise ValueError(fill_unused)
-    for b, L in enumerate(cfg.ctx):
+    for b, L in enumerate(cfg.ctx if with_pools else ()):
         full = L // PAGE
         for which in (k_pool, v_pool):
             if fill_unused == "random":
@@ -247,7 +249,7 @@ def generate(cfg: VerifyConfig, seed: int = 0, fill_unused: str = "nan",
             rem = L - full * PAGE
             if rem:
                 which[page_table[b, full], :, :rem, :] = _normal_bits(rng, (Hkv, rem, D), cfg.dtype)
-    if fill_unused == "random":
+    if fill_unused == "random" and with_pools:
         spare = order[at:]
         for which in (k_pool, v_pool):
             which[spare] = _normal_bits(rng, (len(spare), Hkv, PAGE, D), cfg.dtype)
