@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) merge_kernel(AttnLaunch L)
     const int g = h / p.G;
     const int rg = i / p.rg.NPG;
     const int rl = (i - rg * p.rg.NPG) * p.G + (h % p.G);
-    const int s = (b * p.Hkv + g) * p.rg.NG + rg;
+    const int s = b * p.Hkv + g;
 
     const T* qrow = reinterpret_cast<const T*>(a.q) + (size_t)row * D + lane * DPL;
     float qf[DPL];
@@ -81,9 +81,9 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) merge_kernel(AttnLaunch L)
         const long long nT = total_tiles(p, a.ctx_len);
         const long long first = segment_offset(p, a.ctx_len, s);
         const long long last = first + tiles_of(Lb) - 1;
-        const int c_lo = cta_of_tile(first, nT, p.C), c_hi = cta_of_tile(last, nT, p.C);
+        const int c_lo = cta_of_tile(first, nT, p.Cg), c_hi = cta_of_tile(last, nT, p.Cg);
         for (int c = c_lo; c <= c_hi; ++c) {
-            const float* slot = L.ws + (size_t)(c + s) * slot_floats(p);
+            const float* slot = L.ws + slot_index(p, rg, c, s) * slot_floats(p);
             const float mp = slot[(size_t)p.rg.RG * D + rl];
             const float lp = slot[(size_t)p.rg.RG * D + p.rg.RG + rl];
             if (!(mp > -INFINITY)) continue;  // split saw no valid key

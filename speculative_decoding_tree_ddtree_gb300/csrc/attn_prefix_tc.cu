@@ -1,0 +1,78 @@
+// attn_prefix_tc.cu -- host side of the tensor-core prefix kernel: TMA tensor
+// maps over the K/V pools and the queries, kernel selection by head dim,
+// operand type and padded row count.
+#include <cuda.h>
+
+#include "attn_prefix_tc.cuh"
+
+namespace lucetree {
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+int prefix_grid_ctas(int device) { return device_sm_count(device); }
+
+bool prefix_shape_supported(const lucetree_attn_args& a) {
+    // TMA row coordinates are 32-bit: the pool must stay below 2^31 rows
+    const long long rows = (long long)a.num_pages * a.Hkv * kPage;
+    return rows + kPage < (1ll << 31);
+}
+
+cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream) {
+    const lucetree_attn_args& a = L.a;
+    const PlanDims& p = L.plan;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const CUtensorMapDataType dt =
+        a.dtype == LUCETREE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint32_t estr[3] = {1, 1, 1};
+
+    // K, V pools as 2-D [num_pages * Hkv * 64 rows][D]; box = one 64-token page x 64 dims
+    CUtensorMap tk, tv, tq;
+    const cuuint64_t kv_dims[2] = {(cuuint64_t)a.D, (cuuint64_t)a.num_pages * a.Hkv * kPage};
+    const cuuint64_t kv_strides[1] = {(cuuint64_t)a.D * 2};
+    const cuuint32_t kv_box[2] = {64, (cuuint32_t)kPage};
+    if (enc(&tk, dt, 2, const_cast<void*>(a.k_pool), kv_dims, kv_strides, kv_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (enc(&tv, dt, 2, const_cast<void*>(a.v_pool), kv_dims, kv_strides, kv_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    // queries as 3-D [B*N nodes][Hq heads][D]; box = 64 dims x G heads x NPG nodes
+    const cuuint64_t q_dims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.N};
+    const cuuint64_t q_strides[2] = {(cuuint64_t)a.D * 2, (cuuint64_t)a.Hq * a.D * 2};
+    const cuuint32_t q_box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)p.rg.NPG};
+    if (enc(&tq, dt, 3, const_cast<void*>(a.q), q_dims, q_strides, q_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    const int rgp = (p.rg.RG + 15) / 16 * 16;
+    if (a.dtype == LUCETREE_BF16)
+        return a.D == 256 ? launch_prefix_tc_bf16_256(rgp, tk, tv, tq, L, stream)
+                          : launch_prefix_tc_bf16_128(rgp, tk, tv, tq, L, stream);
+    return a.D == 256 ? launch_prefix_tc_f16_256(rgp, tk, tv, tq, L, stream)
+                      : launch_prefix_tc_f16_128(rgp, tk, tv, tq, L, stream);
+}
+
+}  // namespace lucetree

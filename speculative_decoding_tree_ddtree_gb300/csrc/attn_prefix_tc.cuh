@@ -1,0 +1,605 @@
+// attn_prefix_tc.cuh -- committed-prefix part of tree-verify attention on the
+// 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA-fed operands).
+//
+// Orientation.  Per (sequence, KV head, row group) the query rows are the
+// (node, head-in-group) pairs: 132 at budget 22 with 6 heads per KV head.
+// Keys, not queries, go on the MMA's M = 128 dimension so the rows only pad
+// to a multiple of 16 (the MMA's N):
+//     S^T [128 keys x R]  = K_tile [128 x D]  . Q^T          (K-major A and B)
+//     O^T [D x R]        += V_tile^T [D x 128] . P^T [128 x R] (MN-major A and B)
+// TMEM (512 columns): S^T in [0, R), O^T in [160, 160+R) and [320, 320+R)
+// (d 0..127 and d 128..255).  TMEM lane l holds key l of S^T and output dim
+// l (+128) of O^T.
+//
+// Softmax over keys runs across TMEM lanes.  Each softmax thread owns one key
+// lane and keeps per-column partial sums in registers; the shift m[r] per
+// query row is stale on purpose: a tile whose scores all stay within 2^8 of
+// m (log2 domain) uses it unchanged, otherwise the tile takes the exact
+// column maxima (warp shuffles + shared memory) and rescales the partial sums
+// and the O^T columns that moved.  The first tile of every range takes that
+// path.  Sums are reduced across lanes once, at the end of the range.
+//
+// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2..5 = softmax and
+// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).  K and V stream through
+// a ring of 16 KB chunk slots ([128 keys][64 d], 128-byte swizzle), two TMA
+// boxes (one per 64-token page) per slot; a tile is D/64 K chunks then D/64 V
+// chunks, and V chunk pairs always land in slots (2j, 2j+1) so one MN-major
+// descriptor covers 128 output dims.  Every wait is bounded; a timeout sets
+// LUCETREE_DEV_TIMEOUT, drains this CTA's own copies and MMAs and returns.
+#pragma once
+
+#include "internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace lucetree {
+namespace prefix_tc {
+
+using namespace tc;
+
+constexpr int kThreads = 192;
+constexpr int kChunkBytes = 128 * 128;
+constexpr int kSmemLimit = 227 * 1024;
+constexpr float kTau = 8.0f;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO0 = 160, kColO1 = 320;
+constexpr int kMaxSlots = 12;
+
+// bf16 P keeps 8 significant bits, which alone puts ~1e-3 relative noise on
+// the output; with bf16 operands P is split into hi = bf16(p) and
+// lo = bf16(p - hi) and the PV contraction runs on both (P to ~2^-17).
+// fp16 P (11 bits) needs no split.
+template <int D, int RGP, bool SPLIT>
+struct Layout {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kNch = RGP / 16;
+    static constexpr int kQBytes = kChunks * RGP * 128;
+    static constexpr int kPOneBytes = RGP * 256;
+    static constexpr int kPBytes = kPOneBytes * (SPLIT ? 2 : 1);
+    static constexpr int kMiscBytes = 6144;
+    static constexpr int kRaw = (kSmemLimit - 1024 - kQBytes - kPBytes - kMiscBytes) / kChunkBytes;
+    static constexpr int kNS = (kRaw > kMaxSlots ? kMaxSlots : kRaw) & ~1;
+    static constexpr int kQOff = 0;
+    static constexpr int kPOff = kQBytes;
+    static constexpr int kSlotOff = ((kPOff + kPBytes + 1023) / 1024) * 1024;
+    static constexpr int kMiscOff = kSlotOff + kNS * kChunkBytes;
+    // force one CTA per SM: the kernel owns all 512 TMEM columns
+    static constexpr int kBytesRaw = kMiscOff + kMiscBytes + 1024;
+    static constexpr int kBytes = kBytesRaw < 120 * 1024 ? 120 * 1024 : kBytesRaw;
+    static_assert(kNS >= 2, "shared memory too small for the K/V ring");
+    static_assert(kBytes <= kSmemLimit, "shared memory budget");
+};
+
+struct Misc {
+    uint64_t full[kMaxSlots];
+    uint64_t empty[kMaxSlots];
+    uint64_t q_full, q_empty, s_full, p_full, o_full, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    float ex_red[4];
+    float m_ref[kRowsMax];
+    float alpha[kRowsMax];
+    float col_red[4][kRowsMax];
+};
+static_assert(sizeof(Misc) <= 6144, "misc region");
+
+struct Piece {
+    int s, b, g, L;
+    long long ta, te;  // tile range within the key segment
+};
+
+struct PieceIter {
+    long long t0, t1, off;
+    int s;
+    __device__ bool next(const PlanDims& p, const int32_t* ctx_len, Piece& out) {
+        while (s < p.S && off < t1) {
+            const int b = s / p.Hkv, g = s % p.Hkv;
+            const int L = seq_len_quiet(ctx_len, b, p.max_pages);
+            const long long nt = tiles_of(L);
+            const long long s0 = off, s1 = off + nt;
+            const int cur = s;
+            off = s1;
+            ++s;
+            if (nt == 0 || s1 <= t0) continue;
+            out.s = cur; out.b = b; out.g = g; out.L = L;
+            out.ta = (t0 > s0 ? t0 : s0) - s0;
+            out.te = (t1 < s1 ? t1 : s1) - s0;
+            return true;
+        }
+        return false;
+    }
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+__device__ __forceinline__ void set_abort(Misc* ms, uint32_t* status) {
+    if (atomicExch(&ms->abort_flag, 1) == 0) atomicOr(status, LUCETREE_DEV_TIMEOUT);
+}
+__device__ __forceinline__ bool aborted(Misc* ms) { return *(volatile int*)&ms->abort_flag != 0; }
+
+template <int D, bool BF16, int RGP>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefix_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_q, const AttnLaunch L) {
+    using Lay = Layout<D, RGP, BF16>;
+    constexpr int kChunks = Lay::kChunks;
+    constexpr int kNch = Lay::kNch;
+    constexpr int kNS = Lay::kNS;
+    constexpr uint32_t kAB = BF16 ? 1u : 0u;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem + Lay::kQOff;
+    uint8_t* sP = smem + Lay::kPOff;
+    uint8_t* sSlots = smem + Lay::kSlotOff;
+    Misc* ms = reinterpret_cast<Misc*>(smem + Lay::kMiscOff);
+
+    const lucetree_attn_args& a = L.a;
+    const PlanDims& p = L.plan;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rg = blockIdx.x / p.Cg, cta = blockIdx.x % p.Cg;
+    const int i0 = rg * p.rg.NPG;
+    const int R_seg = (min(p.N, i0 + p.rg.NPG) - i0) * p.G;
+    const int RG = p.rg.RG;
+
+    const long long nT = total_tiles(p, a.ctx_len);
+    const long long t0 = nT ? cta_begin(cta, nT, p.Cg) : 0, t1 = nT ? cta_begin(cta + 1, nT, p.Cg) : 0;
+    if (t0 >= t1) return;  // uniform across the CTA
+
+    // ---------------------------------------------------------------- set-up
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(&ms->full[i], 1);
+            mbar_init(&ms->empty[i], 1);
+        }
+        mbar_init(&ms->q_full, 1);
+        mbar_init(&ms->q_empty, 1);
+        mbar_init(&ms->s_full, 1);
+        mbar_init(&ms->p_full, 4);
+        mbar_init(&ms->o_full, 1);
+        mbar_init(&ms->drain, 1);
+        ms->abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp >= 2) {
+        // rows RG..RGP-1 of Q are padding: zero them once (TMA never writes them)
+        const int st = threadIdx.x - 64;
+        constexpr int kPadMax = RGP;  // bound
+        for (int idx = st; idx < kChunks * kPadMax * 8; idx += 128) {
+            const int c = idx / (kPadMax * 8), r = (idx / 8) % kPadMax, u = idx % 8;
+            if (r >= RG) *reinterpret_cast<uint4*>(sQ + c * RGP * 128 + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(&ms->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_q);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ms->tmem_base;
+
+    if (warp == 0) {
+        // ============================================================ TMA producer
+        const int oob_row = a.num_pages * p.Hkv * kPage;  // first row past the pool: zero fill
+        uint32_t chunk = 0;
+        int piece_no = 0;
+        bool ok = true;
+        PieceIter it{t0, t1, 0, 0};
+        Piece pc;
+        while (ok && it.next(p, a.ctx_len, pc)) {
+            if (piece_no > 0) ok = mbar_wait(&ms->q_empty, (piece_no - 1) & 1);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&ms->q_full, kChunks * RG * 128);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(sQ + c * RGP * 128, &tm_q, 64 * c, pc.g * p.G, pc.b * p.N + i0, &ms->q_full);
+            }
+            __syncwarp();
+            const int npages = (pc.L + kPage - 1) / kPage;
+            const int32_t* pt = a.page_table + (size_t)pc.b * p.max_pages;
+            int batch_pid = -1;
+            for (long long t = pc.ta; t < pc.te && ok; ++t) {
+                if (((t - pc.ta) & 15) == 0) {
+                    const long long pg = 2 * t + lane;
+                    batch_pid = -1;
+                    if (pg < npages && 2 * (t - pc.ta) + lane < 2 * (pc.te - pc.ta)) {
+                        const int pid = pt[pg];
+                        if (pid >= 0 && pid < a.num_pages) batch_pid = pid;
+                        else atomicOr(a.status, LUCETREE_DEV_BAD_PAGE);
+                    }
+                }
+                int row[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int pid = __shfl_sync(0xffffffffu, batch_pid, (int)(2 * ((t - pc.ta) & 15) + h));
+                    row[h] = pid >= 0 ? (pid * p.Hkv + pc.g) * kPage : oob_row;
+                }
+#pragma unroll 1
+                for (int part = 0; part < 2 * kChunks; ++part) {
+                    const int slot = chunk % kNS;
+                    if (!mbar_wait(&ms->empty[slot], ((chunk / kNS) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const CUtensorMap* m = part < kChunks ? &tm_k : &tm_v;
+                        const int c = part % kChunks;
+                        uint8_t* dst = sSlots + slot * kChunkBytes;
+                        mbar_arrive_expect_tx(&ms->full[slot], kChunkBytes);
+                        tma_load_2d(dst, m, 64 * c, row[0], &ms->full[slot]);
+                        tma_load_2d(dst + 8192, m, 64 * c, row[1], &ms->full[slot]);
+                    }
+                    __syncwarp();
+                    ++chunk;
+                }
+            }
+            ++piece_no;
+        }
+        if (!ok || aborted(ms)) {
+            set_abort(ms, a.status);
+            // wait (bounded) for this CTA's own copies still in flight
+            if (lane == 0) {
+                const uint32_t first = chunk > (uint32_t)kNS ? chunk - kNS : 0u;
+                for (uint32_t c = first; c < chunk; ++c) mbar_wait(&ms->full[c % kNS], (c / kNS) & 1, 200000000ll);
+            }
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_qk = idesc_f16(128, RGP, kAB, 0, 0);
+            const uint32_t id_pv = idesc_f16(128, RGP, kAB, 1, 1);
+            constexpr uint64_t hi_k = desc_hi(16, 1024, kLayoutSwizzle128);
+            constexpr uint64_t hi_v = desc_hi(kChunkBytes, 1024, kLayoutSwizzle128);
+            constexpr uint64_t hi_p = desc_hi(128, 2048, kLayoutInterleave);
+            const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aS = smem_u32(sSlots);
+            uint32_t chunk = 0;
+            int J = 0, piece_no = 0;
+            bool ok = true;
+            PieceIter it{t0, t1, 0, 0};
+            Piece pc;
+            while (ok && it.next(p, a.ctx_len, pc)) {
+                if (!(ok = mbar_wait(&ms->q_full, piece_no & 1))) break;
+                for (long long t = pc.ta; t < pc.te; ++t) {
+                    if (aborted(ms)) { ok = false; break; }
+                    // S^T = K . Q^T  (S^T is free: the previous tile's p_full was observed)
+                    for (int c = 0; c < kChunks && ok; ++c) {
+                        const int slot = chunk % kNS;
+                        if (!(ok = mbar_wait(&ms->full[slot], (chunk / kNS) & 1))) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int sub = 0; sub < 4; ++sub) {
+                            const uint64_t ad = make_desc(hi_k, aS + slot * kChunkBytes + sub * 32);
+                            const uint64_t bd = make_desc(hi_k, aQ + c * RGP * 128 + sub * 32);
+                            mma_f16_ss(tmem, ad, bd, id_qk, (c | sub) != 0);
+                        }
+                        mma_commit(&ms->empty[slot]);
+                        ++chunk;
+                    }
+                    if (!ok) break;
+                    if (t == pc.te - 1) mma_commit(&ms->q_empty);
+                    mma_commit(&ms->s_full);
+                    // O^T += V^T . P^T once the softmax has written P^T
+                    if (!(ok = mbar_wait(&ms->p_full, J & 1))) break;
+                    tc_fence_after();
+                    for (int h = 0; h < kChunks / 2 && ok; ++h) {
+                        const int slot = chunk % kNS;  // even; its pair is slot + 1
+                        if (!(ok = mbar_wait(&ms->full[slot], (chunk / kNS) & 1))) break;
+                        if (!(ok = mbar_wait(&ms->full[slot + 1], ((chunk + 1) / kNS) & 1))) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint64_t ad = make_desc(hi_v, aS + slot * kChunkBytes + ks * 2048);
+                            const uint64_t bd = make_desc(hi_p, aP + ks * 256);
+                            mma_f16_ss(tmem + (h ? kColO1 : kColO0), ad, bd, id_pv, !(t == pc.ta && ks == 0));
+                        }
+                        if constexpr (BF16) {
+                            // the lo part of P against the same V
+#pragma unroll
+                            for (int ks = 0; ks < 8; ++ks) {
+                                const uint64_t ad = make_desc(hi_v, aS + slot * kChunkBytes + ks * 2048);
+                                const uint64_t bd = make_desc(hi_p, aP + Lay::kPOneBytes + ks * 256);
+                                mma_f16_ss(tmem + (h ? kColO1 : kColO0), ad, bd, id_pv, 1u);
+                            }
+                        }
+                        mma_commit(&ms->empty[slot]);
+                        mma_commit(&ms->empty[slot + 1]);
+                        chunk += 2;
+                    }
+                    if (!ok) break;
+                    if (t == pc.te - 1) mma_commit(&ms->o_full);
+                    ++J;
+                }
+                ++piece_no;
+            }
+            if (!ok || aborted(ms)) {
+                set_abort(ms, a.status);
+                mma_commit(&ms->drain);  // every MMA issued so far has finished before TMEM is freed
+                mbar_wait(&ms->drain, 0, 200000000ll);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ============================================================ softmax + epilogue
+        const int quarter = warp & 3;
+        const int kl = quarter * 32 + lane;  // key lane of S^T, output dim of O^T
+        const int st = threadIdx.x - 64;     // 0..127
+        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float sl2 = L.scale_log2;
+        int J = 0, piece_no = 0;
+        bool bad = false;
+        PieceIter it{t0, t1, 0, 0};
+        Piece pc;
+        while (it.next(p, a.ctx_len, pc)) {
+            const int npages = (pc.L + kPage - 1) / kPage;
+            const int32_t* pt = a.page_table + (size_t)pc.b * p.max_pages;
+            bar_sync(1, 128);
+            for (int col = st; col < RGP; col += 128) ms->m_ref[col] = -INFINITY;
+            bar_sync(1, 128);
+            float lpart[RGP];
+#pragma unroll
+            for (int col = 0; col < RGP; ++col) lpart[col] = 0.f;
+
+            for (long long t = pc.ta; t < pc.te; ++t, ++J) {
+                const int nvalid = (int)min((long long)kTileKeys, (long long)pc.L - t * kTileKeys);
+                const long long pg = 2 * t + (kl >> 6);
+                bool page_ok = false;
+                if (pg < npages) {
+                    const int pid = pt[pg];
+                    page_ok = pid >= 0 && pid < a.num_pages;
+                }
+                const bool valid = kl < nvalid && page_ok;
+                const bool got = mbar_wait(&ms->s_full, J & 1);
+                if (bar_sync_or(1, 128, bad || !got)) {
+                    bad = true;
+                    break;
+                }
+                tc_fence_after();
+
+                // pass 1: largest exponent this tile would use with the current shifts
+                float ex = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kNch; ++c) {
+                    uint32_t r[16];
+                    tmem_ld16(tl + 16 * c, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = 16 * c + j;
+                        if (valid && col < R_seg) ex = fmaxf(ex, fmaf(__uint_as_float(r[j]), sl2, -ms->m_ref[col]));
+                    }
+                }
+                ex = warp_max(ex);
+                if (lane == 0) ms->ex_red[quarter] = ex;
+                bar_sync(1, 128);
+                ex = fmaxf(fmaxf(ms->ex_red[0], ms->ex_red[1]), fmaxf(ms->ex_red[2], ms->ex_red[3]));
+
+                if (ex > kTau) {
+                    // slow path: exact column maxima of this tile, then move the shifts
+#pragma unroll
+                    for (int c = 0; c < kNch; ++c) {
+                        uint32_t r[16];
+                        tmem_ld16(tl + 16 * c, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = 16 * c + j;
+                            float y = (valid && col < R_seg) ? __uint_as_float(r[j]) * sl2 : -INFINITY;
+                            y = warp_max(y);
+                            if (lane == 0) ms->col_red[quarter][col] = y;
+                        }
+                    }
+                    bar_sync(1, 128);
+                    for (int col = st; col < RGP; col += 128) {
+                        const float cm = fmaxf(fmaxf(ms->col_red[0][col], ms->col_red[1][col]),
+                                               fmaxf(ms->col_red[2][col], ms->col_red[3][col]));
+                        const float mo = ms->m_ref[col];
+                        const float mn = fmaxf(mo, cm);
+                        ms->alpha[col] = mn > mo ? ex2(mo - mn) : 1.f;
+                        ms->m_ref[col] = mn;
+                    }
+                    bar_sync(1, 128);
+#pragma unroll
+                    for (int col = 0; col < RGP; ++col) lpart[col] *= ms->alpha[col];
+                    if (t != pc.ta) {
+                        // O^T columns accumulated so far move with their shift
+#pragma unroll
+                        for (int c = 0; c < kNch; ++c) {
+                            bool any = false;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) any |= ms->alpha[16 * c + j] != 1.f;
+                            if (!any) continue;
+#pragma unroll
+                            for (int h = 0; h < kChunks / 2; ++h) {
+                                uint32_t r[16];
+                                const uint32_t addr = tl + (h ? kColO1 : kColO0) + 16 * c;
+                                tmem_ld16(addr, r);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    r[j] = __float_as_uint(__uint_as_float(r[j]) * ms->alpha[16 * c + j]);
+                                tmem_st16(addr, r);
+                            }
+                        }
+                        tmem_wait_st();
+                    }
+                }
+
+                // pass 2: P = 2^(s*scale*log2e - m), row sums, P^T to shared memory
+#pragma unroll
+                for (int c = 0; c < kNch; ++c) {
+                    uint32_t r[16];
+                    tmem_ld16(tl + 16 * c, r);
+                    tmem_wait_ld();
+                    float pv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = 16 * c + j;
+                        const float x = fmaf(__uint_as_float(r[j]), sl2, -ms->m_ref[col]);
+                        pv[j] = (valid && col < R_seg) ? ex2(x) : 0.f;
+                        lpart[col] += pv[j];
+                    }
+                    uint32_t w[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) w[k] = pack2<BF16>(pv[2 * k], pv[2 * k + 1]);
+                    *reinterpret_cast<uint4*>(sP + (2 * c) * 2048 + kl * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(sP + (2 * c + 1) * 2048 + kl * 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                    if constexpr (BF16) {
+                        // residual p - bf16(p): bf16 keeps the top 16 bits of the fp32 pattern
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float h0 = __uint_as_float(w[k] << 16), h1 = __uint_as_float(w[k] & 0xFFFF0000u);
+                            w[k] = pack2<true>(pv[2 * k] - h0, pv[2 * k + 1] - h1);
+                        }
+                        uint8_t* lo = sP + Lay::kPOneBytes;
+                        *reinterpret_cast<uint4*>(lo + (2 * c) * 2048 + kl * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4*>(lo + (2 * c + 1) * 2048 + kl * 16) =
+                            make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                }
+
+                // keys past L inside the last (partial) page: their V rows hold
+                // whatever the pool has there; zero them so 0 * V stays 0
+                if ((nvalid & (kPage - 1)) != 0 && kl >= nvalid && kl < ((nvalid + kPage - 1) & ~(kPage - 1)) &&
+                    page_ok) {
+                    const uint32_t vbase = (uint32_t)J * (2 * kChunks) + kChunks;
+                    for (int c = 0; c < kChunks; ++c) {
+                        const uint32_t ch = vbase + c;
+                        if (!mbar_wait(&ms->full[ch % kNS], (ch / kNS) & 1)) {
+                            bad = true;
+                            break;
+                        }
+                        uint8_t* row = sSlots + (ch % kNS) * kChunkBytes + (kl >> 6) * 8192 + (kl & 63) * 128;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) reinterpret_cast<uint4*>(row)[u] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ms->p_full);
+            }
+            if (bad) break;
+
+            // ---------------------------------------------------------- epilogue
+            const bool got = mbar_wait(&ms->o_full, piece_no & 1);
+            if (bar_sync_or(1, 128, bad || !got)) {
+                bad = true;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int col = 0; col < RGP; ++col) {
+                const float v = warp_sum(lpart[col]);
+                if (lane == 0) ms->col_red[quarter][col] = v;
+            }
+            bar_sync(1, 128);
+            float* slot = L.ws + slot_index(p, rg, cta, pc.s) * slot_floats(p);
+            float* slot_m = slot + (size_t)RG * D;
+            float* slot_l = slot_m + RG;
+            for (int col = st; col < R_seg; col += 128) {
+                slot_l[col] = ms->col_red[0][col] + ms->col_red[1][col] + ms->col_red[2][col] + ms->col_red[3][col];
+                slot_m[col] = ms->m_ref[col];
+            }
+#pragma unroll
+            for (int c = 0; c < kNch; ++c) {
+#pragma unroll
+                for (int h = 0; h < kChunks / 2; ++h) {
+                    uint32_t r[16];
+                    tmem_ld16(tl + (h ? kColO1 : kColO0) + 16 * c, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = 16 * c + j;
+                        if (col < R_seg) slot[(size_t)col * D + h * 128 + kl] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            ++piece_no;
+        }
+        if (bad) set_abort(ms, a.status);
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D, bool BF16, int RGP>
+cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq, const AttnLaunch& L,
+                       cudaStream_t stream) {
+    using Lay = Layout<D, RGP, BF16>;
+    auto kern = prefix_tc_kernel<D, BF16, RGP>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    kern<<<grid_ctas(L.plan), kThreads, Lay::kBytes, stream>>>(tk, tv, tq, L);
+    return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_rgp(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                       const AttnLaunch& L, cudaStream_t stream) {
+    switch (rgp) {
+        case 16: return launch_one<D, BF16, 16>(tk, tv, tq, L, stream);
+        case 32: return launch_one<D, BF16, 32>(tk, tv, tq, L, stream);
+        case 48: return launch_one<D, BF16, 48>(tk, tv, tq, L, stream);
+        case 64: return launch_one<D, BF16, 64>(tk, tv, tq, L, stream);
+        case 80: return launch_one<D, BF16, 80>(tk, tv, tq, L, stream);
+        case 96: return launch_one<D, BF16, 96>(tk, tv, tq, L, stream);
+        case 112: return launch_one<D, BF16, 112>(tk, tv, tq, L, stream);
+        case 128: return launch_one<D, BF16, 128>(tk, tv, tq, L, stream);
+        case 144: return launch_one<D, BF16, 144>(tk, tv, tq, L, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace prefix_tc
+
+cudaError_t launch_prefix_tc_bf16_256(int rgp, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                      const AttnLaunch&, cudaStream_t);
+cudaError_t launch_prefix_tc_bf16_128(int rgp, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                      const AttnLaunch&, cudaStream_t);
+cudaError_t launch_prefix_tc_f16_256(int rgp, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                     const AttnLaunch&, cudaStream_t);
+cudaError_t launch_prefix_tc_f16_128(int rgp, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                     const AttnLaunch&, cudaStream_t);
+
+}  // namespace lucetree

@@ -1,0 +1,11 @@
+// Instantiations of the tensor-core prefix kernel for bf16 operands, head dim 128.
+#include "attn_prefix_tc.cuh"
+
+namespace lucetree {
+
+cudaError_t launch_prefix_tc_bf16_128(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                                   const AttnLaunch& L, cudaStream_t stream) {
+    return prefix_tc::launch_rgp<128, true>(rgp, tk, tv, tq, L, stream);
+}
+
+}  // namespace lucetree

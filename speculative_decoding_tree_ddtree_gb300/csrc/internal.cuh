@@ -16,14 +16,14 @@ namespace lucetree {
 // Query rows of one (sequence b, KV head g) are the N*G pairs (node i, head
 // h' in the group).  They are cut into NG row groups of NPG consecutive nodes
 // so a group has at most kRowsMax rows (the tensor-core tile's N extent).
-// A "segment" is one (b, g, row group); segments are numbered
-//   s = (b * Hkv + g) * NG + rg
-// and each owns ceil(L_b / kTileKeys) key tiles.  Concatenating all segments'
-// tiles gives a flat list of T tiles; CTA c of a C-CTA persistent grid takes
-// tiles [floor(c*T/C), floor((c+1)*T/C)).  A CTA writes one partial
-// (O, max, sum) per segment its range touches, into workspace slot c + s; the
-// pair (c, s) is unique because both partitions are ordered, so C + S - 1
-// slots always suffice.
+// A "key segment" is one (b, g), s = b * Hkv + g, owning ceil(L_b / kTileKeys)
+// key tiles.  Concatenating the segments' tiles gives a flat list of T tiles.
+// The grid is NG sub-grids of Cg CTAs; CTA c of sub-grid rg takes tiles
+// [floor(c*T/Cg), floor((c+1)*T/Cg)) for row group rg, so the NG CTAs that
+// need the same K/V tiles stream them at the same time.  A CTA writes one
+// partial (O, max, sum) per key segment its range touches, into workspace slot
+// rg * (Cg + S - 1) + c + s; (c, s) is unique because both partitions are
+// ordered, so Cg + S - 1 slots per row group always suffice.
 // ---------------------------------------------------------------------------
 constexpr int kTileKeys = 128;  // keys per tile: two 64-token pages
 constexpr int kRowsMax = 144;   // rows per CTA (multiple of 16)
@@ -44,6 +44,7 @@ __host__ __device__ inline RowGroups make_row_groups(int N, int G) {
         r.NG += 1;
         r.NPG = (N + r.NG - 1) / r.NG;
     }
+    r.NG = (N + r.NPG - 1) / r.NPG;  // no empty trailing group
     r.RG = r.NPG * G;
     return r;
 }
@@ -51,29 +52,35 @@ __host__ __device__ inline RowGroups make_row_groups(int N, int G) {
 struct PlanDims {
     int B, N, Hq, Hkv, D, G;
     RowGroups rg;
-    int S;         // segments
-    int C;         // CTAs of the prefix grid
-    int max_pages; // page-table row length
+    int S;          // key segments = B * Hkv
+    int Cg;         // CTAs per row group
+    int max_pages;  // page-table row length
 };
 
-__host__ __device__ inline PlanDims make_plan(int B, int N, int Hq, int Hkv, int D, int C, int max_pages) {
+__host__ __device__ inline PlanDims make_plan(int B, int N, int Hq, int Hkv, int D, int ctas, int max_pages) {
     PlanDims p;
     p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
     p.rg = make_row_groups(N, p.G);
-    p.S = B * Hkv * p.rg.NG;
-    p.C = C;
+    p.S = B * Hkv;
+    p.Cg = ctas / p.rg.NG;
+    if (p.Cg < 1) p.Cg = 1;
     p.max_pages = max_pages;
     return p;
 }
+
+__host__ __device__ inline int grid_ctas(const PlanDims& p) { return p.Cg * p.rg.NG; }
 
 // floats per workspace slot: O [RG][D], then max [RG], then sum [RG]
 __host__ __device__ inline size_t slot_floats(const PlanDims& p) {
     return (size_t)p.rg.RG * (p.D + 2);
 }
 
+__host__ __device__ inline size_t slot_index(const PlanDims& p, int rg, int c, int s) {
+    return (size_t)rg * (p.Cg + p.S - 1) + c + s;
+}
+
 __host__ __device__ inline size_t attn_workspace_bytes(const PlanDims& p) {
-    size_t slots = (size_t)p.C + p.S - 1;
-    return slots * slot_floats(p) * sizeof(float);
+    return (size_t)p.rg.NG * (p.Cg + p.S - 1) * slot_floats(p) * sizeof(float);
 }
 
 // Committed length used by the kernels: out-of-range values count as 0.
@@ -94,20 +101,19 @@ __device__ inline int seq_len_quiet(const int32_t* ctx_len, int b, int max_pages
 
 __device__ inline long long tiles_of(int L) { return (L + kTileKeys - 1) / kTileKeys; }
 
-// Total flat tiles over all segments.
+// Total flat tiles over all key segments.
 __device__ inline long long total_tiles(const PlanDims& p, const int32_t* ctx_len) {
     long long t = 0;
     for (int b = 0; b < p.B; ++b) t += tiles_of(seq_len_quiet(ctx_len, b, p.max_pages));
-    return t * p.Hkv * p.rg.NG;
+    return t * p.Hkv;
 }
 
-// Flat offset of segment s's first tile.
+// Flat offset of key segment s's first tile.
 __device__ inline long long segment_offset(const PlanDims& p, const int32_t* ctx_len, int s) {
-    int per_seq = p.Hkv * p.rg.NG;
-    int b = s / per_seq, within = s % per_seq;
+    const int b = s / p.Hkv, g = s % p.Hkv;
     long long off = 0;
-    for (int bb = 0; bb < b; ++bb) off += tiles_of(seq_len_quiet(ctx_len, bb, p.max_pages)) * per_seq;
-    return off + (long long)within * tiles_of(seq_len_quiet(ctx_len, b, p.max_pages));
+    for (int bb = 0; bb < b; ++bb) off += tiles_of(seq_len_quiet(ctx_len, bb, p.max_pages)) * p.Hkv;
+    return off + (long long)g * tiles_of(seq_len_quiet(ctx_len, b, p.max_pages));
 }
 
 __device__ inline long long cta_begin(long long c, long long T, int C) { return c * T / C; }
@@ -175,6 +181,7 @@ struct AttnLaunch {
 };
 
 int prefix_grid_ctas(int device);  // persistent grid size of the prefix kernel
+bool prefix_shape_supported(const lucetree_attn_args& a);
 cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_merge(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_build_anc(const int32_t* parent, int B, int N, uint64_t* anc, uint32_t* status,

@@ -77,6 +77,7 @@ lucetree_status lucetree_verify_attn(const lucetree_attn_args* a, void* workspac
         !aligned16(a->v_tree) || !aligned16(a->out))
         return LUCETREE_ERR_INVALID_ARG;
     if (!isfinite(a->scale)) return LUCETREE_ERR_INVALID_ARG;
+    if (!prefix_shape_supported(*a)) return LUCETREE_ERR_UNSUPPORTED;
     const int dev = current_device();
     AttnLaunch L;
     L.a = *a;
