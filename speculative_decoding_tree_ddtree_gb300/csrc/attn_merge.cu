@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) merge_kernel(AttnLaunch L)
         const long long last = first + tiles_of(Lb) - 1;
         const int c_lo = cta_of_tile(first, nT, p.Cg), c_hi = cta_of_tile(last, nT, p.Cg);
         for (int c = c_lo; c <= c_hi; ++c) {
+            // with fewer tiles than CTAs some CTAs own no tile and write no partial
+            if (cta_begin(c, nT, p.Cg) == cta_begin(c + 1, nT, p.Cg)) continue;
             const float* slot = L.ws + slot_index(p, rg, c, s) * slot_floats(p);
             const float mp = slot[(size_t)p.rg.RG * D + rl];
             const float lp = slot[(size_t)p.rg.RG * D + p.rg.RG + rl];

@@ -63,7 +63,7 @@ def run_attention(d: dict, cfg: W.VerifyConfig, anc=None, lse=False):
         anc = torch.empty(B, N, dtype=torch.int64, device=dev)
         LT.lucetree_build_anc_mask(d["parent"], anc, status)
     ws = torch.empty(LT.lucetree_verify_attn_workspace(B, N, Hq, Hkv, D), dtype=torch.uint8, device=dev)
-    ws.fill_(0xFF)  # NaN-poisoned workspace: unwritten partials would show up
+    ws.fill_(0x3F)  # finite garbage (0.747f): a partial read before it is written shows up as a wrong result
     out = torch.full((B, N, Hq, D), float("nan"), dtype=torch.float32, device=dev)
     lse_t = torch.full((B, N, Hq), float("nan"), dtype=torch.float32, device=dev) if lse else None
     LT.lucetree_verify_attn(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"],
