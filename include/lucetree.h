@@ -127,6 +127,29 @@ LUCETREE_API lucetree_status lucetree_verify_attn(const lucetree_attn_args* args
                                      void* stream);
 
 /*
+ * lucetree_verify_attn without a caller-supplied workspace.  The Lucebox
+ * pages have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory: a serving process that has handed all free device
+ * memory to its KV page pool up front, or a plugin / foreign-language host
+ * that only receives raw device pointers and has no allocator of its own.
+ * It computes exactly what lucetree_verify_attn computes (same kernels), and
+ * allocates nothing: the split-K partials go to a file-scope device array of
+ * 32 MiB (33554432 bytes) inside this library, which every GPU that loads the
+ * library keeps until the process exits.
+ *   - Sizes whose workspace (lucetree_verify_attn_workspace) exceeds 32 MiB
+ *     are rejected with LUCETREE_ERR_WORKSPACE before anything is launched;
+ *     other errors are those of lucetree_verify_attn.
+ *   - The first call on a device (made with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents (the kernels need none of it cleared).  Calls whose
+ *     work overlaps on the GPU (different streams, or host threads without
+ *     ordering) race on it; serialise them.
+ */
+LUCETREE_API lucetree_status lucetree_verify_attn_noalloc(const lucetree_attn_args* args, void* stream);
+
+/*
  * anc[b][i] = bit i | anc[b][parent[b][i]] (parent -1 = the root, which holds
  * no bit).  Requires parent[b][i] in [-1, i) (topological order); otherwise
  * BAD_PARENT is raised and anc[b][i] holds bit i only.  parent [B][N],

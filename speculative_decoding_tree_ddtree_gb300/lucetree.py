@@ -38,6 +38,7 @@ EXPORTED = (
     "lucetree_commit",
     "lucetree_status_string",
     "lucetree_abi_version",
+    "lucetree_verify_attn_noalloc",
 )
 
 
@@ -91,6 +92,7 @@ def load(path: str | None = None):
     lib.lucetree_status_string.argtypes = [I]
     lib.lucetree_status_string.restype = ctypes.c_char_p
     lib.lucetree_abi_version.argtypes = []
+    lib.lucetree_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnArgs), P]
     for name in EXPORTED:
         if name not in ("lucetree_status_string", "lucetree_abi_version"):
             getattr(lib, name).restype = I
@@ -232,3 +234,34 @@ class VerifyStep:
                         self.status, stream)
         lucetree_commit(k_tree, v_tree, self.acc_nodes, self.acc_len, page_table, ctx_len, self.ctx_out, k_pool,
                         v_pool, self.status, stream)
+
+
+# ---------------------------------------------------------------- allocation-free variant
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def lucetree_verify_attn_noalloc(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status,
+                                 lse=None, scale: float | None = None, stream=None):
+    """lucetree_verify_attn for callers that cannot allocate device memory: the
+    split-K scratch is a fixed 32 MiB device array inside the library (shared
+    by every call on a device; calls that overlap on the GPU race on it).  The
+    first call on a device looks up that array's address, so make it before
+    any stream capture.  Shapes whose workspace would exceed 32 MiB raise."""
+    B, N, Hq, D = q.shape
+    Hkv = k_pool.shape[1]
+    need = lucetree_verify_attn_workspace(B, N, Hq, Hkv, D)
+    if need > NOALLOC_SCRATCH_BYTES:
+        raise LucetreeError(f"lucetree_verify_attn_noalloc: these sizes need {need} bytes of scratch, "
+                            f"more than the fixed {NOALLOC_SCRATCH_BYTES}")
+    a = AttnArgs()
+    a.dtype = dtype_code(q)
+    a.B, a.N, a.Hq, a.Hkv, a.D = B, N, Hq, Hkv, D
+    a.page_size = k_pool.shape[2]
+    a.scale = float(scale) if scale is not None else float(D) ** -0.5
+    a.q, a.k_pool, a.v_pool = _ptr(q), _ptr(k_pool), _ptr(v_pool)
+    a.num_pages = k_pool.shape[0]
+    a.page_table, a.max_pages_per_seq = _ptr(page_table), page_table.shape[1]
+    a.ctx_len, a.k_tree, a.v_tree, a.anc_mask = _ptr(ctx_len), _ptr(k_tree), _ptr(v_tree), _ptr(anc_mask)
+    a.out, a.lse, a.status = _ptr(out), _ptr(lse), _ptr(status)
+    _check(load().lucetree_verify_attn_noalloc(ctypes.byref(a), _stream(stream)))
