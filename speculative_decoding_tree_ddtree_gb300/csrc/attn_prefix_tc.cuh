@@ -13,14 +13,19 @@
 //
 // Softmax over keys runs across TMEM lanes.  Each softmax thread owns one key
 // lane and keeps per-column partial sums in registers; the shift m[r] per
-// query row is stale on purpose: a tile whose scores all stay within 2^8 of
-// m (log2 domain) uses it unchanged, otherwise the tile takes the exact
-// column maxima (warp shuffles + shared memory) and rescales the partial sums
-// and the O^T columns that moved.  The first tile of every range takes that
-// path.  Sums are reduced across lanes once, at the end of the range.
+// query row is stale on purpose.  A tile is first exponentiated with the
+// current shifts (one pass: P^T written, sums accumulated, largest exponent
+// tracked); if any exponent exceeds 8 (log2 domain) the pass is taken back
+// out exactly, the tile's column maxima are found (warp shuffles + shared
+// memory) and the partial sums and already-accumulated O^T columns are
+// rescaled before the tile is redone.  The first tile of every range goes
+// straight to that path.  Sums are reduced across lanes once per range.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2..5 = softmax and
-// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).  K and V stream through
+// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2..13 = softmax and
+// epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and handles one third of
+// the row tile's column chunks, so three warps share each lane quarter (the
+// per-column partial sums then fit in registers) and hide each other's
+// latency.  K and V stream through
 // a ring of 16 KB chunk slots ([128 keys][64 d], 128-byte swizzle), two TMA
 // boxes (one per 64-token page) per slot; a tile is D/64 K chunks then D/64 V
 // chunks, and V chunk pairs always land in slots (2j, 2j+1) so one MN-major
@@ -36,7 +41,11 @@ namespace prefix_tc {
 
 using namespace tc;
 
-constexpr int kThreads = 192;
+constexpr int kSmGroups = 3;                        // softmax warps per TMEM lane quarter
+constexpr int kSmWarps = 4 * kSmGroups;             // 12 softmax warps
+constexpr int kSoftmaxThreads = 32 * kSmWarps;      // 384
+constexpr int kThreads = 64 + kSoftmaxThreads;      // + producer warp + MMA warp
+
 constexpr int kChunkBytes = 128 * 128;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr float kTau = 8.0f;
@@ -70,15 +79,15 @@ struct Layout {
 };
 
 struct Misc {
+    alignas(16) float m_ref[kRowsMax];
+    alignas(16) float alpha[kRowsMax];
+    alignas(16) float col_red[4][kRowsMax];
+    float ex_red[kSmWarps];
     uint64_t full[kMaxSlots];
     uint64_t empty[kMaxSlots];
     uint64_t q_full, q_empty, s_full, p_full, o_full, drain;
     uint32_t tmem_base;
     int abort_flag;
-    float ex_red[4];
-    float m_ref[kRowsMax];
-    float alpha[kRowsMax];
-    float col_red[4][kRowsMax];
 };
 static_assert(sizeof(Misc) <= 6144, "misc region");
 
@@ -149,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Lay = Layout<D, RGP, BF16>;
     constexpr int kChunks = Lay::kChunks;
     constexpr int kNch = Lay::kNch;
+    constexpr int kNa = (kNch + kSmGroups - 1) / kSmGroups;  // column chunks per softmax warp (at most)
     constexpr int kNS = Lay::kNS;
     constexpr uint32_t kAB = BF16 ? 1u : 0u;
 
@@ -180,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ms->q_full, 1);
         mbar_init(&ms->q_empty, 1);
         mbar_init(&ms->s_full, 1);
-        mbar_init(&ms->p_full, 4);
+        mbar_init(&ms->p_full, kSmWarps);
         mbar_init(&ms->o_full, 1);
         mbar_init(&ms->drain, 1);
         ms->abort_flag = 0;
@@ -190,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rows RG..RGP-1 of Q are padding: zero them once (TMA never writes them)
         const int st = threadIdx.x - 64;
         constexpr int kPadMax = RGP;  // bound
-        for (int idx = st; idx < kChunks * kPadMax * 8; idx += 128) {
+        for (int idx = st; idx < kChunks * kPadMax * 8; idx += kSoftmaxThreads) {
             const int c = idx / (kPadMax * 8), r = (idx / 8) % kPadMax, u = idx % 8;
             if (r >= RG) *reinterpret_cast<uint4*>(sQ + c * RGP * 128 + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
         }
@@ -229,21 +239,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             const int npages = (pc.L + kPage - 1) / kPage;
             const int32_t* pt = a.page_table + (size_t)pc.b * p.max_pages;
-            int batch_pid = -1;
+            // page ids of this piece, 16 tiles (32 pages) per warp-wide load, one batch ahead
+            auto load_batch = [&](long long tb) {
+                const long long pg = 2 * tb + lane;
+                int pid = -1;
+                if (pg < npages && pg < 2 * pc.te) {
+                    const int v = pt[pg];
+                    if (v >= 0 && v < a.num_pages) pid = v;
+                    else atomicOr(a.status, LUCETREE_DEV_BAD_PAGE);
+                }
+                return pid;
+            };
+            int pid_cur = load_batch(pc.ta), pid_next = load_batch(pc.ta + 16);
             for (long long t = pc.ta; t < pc.te && ok; ++t) {
-                if (((t - pc.ta) & 15) == 0) {
-                    const long long pg = 2 * t + lane;
-                    batch_pid = -1;
-                    if (pg < npages && 2 * (t - pc.ta) + lane < 2 * (pc.te - pc.ta)) {
-                        const int pid = pt[pg];
-                        if (pid >= 0 && pid < a.num_pages) batch_pid = pid;
-                        else atomicOr(a.status, LUCETREE_DEV_BAD_PAGE);
-                    }
+                const long long rel = t - pc.ta;
+                if (rel > 0 && (rel & 15) == 0) {
+                    pid_cur = pid_next;
+                    pid_next = load_batch(t + 16);
                 }
                 int row[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int pid = __shfl_sync(0xffffffffu, batch_pid, (int)(2 * ((t - pc.ta) & 15) + h));
+                    const int pid = __shfl_sync(0xffffffffu, pid_cur, (int)(2 * (rel & 15) + h));
                     row[h] = pid >= 0 ? (pid * p.Hkv + pc.g) * kPage : oob_row;
                 }
 #pragma unroll 1
@@ -352,147 +369,204 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ============================================================ softmax + epilogue
+        // 12 warps: warp w reads TMEM lanes 32*(w%4)..+31 (its key lanes) and
+        // handles share hf = (w-2)/4 of the row tile's column chunks.
         const int quarter = warp & 3;
+        const int hf = (warp - 2) >> 2;  // which share of the column chunks
         const int kl = quarter * 32 + lane;  // key lane of S^T, output dim of O^T
-        const int st = threadIdx.x - 64;     // 0..127
+        const int st = threadIdx.x - 64;     // 0..255
+        const int cb = min(hf * kNa, kNch), ce = min(cb + kNa, kNch);
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
         const float sl2 = L.scale_log2;
+        const int my_half = kl >> 6;         // which 64-token page of the tile holds my key
         int J = 0, piece_no = 0;
         bool bad = false;
         PieceIter it{t0, t1, 0, 0};
         Piece pc;
+
+        // P = 2^(s*scale*log2e - m) for my chunks; lpart += P (sign +1) or -= P
+        // (sign -1, the exact undo of a pass made with the same m); optionally
+        // writes P^T (hi and, for bf16, lo) and tracks the largest exponent.
+        // CHECK = false: every key lane of the warp is valid and every column of
+        // its chunks is a real row, so no per-element masking is needed
+        auto exp_pass = [&](const bool kCheck, float (&lpart)[kNa * 16], bool valid, float sign, bool write_p,
+                            float& ex) {
+            // 8-column blocks b = 2*cc + hb; the TMEM load of block b+1 is in
+            // flight while block b is computed
+            constexpr int kBlocks = 2 * kNa;
+            const int nblk = 2 * (ce - cb);
+            uint32_t rn[8];
+            tmem_ld8(tl + 16 * cb, rn);
+#pragma unroll
+            for (int bi = 0; bi < kBlocks; ++bi) {
+                if (bi >= nblk) continue;
+                uint32_t r[8];
+                tmem_wait_ld_regs(rn);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r[j] = rn[j];
+                if (bi + 1 < nblk) tmem_ld8(tl + 16 * cb + 8 * (bi + 1), rn);
+                const int cc = bi >> 1, hb = bi & 1;
+                const int c = cb + cc;
+                const int lim = valid ? R_seg - 16 * c : 0;
+                const float4* m4 = reinterpret_cast<const float4*>(ms->m_ref + 16 * c + 8 * hb);
+                const float4 ma = m4[0], mb = m4[1];
+                const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                float pv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float x = fmaf(__uint_as_float(r[j]), sl2, -mv[j]);
+                    if (kCheck) {
+                        const bool ok = 8 * hb + j < lim;
+                        if (ok) ex = fmaxf(ex, x);
+                        pv[j] = ok ? ex2(x) : 0.f;
+                    } else {
+                        ex = fmaxf(ex, x);
+                        pv[j] = ex2(x);
+                    }
+                    float& acc = lpart[cc * 16 + 8 * hb + j];
+                    acc = fmaf(sign, pv[j], acc);
+                }
+                if (write_p) {
+                    const int nb = 2 * c + hb;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) w[k] = pack2<BF16>(pv[2 * k], pv[2 * k + 1]);
+                    *reinterpret_cast<uint4*>(sP + nb * 2048 + kl * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                    if constexpr (BF16) {
+                        // residual p - bf16(p): bf16 keeps the top 16 bits of the fp32 pattern
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float h0 = __uint_as_float(w[k] << 16);
+                            const float h1 = __uint_as_float(w[k] & 0xFFFF0000u);
+                            w[k] = pack2<true>(pv[2 * k] - h0, pv[2 * k + 1] - h1);
+                        }
+                        *reinterpret_cast<uint4*>(sP + Lay::kPOneBytes + nb * 2048 + kl * 16) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        };
+
         while (it.next(p, a.ctx_len, pc)) {
             const int npages = (pc.L + kPage - 1) / kPage;
             const int32_t* pt = a.page_table + (size_t)pc.b * p.max_pages;
-            bar_sync(1, 128);
-            for (int col = st; col < RGP; col += 128) ms->m_ref[col] = -INFINITY;
-            bar_sync(1, 128);
-            float lpart[RGP];
+            bar_sync(1, kSoftmaxThreads);
+            for (int col = st; col < RGP; col += kSoftmaxThreads) ms->m_ref[col] = -INFINITY;
+            bar_sync(1, kSoftmaxThreads);
+            float lpart[kNa * 16];
 #pragma unroll
-            for (int col = 0; col < RGP; ++col) lpart[col] = 0.f;
+            for (int i = 0; i < kNa * 16; ++i) lpart[i] = 0.f;
+            uint32_t page_bits = 0;
 
             for (long long t = pc.ta; t < pc.te; ++t, ++J) {
-                const int nvalid = (int)min((long long)kTileKeys, (long long)pc.L - t * kTileKeys);
-                const long long pg = 2 * t + (kl >> 6);
-                bool page_ok = false;
-                if (pg < npages) {
-                    const int pid = pt[pg];
-                    page_ok = pid >= 0 && pid < a.num_pages;
+                // validity of my page for 32 tiles at a time (one load per lane)
+                const int tb = (int)((t - pc.ta) & 31);
+                if (tb == 0) {
+                    const long long tt = t + lane;
+                    const long long pg = 2 * tt + my_half;
+                    bool ok = false;
+                    if (tt < pc.te && pg < npages) {
+                        const int pid = pt[pg];
+                        ok = pid >= 0 && pid < a.num_pages;
+                    }
+                    page_bits = __ballot_sync(0xffffffffu, ok);
                 }
+                const int nvalid = (int)min((long long)kTileKeys, (long long)pc.L - t * kTileKeys);
+                const bool page_ok = (page_bits >> tb) & 1u;
                 const bool valid = kl < nvalid && page_ok;
                 const bool got = mbar_wait(&ms->s_full, J & 1);
-                if (bar_sync_or(1, 128, bad || !got)) {
+                if (bar_sync_or(1, kSoftmaxThreads, bad || !got)) {
                     bad = true;
                     break;
                 }
                 tc_fence_after();
 
-                // pass 1: largest exponent this tile would use with the current shifts
-                float ex = -INFINITY;
+                // pass 0: exponents with the current shifts (P^T written, sums added,
+                //         largest exponent voted across the CTA)
+                // pass 1: if an exponent exceeded kTau, the same pass with the sums
+                //         subtracted (exact undo)
+                // pass 2: exact column maxima move the shifts, then P^T and sums again
+                // The first tile of a range has no shifts yet and starts at pass 2.
+                bool slow = t == pc.ta;
+                const bool unmasked = __all_sync(0xffffffffu, valid) && R_seg >= 16 * ce;
+                for (int pass = slow ? 2 : 0; pass < 3; ++pass) {
+                    if (pass == 2) {
+                        // exact column maxima of this tile, then move the shifts
+#pragma unroll 1
+                        for (int cc = 0; cc < kNa; ++cc) {
+                            const int c = cb + cc;
+                            if (c >= ce) continue;
+                            uint32_t r[16];
+                            tmem_ld16(tl + 16 * c, r);
+                            tmem_wait_ld();
+                            const int lim = valid ? R_seg - 16 * c : 0;
 #pragma unroll
-                for (int c = 0; c < kNch; ++c) {
-                    uint32_t r[16];
-                    tmem_ld16(tl + 16 * c, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = 16 * c + j;
-                        if (valid && col < R_seg) ex = fmaxf(ex, fmaf(__uint_as_float(r[j]), sl2, -ms->m_ref[col]));
-                    }
-                }
-                ex = warp_max(ex);
-                if (lane == 0) ms->ex_red[quarter] = ex;
-                bar_sync(1, 128);
-                ex = fmaxf(fmaxf(ms->ex_red[0], ms->ex_red[1]), fmaxf(ms->ex_red[2], ms->ex_red[3]));
-
-                if (ex > kTau) {
-                    // slow path: exact column maxima of this tile, then move the shifts
-#pragma unroll
-                    for (int c = 0; c < kNch; ++c) {
-                        uint32_t r[16];
-                        tmem_ld16(tl + 16 * c, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int col = 16 * c + j;
-                            float y = (valid && col < R_seg) ? __uint_as_float(r[j]) * sl2 : -INFINITY;
-                            y = warp_max(y);
-                            if (lane == 0) ms->col_red[quarter][col] = y;
-                        }
-                    }
-                    bar_sync(1, 128);
-                    for (int col = st; col < RGP; col += 128) {
-                        const float cm = fmaxf(fmaxf(ms->col_red[0][col], ms->col_red[1][col]),
-                                               fmaxf(ms->col_red[2][col], ms->col_red[3][col]));
-                        const float mo = ms->m_ref[col];
-                        const float mn = fmaxf(mo, cm);
-                        ms->alpha[col] = mn > mo ? ex2(mo - mn) : 1.f;
-                        ms->m_ref[col] = mn;
-                    }
-                    bar_sync(1, 128);
-#pragma unroll
-                    for (int col = 0; col < RGP; ++col) lpart[col] *= ms->alpha[col];
-                    if (t != pc.ta) {
-                        // O^T columns accumulated so far move with their shift
-#pragma unroll
-                        for (int c = 0; c < kNch; ++c) {
-                            bool any = false;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) any |= ms->alpha[16 * c + j] != 1.f;
-                            if (!any) continue;
-#pragma unroll
-                            for (int h = 0; h < kChunks / 2; ++h) {
-                                uint32_t r[16];
-                                const uint32_t addr = tl + (h ? kColO1 : kColO0) + 16 * c;
-                                tmem_ld16(addr, r);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int j = 0; j < 16; ++j)
-                                    r[j] = __float_as_uint(__uint_as_float(r[j]) * ms->alpha[16 * c + j]);
-                                tmem_st16(addr, r);
+                            for (int j = 0; j < 16; ++j) {
+                                float y = j < lim ? __uint_as_float(r[j]) * sl2 : -INFINITY;
+                                y = warp_max(y);
+                                if (lane == 0) ms->col_red[quarter][16 * c + j] = y;
                             }
                         }
-                        tmem_wait_st();
-                    }
-                }
-
-                // pass 2: P = 2^(s*scale*log2e - m), row sums, P^T to shared memory
-#pragma unroll
-                for (int c = 0; c < kNch; ++c) {
-                    uint32_t r[16];
-                    tmem_ld16(tl + 16 * c, r);
-                    tmem_wait_ld();
-                    float pv[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = 16 * c + j;
-                        const float x = fmaf(__uint_as_float(r[j]), sl2, -ms->m_ref[col]);
-                        pv[j] = (valid && col < R_seg) ? ex2(x) : 0.f;
-                        lpart[col] += pv[j];
-                    }
-                    uint32_t w[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) w[k] = pack2<BF16>(pv[2 * k], pv[2 * k + 1]);
-                    *reinterpret_cast<uint4*>(sP + (2 * c) * 2048 + kl * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4*>(sP + (2 * c + 1) * 2048 + kl * 16) = make_uint4(w[4], w[5], w[6], w[7]);
-                    if constexpr (BF16) {
-                        // residual p - bf16(p): bf16 keeps the top 16 bits of the fp32 pattern
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const float h0 = __uint_as_float(w[k] << 16), h1 = __uint_as_float(w[k] & 0xFFFF0000u);
-                            w[k] = pack2<true>(pv[2 * k] - h0, pv[2 * k + 1] - h1);
+                        bar_sync(1, kSoftmaxThreads);
+                        for (int col = st; col < RGP; col += kSoftmaxThreads) {
+                            const float cm = fmaxf(fmaxf(ms->col_red[0][col], ms->col_red[1][col]),
+                                                   fmaxf(ms->col_red[2][col], ms->col_red[3][col]));
+                            const float mo = ms->m_ref[col];
+                            const float mn = fmaxf(mo, cm);
+                            ms->alpha[col] = mn > mo ? ex2(mo - mn) : 1.f;
+                            ms->m_ref[col] = mn;
                         }
-                        uint8_t* lo = sP + Lay::kPOneBytes;
-                        *reinterpret_cast<uint4*>(lo + (2 * c) * 2048 + kl * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                        *reinterpret_cast<uint4*>(lo + (2 * c + 1) * 2048 + kl * 16) =
-                            make_uint4(w[4], w[5], w[6], w[7]);
+                        bar_sync(1, kSoftmaxThreads);
+#pragma unroll
+                        for (int cc = 0; cc < kNa; ++cc) {
+                            const int c = cb + cc;
+                            if (c >= ce) continue;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) lpart[cc * 16 + j] *= ms->alpha[16 * c + j];
+                        }
+                        if (t != pc.ta) {
+                            // O^T columns accumulated so far move with their shift
+#pragma unroll 1
+                            for (int cc = 0; cc < kNa; ++cc) {
+                                const int c = cb + cc;
+                                if (c >= ce) continue;
+                                bool any = false;
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) any |= ms->alpha[16 * c + j] != 1.f;
+                                if (!any) continue;
+#pragma unroll 1
+                                for (int h = 0; h < kChunks / 2; ++h) {
+                                    uint32_t r[16];
+                                    const uint32_t addr = tl + (h ? kColO1 : kColO0) + 16 * c;
+                                    tmem_ld16(addr, r);
+                                    tmem_wait_ld();
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j)
+                                        r[j] = __float_as_uint(__uint_as_float(r[j]) * ms->alpha[16 * c + j]);
+                                    tmem_st16(addr, r);
+                                }
+                            }
+                            tmem_wait_st();
+                        }
+                    }
+                    float ex = -INFINITY;
+                    if (pass == 0 && unmasked) exp_pass(false, lpart, valid, 1.f, true, ex);
+                    else exp_pass(true, lpart, valid, pass == 1 ? -1.f : 1.f, pass != 1, ex);
+                    if (pass == 0) {
+                        ex = warp_max(ex);
+                        if (lane == 0) ms->ex_red[warp - 2] = ex;
+                        bar_sync(1, kSoftmaxThreads);
+#pragma unroll
+                        for (int w = 0; w < kSmWarps; ++w) ex = fmaxf(ex, ms->ex_red[w]);
+                        slow = ex > kTau;
+                        if (!slow) break;
                     }
                 }
 
                 // keys past L inside the last (partial) page: their V rows hold
                 // whatever the pool has there; zero them so 0 * V stays 0
-                if ((nvalid & (kPage - 1)) != 0 && kl >= nvalid && kl < ((nvalid + kPage - 1) & ~(kPage - 1)) &&
-                    page_ok) {
+                if (hf == 0 && (nvalid & (kPage - 1)) != 0 && kl >= nvalid &&
+                    kl < ((nvalid + kPage - 1) & ~(kPage - 1)) && page_ok) {
                     const uint32_t vbase = (uint32_t)J * (2 * kChunks) + kChunks;
                     for (int c = 0; c < kChunks; ++c) {
                         const uint32_t ch = vbase + c;
@@ -514,26 +588,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---------------------------------------------------------- epilogue
             const bool got = mbar_wait(&ms->o_full, piece_no & 1);
-            if (bar_sync_or(1, 128, bad || !got)) {
+            if (bar_sync_or(1, kSoftmaxThreads, bad || !got)) {
                 bad = true;
                 break;
             }
             tc_fence_after();
 #pragma unroll
-            for (int col = 0; col < RGP; ++col) {
-                const float v = warp_sum(lpart[col]);
-                if (lane == 0) ms->col_red[quarter][col] = v;
+            for (int cc = 0; cc < kNa; ++cc) {
+                const int c = cb + cc;
+                if (c >= ce) continue;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float v = warp_sum(lpart[cc * 16 + j]);
+                    if (lane == 0) ms->col_red[quarter][16 * c + j] = v;
+                }
             }
-            bar_sync(1, 128);
+            bar_sync(1, kSoftmaxThreads);
             float* slot = L.ws + slot_index(p, rg, cta, pc.s) * slot_floats(p);
             float* slot_m = slot + (size_t)RG * D;
             float* slot_l = slot_m + RG;
-            for (int col = st; col < R_seg; col += 128) {
+            for (int col = st; col < R_seg; col += kSoftmaxThreads) {
                 slot_l[col] = ms->col_red[0][col] + ms->col_red[1][col] + ms->col_red[2][col] + ms->col_red[3][col];
                 slot_m[col] = ms->m_ref[col];
             }
 #pragma unroll
-            for (int c = 0; c < kNch; ++c) {
+            for (int cc = 0; cc < kNa; ++cc) {
+                const int c = cb + cc;
+                if (c >= ce) continue;
 #pragma unroll
                 for (int h = 0; h < kChunks / 2; ++h) {
                     uint32_t r[16];
