@@ -46,20 +46,41 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const float* __restric
     __shared__ unsigned long long red[kThreads / 32];
     __shared__ bool is_last;
     const int row = blockIdx.y, ch = blockIdx.x;
-    const long long per = ((long long)vocab + chunks - 1) / chunks;
+    const long long per = (((long long)vocab + chunks - 1) / chunks + 3) / 4 * 4;  // multiple of 4 elements
     const long long k0 = ch * per;
     const long long k1 = min((long long)vocab, k0 + per);
     const float* x = logits + row * row_stride;
     unsigned long long best = 0ull;
-    // 4 independent loads in flight per thread
-    long long k = k0 + threadIdx.x;
-    for (; k + 3 * kThreads < k1; k += 4 * kThreads) {
-        const float a0 = __ldg(x + k), a1 = __ldg(x + k + kThreads);
-        const float a2 = __ldg(x + k + 2 * kThreads), a3 = __ldg(x + k + 3 * kThreads);
-        best = umax64(best, pack_key(a0, (unsigned)k));
-        best = umax64(best, pack_key(a1, (unsigned)(k + kThreads)));
-        best = umax64(best, pack_key(a2, (unsigned)(k + 2 * kThreads)));
-        best = umax64(best, pack_key(a3, (unsigned)(k + 3 * kThreads)));
+    long long k = k0;
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+        // 16-byte loads, 4 in flight per thread
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        const long long q0 = k0 / 4, q1 = k1 / 4;  // full float4 groups in [k0, k1)
+        long long q = q0 + threadIdx.x;
+        for (; q + 3 * kThreads < q1; q += 4 * kThreads) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = __ldg(x4 + q + u * kThreads);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const unsigned base = (unsigned)(4 * (q + u * kThreads));
+                best = umax64(best, pack_key(v[u].x, base));
+                best = umax64(best, pack_key(v[u].y, base + 1));
+                best = umax64(best, pack_key(v[u].z, base + 2));
+                best = umax64(best, pack_key(v[u].w, base + 3));
+            }
+        }
+        for (; q < q1; q += kThreads) {
+            const float4 v = __ldg(x4 + q);
+            const unsigned base = (unsigned)(4 * q);
+            best = umax64(best, pack_key(v.x, base));
+            best = umax64(best, pack_key(v.y, base + 1));
+            best = umax64(best, pack_key(v.z, base + 2));
+            best = umax64(best, pack_key(v.w, base + 3));
+        }
+        k = q1 * 4 + threadIdx.x;  // ragged tail (vocab not a multiple of 4)
+    } else {
+        k = k0 + threadIdx.x;
     }
     for (; k < k1; k += kThreads) best = umax64(best, pack_key(__ldg(x + k), (unsigned)k));
     best = block_max(best, red);

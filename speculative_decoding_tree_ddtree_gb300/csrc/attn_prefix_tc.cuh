@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ============================================================ TMA producer
         const int oob_row = a.num_pages * p.Hkv * kPage;  // first row past the pool: zero fill
+        const uint64_t pol_stream = policy_evict_first();  // K/V are read once: do not keep them in L2
         uint32_t chunk = 0;
         int piece_no = 0;
         bool ok = true;
@@ -275,8 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int c = part % kChunks;
                         uint8_t* dst = sSlots + slot * kChunkBytes;
                         mbar_arrive_expect_tx(&ms->full[slot], kChunkBytes);
-                        tma_load_2d(dst, m, 64 * c, row[0], &ms->full[slot]);
-                        tma_load_2d(dst + 8192, m, 64 * c, row[1], &ms->full[slot]);
+                        tma_load_2d_hint(dst, m, 64 * c, row[0], &ms->full[slot], pol_stream);
+                        tma_load_2d_hint(dst + 8192, m, 64 * c, row[1], &ms->full[slot], pol_stream);
                     }
                     __syncwarp();
                     ++chunk;

@@ -70,9 +70,10 @@ __host__ __device__ inline PlanDims make_plan(int B, int N, int Hq, int Hkv, int
 
 __host__ __device__ inline int grid_ctas(const PlanDims& p) { return p.Cg * p.rg.NG; }
 
-// floats per workspace slot: O [RG][D], then max [RG], then sum [RG]
+// floats per workspace slot: O [RG][D], then max [RG], then sum [RG]; the
+// stride is rounded up to 256 bytes so every slot starts 16-byte aligned
 __host__ __device__ inline size_t slot_floats(const PlanDims& p) {
-    return (size_t)p.rg.RG * (p.D + 2);
+    return ((size_t)p.rg.RG * (p.D + 2) + 63) / 64 * 64;
 }
 
 __host__ __device__ inline size_t slot_index(const PlanDims& p, int rg, int c, int s) {

@@ -13,76 +13,114 @@ namespace lucetree {
 
 namespace {
 
-// One thread per sequence; N <= 64 so the masks fit one word per node.
-__global__ void build_anc_kernel(const int32_t* __restrict__ parent, int B, int N, uint64_t* __restrict__ anc,
-                                 uint32_t* status) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+// One warp per sequence; node i lives in lane i % 32, slot i / 32.  Parents
+// are loaded in parallel, then the masks are built in node order (each node
+// needs its parent's mask) with shuffles instead of dependent global loads.
+__global__ void __launch_bounds__(128) build_anc_kernel(const int32_t* __restrict__ parent, int B, int N,
+                                                        uint64_t* __restrict__ anc, uint32_t* status) {
+    const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
     if (b >= B) return;
     const int32_t* par = parent + (size_t)b * N;
-    uint64_t* out = anc + (size_t)b * N;
-    uint64_t local[LUCETREE_MAX_NODES];
+    int p0 = lane < N ? par[lane] : -1;
+    int p1 = lane + 32 < N ? par[lane + 32] : -1;
+    uint64_t m0 = 0, m1 = 0;  // this lane's nodes' masks
+    bool bad = false;
     for (int i = 0; i < N; ++i) {
-        const int pi = par[i];
-        uint64_t m = 1ull << i;
+        const int pi = __shfl_sync(0xffffffffu, i < 32 ? p0 : p1, i & 31);
+        uint64_t pm = 0;
         if (pi >= 0 && pi < i) {
-            m |= local[pi];
+            const uint64_t a0 = __shfl_sync(0xffffffffu, m0, pi & 31);
+            const uint64_t a1 = __shfl_sync(0xffffffffu, m1, pi & 31);
+            pm = pi < 32 ? a0 : a1;
         } else if (pi != -1) {
-            atomicOr(status, LUCETREE_DEV_BAD_PARENT);
+            bad = true;
         }
-        local[i] = m;
-        out[i] = m;
+        const uint64_t mi = pm | (1ull << i);
+        if ((i & 31) == lane) {
+            if (i < 32) m0 = mi;
+            else m1 = mi;
+        }
     }
+    uint64_t* out = anc + (size_t)b * N;
+    if (lane < N) out[lane] = m0;
+    if (lane + 32 < N) out[lane + 32] = m1;
+    if (bad && lane == 0) atomicOr(status, LUCETREE_DEV_BAD_PARENT);
 }
 
-// One thread per sequence.  ok[i]: node i and all its ancestors match; the
-// deepest ok node (lowest id among equals, by scanning ids upward with a
-// strict comparison) ends the accepted path.
-__global__ void accept_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ draft,
-                              const int32_t* __restrict__ argmax, int B, int N, int vocab,
-                              int32_t* __restrict__ acc_nodes, int32_t* __restrict__ acc_len,
-                              int32_t* __restrict__ bonus, uint32_t* status) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+// One warp per sequence.  Lanes load the tree (node i in lane i % 32) and
+// decide whether each node's draft token equals its parent row's argmax; the
+// ok-flags (node and all ancestors match) and depths then follow in node
+// order.  The deepest ok node (lowest id among equals: ids are scanned upward
+// with a strict comparison) ends the accepted path.
+__global__ void __launch_bounds__(128) accept_kernel(const int32_t* __restrict__ parent,
+                                                     const int32_t* __restrict__ draft,
+                                                     const int32_t* __restrict__ argmax, int B, int N, int vocab,
+                                                     int32_t* __restrict__ acc_nodes, int32_t* __restrict__ acc_len,
+                                                     int32_t* __restrict__ bonus, uint32_t* status) {
+    const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
     if (b >= B) return;
     const int32_t* par = parent + (size_t)b * N;
     const int32_t* dr = draft + (size_t)b * N;
     const int32_t* am = argmax + (size_t)b * (N + 1);
-    int32_t* out = acc_nodes + (size_t)b * N;
-    int depth[LUCETREE_MAX_NODES];
-    uint64_t ok = 0;
-    int best = -1, best_depth = 0;
-    bool bad = false;
-    for (int i = 0; i < N; ++i) {
-        const int pi = par[i];
-        if (pi < -1 || pi >= i) {
-            bad = true;
-            break;
-        }
-        const int t = dr[i];
-        bool match = t == am[pi + 1];
-        if (t < 0 || t >= vocab) {
-            atomicOr(status, LUCETREE_DEV_BAD_TOKEN);
-            match = false;
-        }
-        const bool parent_ok = pi < 0 || ((ok >> pi) & 1ull);
-        depth[i] = (pi < 0 ? 0 : depth[pi]) + 1;
-        if (match && parent_ok) {
-            ok |= 1ull << i;
-            if (depth[i] > best_depth) {
-                best = i;
-                best_depth = depth[i];
+    int p[2] = {-1, -1};
+    bool match[2] = {false, false};
+    bool bad = false, bad_tok = false;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = lane + 32 * k;
+        if (i < N) {
+            p[k] = par[i];
+            if (p[k] < -1 || p[k] >= i) {
+                bad = true;
+            } else {
+                const int t = dr[i];
+                if (t < 0 || t >= vocab) bad_tok = true;
+                else match[k] = t == am[p[k] + 1];
             }
         }
     }
-    if (bad) {
+    bad = __any_sync(0xffffffffu, bad);
+    if (__any_sync(0xffffffffu, bad_tok) && lane == 0) atomicOr(status, LUCETREE_DEV_BAD_TOKEN);
+    const uint32_t mlo = __ballot_sync(0xffffffffu, match[0]), mhi = __ballot_sync(0xffffffffu, match[1]);
+    const uint64_t matched = ((uint64_t)mhi << 32) | mlo;
+    int best = -1, best_depth = 0;
+    uint64_t ok = 0;
+    int d0 = 0, d1 = 0;  // depths of this lane's nodes
+    if (!bad) {
+        for (int i = 0; i < N; ++i) {
+            const int pi = __shfl_sync(0xffffffffu, i < 32 ? p[0] : p[1], i & 31);
+            int dp = 0;
+            if (pi >= 0) {
+                const int a0 = __shfl_sync(0xffffffffu, d0, pi & 31), a1 = __shfl_sync(0xffffffffu, d1, pi & 31);
+                dp = pi < 32 ? a0 : a1;
+            }
+            const int di = dp + 1;
+            if ((i & 31) == lane) {
+                if (i < 32) d0 = di;
+                else d1 = di;
+            }
+            const bool ok_i = ((matched >> i) & 1ull) && (pi < 0 || ((ok >> pi) & 1ull));
+            if (ok_i) {
+                ok |= 1ull << i;
+                if (di > best_depth) {
+                    best = i;
+                    best_depth = di;
+                }
+            }
+        }
+    } else if (lane == 0) {
         atomicOr(status, LUCETREE_DEV_BAD_PARENT);
-        best = -1;
-        best_depth = 0;
     }
-    for (int k = best_depth; k < N; ++k) out[k] = -1;
-    int k = best_depth;
-    for (int c = best; c >= 0; c = par[c]) out[--k] = c;
-    acc_len[b] = best_depth;
-    bonus[b] = am[best + 1];
+    int32_t* out = acc_nodes + (size_t)b * N;
+    for (int k = best_depth + lane; k < N; k += 32) out[k] = -1;
+    if (lane == 0) {
+        int k = best_depth;
+        for (int c = best; c >= 0; c = par[c]) out[--k] = c;
+        acc_len[b] = best_depth;
+        bonus[b] = am[best + 1];
+    }
 }
 
 // One block per sequence: 16-byte vector copies of every accepted node's K and
@@ -145,15 +183,15 @@ __global__ void __launch_bounds__(256) commit_kernel(lucetree_commit_args c, int
 
 cudaError_t launch_build_anc(const int32_t* parent, int B, int N, uint64_t* anc, uint32_t* status,
                              cudaStream_t stream) {
-    build_anc_kernel<<<(B + 63) / 64, 64, 0, stream>>>(parent, B, N, anc, status);
+    build_anc_kernel<<<(B + 3) / 4, 128, 0, stream>>>(parent, B, N, anc, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int B, int N,
                           int vocab, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus, uint32_t* status,
                           cudaStream_t stream) {
-    accept_kernel<<<(B + 63) / 64, 64, 0, stream>>>(parent, draft, argmax, B, N, vocab, acc_nodes, acc_len, bonus,
-                                                    status);
+    accept_kernel<<<(B + 3) / 4, 128, 0, stream>>>(parent, draft, argmax, B, N, vocab, acc_nodes, acc_len, bonus,
+                                                   status);
     return cudaGetLastError();
 }
 
