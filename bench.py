@@ -76,7 +76,7 @@ def prefix_kernel_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_tree_ddtree_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.startswith("attn_prefix") or fn == "internal.cuh":
+        if fn.startswith("attn_prefix") or fn in ("internal.cuh", "tc_ptx.cuh"):
             with open(os.path.join(csrc, fn), "rb") as f:
                 h.update(f.read())
     return h.hexdigest()[:16]
