@@ -33,7 +33,9 @@ int prefix_grid_ctas(int device) { return device_sm_count(device); }
 bool prefix_shape_supported(const lucetree_attn_args& a) {
     // TMA row coordinates are 32-bit: the pool must stay below 2^31 rows
     const long long rows = (long long)a.num_pages * a.Hkv * kPage;
-    return rows + kPage < (1ll << 31);
+    // the kernel counts key tiles in 32 bits
+    const long long tiles = (long long)a.B * a.Hkv * (((long long)a.max_pages_per_seq * kPage + kTileKeys - 1) / kTileKeys);
+    return rows + kPage < (1ll << 31) && tiles < (1ll << 31);
 }
 
 cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream) {

@@ -2,35 +2,51 @@
 // 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA-fed operands).
 //
 // Orientation.  Per (sequence, KV head, row group) the query rows are the
-// (node, head-in-group) pairs: 132 at budget 22 with 6 heads per KV head.
-// Keys, not queries, go on the MMA's M = 128 dimension so the rows only pad
-// to a multiple of 16 (the MMA's N):
+// (node, head-in-group) pairs of the group's nodes (132 at budget 22 with 6
+// heads per KV head, one group).  Keys, not queries, go on the MMA's M = 128
+// dimension so the rows only pad to a multiple of 16 (the MMA's N):
 //     S^T [128 keys x R]  = K_tile [128 x D]  . Q^T          (K-major A and B)
 //     O^T [D x R]        += V_tile^T [D x 128] . P^T [128 x R] (MN-major A and B)
-// TMEM (512 columns): S^T in [0, R), O^T in [160, 160+R) and [320, 320+R)
-// (d 0..127 and d 128..255).  TMEM lane l holds key l of S^T and output dim
-// l (+128) of O^T.
+// Keeping all of a KV head's rows in one CTA means each K/V tile passes
+// through one SM's shared memory and tensor cores once; splitting the rows
+// over several CTAs would multiply that traffic, which is what bounds this
+// kernel on the SM side.
+//
+// TMEM (512 columns): S^T at columns [0, R), then O^T for d 0..127 and d
+// 128..255.  With bf16 operands P is split into hi and lo parts (below); when
+// TMEM and the MMA's N <= 256 allow it (R <= 96), P_hi^T and P_lo^T sit side
+// by side as one B operand so a single MMA of N = 2R reads V once and writes
+// both products into adjacent column ranges that the epilogue adds; for
+// larger R the two products are separate MMAs into one accumulator.  TMEM
+// lane l holds key l of S^T and output dim l (+128) of O^T.
+//
+// Software pipeline.  The MMA warp issues QK(t+1) as soon as the softmax has
+// released S^T(t) (after its exponent vote), before PV(t); so the scores of
+// the next tile are computed on the tensor cores while the softmax stores
+// P^T(t), and PV(t) follows.  The softmax of tile t starts writing P^T once
+// PV(t-1) has finished reading it.  K and V chunks stream through the ring
+// in that consumption order: K(0) K(1) V(0) K(2) V(1) ... K(n-1) V(n-2) V(n-1).
 //
 // Softmax over keys runs across TMEM lanes.  Each softmax thread owns one key
 // lane and keeps per-column partial sums in registers; the shift m[r] per
 // query row is stale on purpose.  A tile is first exponentiated with the
-// current shifts (one pass: P^T written, sums accumulated, largest exponent
-// tracked); if any exponent exceeds 8 (log2 domain) the pass is taken back
-// out exactly, the tile's column maxima are found (warp shuffles + shared
-// memory) and the partial sums and already-accumulated O^T columns are
+// current shifts (one streaming pass: P^T written, sums accumulated, largest
+// exponent tracked); if any exponent exceeds 8 (log2 domain) the pass is taken
+// back out exactly, the tile's column maxima are found (warp shuffles +
+// shared memory) and the partial sums and already-accumulated O^T columns are
 // rescaled before the tile is redone.  The first tile of every range goes
 // straight to that path.  Sums are reduced across lanes once per range.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2..13 = softmax and
-// epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and handles one third of
-// the row tile's column chunks, so three warps share each lane quarter (the
-// per-column partial sums then fit in registers) and hide each other's
-// latency.  K and V stream through
+// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2..3 idle (they
+// complete warpgroup 0, which hands most of its registers to the others),
+// 4..15 = softmax and epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and
+// handles one third of the row tile's column chunks.  K and V stream through
 // a ring of 16 KB chunk slots ([128 keys][64 d], 128-byte swizzle), two TMA
-// boxes (one per 64-token page) per slot; a tile is D/64 K chunks then D/64 V
-// chunks, and V chunk pairs always land in slots (2j, 2j+1) so one MN-major
-// descriptor covers 128 output dims.  Every wait is bounded; a timeout sets
-// LUCETREE_DEV_TIMEOUT, drains this CTA's own copies and MMAs and returns.
+// boxes (one per 64-token page) per slot; an operand (one tile's K or V) is
+// D/64 consecutive chunks, and V chunk pairs always land in slots (2j, 2j+1)
+// so one MN-major descriptor covers 128 output dims.  Every wait is bounded; a
+// timeout sets LUCETREE_DEV_TIMEOUT, drains this CTA's own copies and MMAs
+// and returns.
 #pragma once
 
 #include "internal.cuh"
@@ -44,14 +60,20 @@ using namespace tc;
 constexpr int kSmGroups = 3;                        // softmax warps per TMEM lane quarter
 constexpr int kSmWarps = 4 * kSmGroups;             // 12 softmax warps
 constexpr int kSoftmaxThreads = 32 * kSmWarps;      // 384
-constexpr int kThreads = 64 + kSoftmaxThreads;      // + producer warp + MMA warp
+constexpr int kThreads = 128 + kSoftmaxThreads;     // + warpgroup 0 (producer, MMA, two idle warps)
+// Register split (setmaxnreg): the block is launched with 128 per thread
+// (65536 / 512); warpgroup 0 gives back down to kRegsIssue and the three
+// softmax warpgroups take kRegsSoftmax.  4*32*56 + 12*32*152 = 65536.
+constexpr uint32_t kRegsIssue = 56, kRegsSoftmax = 152;
+static_assert(kThreads == 512, "register split assumes 16 warps");
+static_assert(128 * kRegsIssue + kSoftmaxThreads * kRegsSoftmax <= 65536, "register split exceeds the launch");
 
 constexpr int kChunkBytes = 128 * 128;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr float kTau = 8.0f;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO0 = 160, kColO1 = 320;
 constexpr int kMaxSlots = 12;
+static_assert(3 * kRowsMax <= (int)kTmemCols, "S^T and two O^T halves in TMEM");
 
 // bf16 P keeps 8 significant bits, which alone puts ~1e-3 relative noise on
 // the output; with bf16 operands P is split into hi = bf16(p) and
@@ -60,11 +82,18 @@ constexpr int kMaxSlots = 12;
 template <int D, int RGP, bool SPLIT>
 struct Layout {
     static constexpr int kChunks = D / 64;
+    static constexpr int kDh = D / 128;                 // O^T halves of 128 output dims
     static constexpr int kNch = RGP / 16;
     static constexpr int kQBytes = kChunks * RGP * 128;
     static constexpr int kPOneBytes = RGP * 256;
     static constexpr int kPBytes = kPOneBytes * (SPLIT ? 2 : 1);
-    static constexpr int kMiscBytes = 6144;
+    // hi and lo of P as one B operand (N = 2R) when that fits the MMA and TMEM
+    static constexpr bool kMerge = SPLIT && 2 * RGP <= 256 && RGP + kDh * 2 * RGP <= (int)kTmemCols;
+    static constexpr int kPvN = kMerge ? 2 * RGP : RGP;  // N of the PV MMA
+    static constexpr uint32_t kColO0 = RGP;              // O^T, d 0..127
+    static constexpr uint32_t kColO1 = RGP + kPvN;       // O^T, d 128..255
+    static_assert(RGP + kDh * kPvN <= (int)kTmemCols, "TMEM columns");
+    static constexpr int kMiscBytes = 4096;
     static constexpr int kRaw = (kSmemLimit - 1024 - kQBytes - kPBytes - kMiscBytes) / kChunkBytes;
     static constexpr int kNS = (kRaw > kMaxSlots ? kMaxSlots : kRaw) & ~1;
     static constexpr int kQOff = 0;
@@ -74,7 +103,7 @@ struct Layout {
     // force one CTA per SM: the kernel owns all 512 TMEM columns
     static constexpr int kBytesRaw = kMiscOff + kMiscBytes + 1024;
     static constexpr int kBytes = kBytesRaw < 120 * 1024 ? 120 * 1024 : kBytesRaw;
-    static_assert(kNS >= 2, "shared memory too small for the K/V ring");
+    static_assert(kNS >= kChunks, "the K/V ring must hold one whole operand");
     static_assert(kBytes <= kSmemLimit, "shared memory budget");
 };
 
@@ -82,34 +111,33 @@ struct Misc {
     alignas(16) float m_ref[kRowsMax];
     alignas(16) float alpha[kRowsMax];
     alignas(16) float col_red[4][kRowsMax];
-    float ex_red[kSmWarps];
     uint64_t full[kMaxSlots];
     uint64_t empty[kMaxSlots];
-    uint64_t q_full, q_empty, s_full, p_full, o_full, drain;
+    uint64_t s_full, s_free, q_full, q_empty, p_full, pv_done, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
-static_assert(sizeof(Misc) <= 6144, "misc region");
+static_assert(sizeof(Misc) <= 4096, "misc region");
 
+// A key segment's share of this CTA's tiles.  Tile indices are 32-bit: the
+// host refuses shapes whose flat tile count reaches 2^31.
 struct Piece {
-    int s, b, g, L;
-    long long ta, te;  // tile range within the key segment
+    int s, L;    // key segment (b * Hkv + g) and its committed length
+    int ta, te;  // tile range within the segment
 };
 
 struct PieceIter {
-    long long t0, t1, off;
-    int s;
+    int t0, t1, off, s;
     __device__ bool next(const PlanDims& p, const int32_t* ctx_len, Piece& out) {
         while (s < p.S && off < t1) {
-            const int b = s / p.Hkv, g = s % p.Hkv;
-            const int L = seq_len_quiet(ctx_len, b, p.max_pages);
-            const long long nt = tiles_of(L);
-            const long long s0 = off, s1 = off + nt;
+            const int L = seq_len_quiet(ctx_len, s / p.Hkv, p.max_pages);
+            const int s0 = off, s1 = off + (int)tiles_of(L);
             const int cur = s;
             off = s1;
             ++s;
-            if (nt == 0 || s1 <= t0) continue;
-            out.s = cur; out.b = b; out.g = g; out.L = L;
+            if (s1 == s0 || s1 <= t0) continue;
+            out.s = cur;
+            out.L = L;
             out.ta = (t0 > s0 ? t0 : s0) - s0;
             out.te = (t1 < s1 ? t1 : s1) - s0;
             return true;
@@ -117,6 +145,37 @@ struct PieceIter {
         return false;
     }
 };
+
+// The CTA's tiles in order: piece (key segment) and tile within the segment.
+struct TileCursor {
+    PieceIter it;
+    Piece pc;
+    int t;
+    int piece_no;
+    bool live;
+    __device__ void start(int t0, int t1, const PlanDims& p, const int32_t* ctx_len) {
+        it = PieceIter{t0, t1, 0, 0};
+        piece_no = -1;
+        t = 0;
+        next_piece(p, ctx_len);
+    }
+    __device__ void next_piece(const PlanDims& p, const int32_t* ctx_len) {
+        live = it.next(p, ctx_len, pc);
+        if (live) {
+            t = pc.ta;
+            ++piece_no;
+        }
+    }
+    __device__ bool first() const { return t == pc.ta; }
+    __device__ bool last() const { return t == pc.te - 1; }
+    __device__ void step(const PlanDims& p, const int32_t* ctx_len) {
+        if (++t >= pc.te) next_piece(p, ctx_len);
+    }
+};
+
+// Position of tile j's V operand in the ring's operand sequence
+// K(0) K(1) V(0) K(2) V(1) ... K(n-1) V(n-2) V(n-1).
+__device__ __forceinline__ uint32_t v_operand(uint32_t j, uint32_t n) { return j + 1 < n ? 2 * j + 2 : 2 * j + 1; }
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -178,8 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int RG = p.rg.RG;
 
     const long long nT = total_tiles(p, a.ctx_len);
-    const long long t0 = nT ? cta_begin(cta, nT, p.Cg) : 0, t1 = nT ? cta_begin(cta + 1, nT, p.Cg) : 0;
+    const int t0 = nT ? (int)cta_begin(cta, nT, p.Cg) : 0, t1 = nT ? (int)cta_begin(cta + 1, nT, p.Cg) : 0;
     if (t0 >= t1) return;  // uniform across the CTA
+    const uint32_t n_tiles = (uint32_t)(t1 - t0);
 
     // ---------------------------------------------------------------- set-up
     if (threadIdx.x == 0) {
@@ -187,21 +247,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ms->full[i], 1);
             mbar_init(&ms->empty[i], 1);
         }
+        mbar_init(&ms->s_full, 1);
+        mbar_init(&ms->s_free, kSmWarps);
         mbar_init(&ms->q_full, 1);
         mbar_init(&ms->q_empty, 1);
-        mbar_init(&ms->s_full, 1);
         mbar_init(&ms->p_full, kSmWarps);
-        mbar_init(&ms->o_full, 1);
+        mbar_init(&ms->pv_done, 1);
         mbar_init(&ms->drain, 1);
         ms->abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp >= 2) {
+    if (warp >= 4) {
         // rows RG..RGP-1 of Q are padding: zero them once (TMA never writes them)
-        const int st = threadIdx.x - 64;
-        constexpr int kPadMax = RGP;  // bound
-        for (int idx = st; idx < kChunks * kPadMax * 8; idx += kSoftmaxThreads) {
-            const int c = idx / (kPadMax * 8), r = (idx / 8) % kPadMax, u = idx % 8;
+        const int st = threadIdx.x - 128;
+        for (int idx = st; idx < kChunks * RGP * 8; idx += kSoftmaxThreads) {
+            const int c = idx / (RGP * 8), r = (idx / 8) % RGP, u = idx % 8;
             if (r >= RG) *reinterpret_cast<uint4*>(sQ + c * RGP * 128 + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
@@ -220,146 +280,181 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
 
+    if (warp < 4) {
+    regs_dec<kRegsIssue>();
     if (warp == 0) {
         // ============================================================ TMA producer
         const int oob_row = a.num_pages * p.Hkv * kPage;  // first row past the pool: zero fill
         const uint64_t pol_stream = policy_evict_first();  // K/V are read once: do not keep them in L2
         uint32_t chunk = 0;
-        int piece_no = 0;
+        int q_loads = 0;
         bool ok = true;
-        PieceIter it{t0, t1, 0, 0};
-        Piece pc;
-        while (ok && it.next(p, a.ctx_len, pc)) {
-            if (piece_no > 0) ok = mbar_wait(&ms->q_empty, (piece_no - 1) & 1);
-            if (!ok) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&ms->q_full, kChunks * RG * 128);
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sQ + c * RGP * 128, &tm_q, 64 * c, pc.g * p.G, pc.b * p.N + i0, &ms->q_full);
+        // one operand (one tile's K or V): kChunks slots of two boxes each
+        auto issue = [&](const CUtensorMap* m, int row0, int row1) -> bool {
+            for (int c = 0; c < kChunks; ++c) {
+                const int slot = chunk % kNS;
+                const bool w = mbar_wait(&ms->empty[slot], ((chunk / kNS) & 1) ^ 1);
+                if (!__all_sync(0xffffffffu, w)) return false;  // lanes agree on a timeout
+                if (lane == 0) {
+                    uint8_t* dst = sSlots + slot * kChunkBytes;
+                    mbar_arrive_expect_tx(&ms->full[slot], kChunkBytes);
+                    tma_load_2d_hint(dst, m, 64 * c, row0, &ms->full[slot], pol_stream);
+                    tma_load_2d_hint(dst + 8192, m, 64 * c, row1, &ms->full[slot], pol_stream);
+                }
+                __syncwarp();
+                ++chunk;
             }
-            __syncwarp();
-            const int npages = (pc.L + kPage - 1) / kPage;
-            const int32_t* pt = a.page_table + (size_t)pc.b * p.max_pages;
-            // page ids of this piece, 16 tiles (32 pages) per warp-wide load, one batch ahead
-            auto load_batch = [&](long long tb) {
-                const long long pg = 2 * tb + lane;
-                int pid = -1;
-                if (pg < npages && pg < 2 * pc.te) {
-                    const int v = pt[pg];
-                    if (v >= 0 && v < a.num_pages) pid = v;
-                    else atomicOr(a.status, LUCETREE_DEV_BAD_PAGE);
+            return true;
+        };
+        TileCursor cur;
+        cur.start(t0, t1, p, a.ctx_len);
+        int npages = 0;
+        const int32_t* pt = a.page_table;
+        // page ids of the current piece, 16 tiles (32 pages) per warp-wide load, one batch ahead
+        auto load_batch = [&](int tb) {
+            const int pg = 2 * tb + lane;
+            int pid = -1;
+            if (pg < npages && pg < 2 * cur.pc.te) {
+                const int v = pt[pg];
+                if (v >= 0 && v < a.num_pages) pid = v;
+                else atomicOr(a.status, LUCETREE_DEV_BAD_PAGE);
+            }
+            return pid;
+        };
+        int pid_cur = -1, pid_next = -1;
+        int v_row0 = 0, v_row1 = 0;
+        bool have_v = false;
+        while (ok && cur.live) {
+            const int rel = cur.t - cur.pc.ta;
+            if (rel == 0) {
+                // a new key segment: its queries replace the previous ones once their last QK is done
+                if (cur.piece_no > 0) {
+                    const bool w = mbar_wait(&ms->q_empty, (cur.piece_no - 1) & 1);
+                    if (!(ok = __all_sync(0xffffffffu, w))) break;
                 }
-                return pid;
-            };
-            int pid_cur = load_batch(pc.ta), pid_next = load_batch(pc.ta + 16);
-            for (long long t = pc.ta; t < pc.te && ok; ++t) {
-                const long long rel = t - pc.ta;
-                if (rel > 0 && (rel & 15) == 0) {
-                    pid_cur = pid_next;
-                    pid_next = load_batch(t + 16);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&ms->q_full, kChunks * RG * 128);
+                    const int b = cur.pc.s / p.Hkv, g = cur.pc.s % p.Hkv;
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(sQ + c * RGP * 128, &tm_q, 64 * c, g * p.G, b * p.N + i0, &ms->q_full);
                 }
-                int row[2];
+                __syncwarp();
+                ++q_loads;
+                npages = (cur.pc.L + kPage - 1) / kPage;
+                pt = a.page_table + (size_t)(cur.pc.s / p.Hkv) * p.max_pages;
+                pid_cur = load_batch(cur.pc.ta);
+                pid_next = load_batch(cur.pc.ta + 16);
+            } else if ((rel & 15) == 0) {
+                pid_cur = pid_next;
+                pid_next = load_batch(cur.t + 16);
+            }
+            int row[2];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int pid = __shfl_sync(0xffffffffu, pid_cur, (int)(2 * (rel & 15) + h));
-                    row[h] = pid >= 0 ? (pid * p.Hkv + pc.g) * kPage : oob_row;
-                }
-#pragma unroll 1
-                for (int part = 0; part < 2 * kChunks; ++part) {
-                    const int slot = chunk % kNS;
-                    if (!mbar_wait(&ms->empty[slot], ((chunk / kNS) & 1) ^ 1)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        const CUtensorMap* m = part < kChunks ? &tm_k : &tm_v;
-                        const int c = part % kChunks;
-                        uint8_t* dst = sSlots + slot * kChunkBytes;
-                        mbar_arrive_expect_tx(&ms->full[slot], kChunkBytes);
-                        tma_load_2d_hint(dst, m, 64 * c, row[0], &ms->full[slot], pol_stream);
-                        tma_load_2d_hint(dst + 8192, m, 64 * c, row[1], &ms->full[slot], pol_stream);
-                    }
-                    __syncwarp();
-                    ++chunk;
-                }
+            for (int h = 0; h < 2; ++h) {
+                const int pid = __shfl_sync(0xffffffffu, pid_cur, 2 * (rel & 15) + h);
+                row[h] = pid >= 0 ? (pid * p.Hkv + cur.pc.s % p.Hkv) * kPage : oob_row;
             }
-            ++piece_no;
+            if (!(ok = issue(&tm_k, row[0], row[1]))) break;
+            if (have_v && !(ok = issue(&tm_v, v_row0, v_row1))) break;
+            v_row0 = row[0];
+            v_row1 = row[1];
+            have_v = true;
+            cur.step(p, a.ctx_len);
         }
+        if (ok && have_v) ok = issue(&tm_v, v_row0, v_row1);
         if (!ok || aborted(ms)) {
             set_abort(ms, a.status);
             // wait (bounded) for this CTA's own copies still in flight
             if (lane == 0) {
                 const uint32_t first = chunk > (uint32_t)kNS ? chunk - kNS : 0u;
                 for (uint32_t c = first; c < chunk; ++c) mbar_wait(&ms->full[c % kNS], (c / kNS) & 1, 200000000ll);
+                if (q_loads > 0) mbar_wait(&ms->q_full, (q_loads - 1) & 1, 200000000ll);
             }
         }
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         if (lane == 0) {
             const uint32_t id_qk = idesc_f16(128, RGP, kAB, 0, 0);
-            const uint32_t id_pv = idesc_f16(128, RGP, kAB, 1, 1);
+            const uint32_t id_pv = idesc_f16(128, Lay::kPvN, kAB, 1, 1);
             constexpr uint64_t hi_k = desc_hi(16, 1024, kLayoutSwizzle128);
             constexpr uint64_t hi_v = desc_hi(kChunkBytes, 1024, kLayoutSwizzle128);
             constexpr uint64_t hi_p = desc_hi(128, 2048, kLayoutInterleave);
             const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aS = smem_u32(sSlots);
-            uint32_t chunk = 0;
-            int J = 0, piece_no = 0;
+            uint32_t chunk = 0, jq = 0, j = 0;
             bool ok = true;
-            PieceIter it{t0, t1, 0, 0};
-            Piece pc;
-            while (ok && it.next(p, a.ctx_len, pc)) {
-                if (!(ok = mbar_wait(&ms->q_full, piece_no & 1))) break;
-                for (long long t = pc.ta; t < pc.te; ++t) {
-                    if (aborted(ms)) { ok = false; break; }
-                    // S^T = K . Q^T  (S^T is free: the previous tile's p_full was observed)
-                    for (int c = 0; c < kChunks && ok; ++c) {
-                        const int slot = chunk % kNS;
-                        if (!(ok = mbar_wait(&ms->full[slot], (chunk / kNS) & 1))) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int sub = 0; sub < 4; ++sub) {
-                            const uint64_t ad = make_desc(hi_k, aS + slot * kChunkBytes + sub * 32);
-                            const uint64_t bd = make_desc(hi_k, aQ + c * RGP * 128 + sub * 32);
-                            mma_f16_ss(tmem, ad, bd, id_qk, (c | sub) != 0);
-                        }
-                        mma_commit(&ms->empty[slot]);
-                        ++chunk;
-                    }
-                    if (!ok) break;
-                    if (t == pc.te - 1) mma_commit(&ms->q_empty);
-                    mma_commit(&ms->s_full);
-                    // O^T += V^T . P^T once the softmax has written P^T
-                    if (!(ok = mbar_wait(&ms->p_full, J & 1))) break;
+            TileCursor qk, pv;
+            qk.start(t0, t1, p, a.ctx_len);
+            pv.start(t0, t1, p, a.ctx_len);
+            // S^T(jq) = K(jq) . Q^T; S^T is free once the softmax has read tile jq-1
+            auto issue_qk = [&]() -> bool {
+                if (jq > 0) {
+                    if (!mbar_wait(&ms->s_free, (jq - 1) & 1)) return false;
                     tc_fence_after();
-                    for (int h = 0; h < kChunks / 2 && ok; ++h) {
-                        const int slot = chunk % kNS;  // even; its pair is slot + 1
-                        if (!(ok = mbar_wait(&ms->full[slot], (chunk / kNS) & 1))) break;
-                        if (!(ok = mbar_wait(&ms->full[slot + 1], ((chunk + 1) / kNS) & 1))) break;
-                        tc_fence_after();
+                }
+                if (qk.first()) {
+                    if (!mbar_wait(&ms->q_full, qk.piece_no & 1)) return false;
+                    tc_fence_after();
+                }
+                for (int c = 0; c < kChunks; ++c) {
+                    const int slot = chunk % kNS;
+                    if (!mbar_wait(&ms->full[slot], (chunk / kNS) & 1)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int sub = 0; sub < 4; ++sub) {
+                        const uint64_t ad = make_desc(hi_k, aS + slot * kChunkBytes + sub * 32);
+                        const uint64_t bd = make_desc(hi_k, aQ + c * RGP * 128 + sub * 32);
+                        mma_f16_ss(tmem, ad, bd, id_qk, (c | sub) != 0);
+                    }
+                    mma_commit(&ms->empty[slot]);
+                    ++chunk;
+                }
+                mma_commit(&ms->s_full);
+                if (qk.last()) mma_commit(&ms->q_empty);
+                ++jq;
+                qk.step(p, a.ctx_len);
+                return true;
+            };
+            if (qk.live) ok = issue_qk();
+            while (ok && pv.live) {
+                if (aborted(ms)) {
+                    ok = false;
+                    break;
+                }
+                if (qk.live && !(ok = issue_qk())) break;  // QK(j+1)
+                // O^T += V^T . P^T once the softmax has written P^T(j)
+                if (!(ok = mbar_wait(&ms->p_full, j & 1))) break;
+                tc_fence_after();
+                const bool first = pv.first();
+                for (int h = 0; h < kChunks / 2 && ok; ++h) {
+                    const int slot = chunk % kNS;  // even; its pair is slot + 1
+                    ok = mbar_wait(&ms->full[slot], (chunk / kNS) & 1) &&
+                         mbar_wait(&ms->full[slot + 1], ((chunk + 1) / kNS) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t dO = tmem + (h ? Lay::kColO1 : Lay::kColO0);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t ad = make_desc(hi_v, aS + slot * kChunkBytes + ks * 2048);
+                        const uint64_t bd = make_desc(hi_p, aP + ks * 256);
+                        mma_f16_ss(dO, ad, bd, id_pv, !(first && ks == 0));
+                    }
+                    if constexpr (BF16 && !Lay::kMerge) {
+                        // the lo part of P against the same V, into the same accumulator
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks) {
                             const uint64_t ad = make_desc(hi_v, aS + slot * kChunkBytes + ks * 2048);
-                            const uint64_t bd = make_desc(hi_p, aP + ks * 256);
-                            mma_f16_ss(tmem + (h ? kColO1 : kColO0), ad, bd, id_pv, !(t == pc.ta && ks == 0));
+                            const uint64_t bd = make_desc(hi_p, aP + Lay::kPOneBytes + ks * 256);
+                            mma_f16_ss(dO, ad, bd, id_pv, 1u);
                         }
-                        if constexpr (BF16) {
-                            // the lo part of P against the same V
-#pragma unroll
-                            for (int ks = 0; ks < 8; ++ks) {
-                                const uint64_t ad = make_desc(hi_v, aS + slot * kChunkBytes + ks * 2048);
-                                const uint64_t bd = make_desc(hi_p, aP + Lay::kPOneBytes + ks * 256);
-                                mma_f16_ss(tmem + (h ? kColO1 : kColO0), ad, bd, id_pv, 1u);
-                            }
-                        }
-                        mma_commit(&ms->empty[slot]);
-                        mma_commit(&ms->empty[slot + 1]);
-                        chunk += 2;
                     }
-                    if (!ok) break;
-                    if (t == pc.te - 1) mma_commit(&ms->o_full);
-                    ++J;
+                    mma_commit(&ms->empty[slot]);
+                    mma_commit(&ms->empty[slot + 1]);
+                    chunk += 2;
                 }
-                ++piece_no;
+                if (!ok) break;
+                mma_commit(&ms->pv_done);
+                ++j;
+                pv.step(p, a.ctx_len);
             }
             if (!ok || aborted(ms)) {
                 set_abort(ms, a.status);
@@ -368,34 +463,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    }
     } else {
+        regs_inc<kRegsSoftmax>();
         // ============================================================ softmax + epilogue
         // 12 warps: warp w reads TMEM lanes 32*(w%4)..+31 (its key lanes) and
-        // handles share hf = (w-2)/4 of the row tile's column chunks.
+        // handles share hf = (w-4)/4 of the row tile's column chunks.
         const int quarter = warp & 3;
-        const int hf = (warp - 2) >> 2;  // which share of the column chunks
+        const int hf = (warp - 4) >> 2;
         const int kl = quarter * 32 + lane;  // key lane of S^T, output dim of O^T
-        const int st = threadIdx.x - 64;     // 0..255
+        const int st = threadIdx.x - 128;    // 0..383
         const int cb = min(hf * kNa, kNch), ce = min(cb + kNa, kNch);
+        const int nch = ce - cb;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
         const float sl2 = L.scale_log2;
-        const int my_half = kl >> 6;         // which 64-token page of the tile holds my key
-        int J = 0, piece_no = 0;
-        bool bad = false;
-        PieceIter it{t0, t1, 0, 0};
-        Piece pc;
+        const int my_half = kl >> 6;  // which 64-token page of the tile holds my key
+        uint32_t j = 0;
+        bool bad = false;  // warp-uniform at every tcgen05 load / store below
+        // bounded wait whose outcome all lanes of the warp agree on
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            const bool w = mbar_wait(bar, parity);
+            return __all_sync(0xffffffffu, w);
+        };
+        // the O^T columns of chunk c: d-half h, product part (hi, lo when separate ranges)
+        constexpr int kParts = Lay::kMerge ? 2 : 1;
 
-        // P = 2^(s*scale*log2e - m) for my chunks; lpart += P (sign +1) or -= P
-        // (sign -1, the exact undo of a pass made with the same m); optionally
-        // writes P^T (hi and, for bf16, lo) and tracks the largest exponent.
-        // CHECK = false: every key lane of the warp is valid and every column of
-        // its chunks is a real row, so no per-element masking is needed
+        // One streaming pass over my chunks of S^T: P = 2^(s*scale*log2e - m)
+        // with the current shifts; lpart += P (sign +1) or -= P (sign -1, the
+        // exact undo of a pass made with the same shifts); optionally stores
+        // P^T (hi and, for bf16, lo) and tracks the largest exponent.
+        // kCheck = false: every key lane of the warp is valid and every column
+        // of its chunks is a real row, so no per-element masking is needed.
         auto exp_pass = [&](const bool kCheck, float (&lpart)[kNa * 16], bool valid, float sign, bool write_p,
                             float& ex) {
             // 8-column blocks b = 2*cc + hb; the TMEM load of block b+1 is in
             // flight while block b is computed
             constexpr int kBlocks = 2 * kNa;
-            const int nblk = 2 * (ce - cb);
+            const int nblk = 2 * nch;
             uint32_t rn[8];
             tmem_ld8(tl + 16 * cb, rn);
 #pragma unroll
@@ -404,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[8];
                 tmem_wait_ld_regs(rn);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) r[j] = rn[j];
+                for (int k = 0; k < 8; ++k) r[k] = rn[k];
                 if (bi + 1 < nblk) tmem_ld8(tl + 16 * cb + 8 * (bi + 1), rn);
                 const int cc = bi >> 1, hb = bi & 1;
                 const int c = cb + cc;
@@ -414,18 +518,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
                 float pv[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float x = fmaf(__uint_as_float(r[j]), sl2, -mv[j]);
+                for (int k = 0; k < 8; ++k) {
+                    const float x = fmaf(__uint_as_float(r[k]), sl2, -mv[k]);
                     if (kCheck) {
-                        const bool ok = 8 * hb + j < lim;
+                        const bool ok = 8 * hb + k < lim;
                         if (ok) ex = fmaxf(ex, x);
-                        pv[j] = ok ? ex2(x) : 0.f;
+                        pv[k] = ok ? ex2(x) : 0.f;
                     } else {
                         ex = fmaxf(ex, x);
-                        pv[j] = ex2(x);
+                        pv[k] = ex2(x);
                     }
-                    float& acc = lpart[cc * 16 + 8 * hb + j];
-                    acc = fmaf(sign, pv[j], acc);
+                    float& acc = lpart[cc * 16 + 8 * hb + k];
+                    acc = fmaf(sign, pv[k], acc);
                 }
                 if (write_p) {
                     const int nb = 2 * c + hb;
@@ -448,9 +552,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
 
-        while (it.next(p, a.ctx_len, pc)) {
-            const int npages = (pc.L + kPage - 1) / kPage;
-            const int32_t* pt = a.page_table + (size_t)pc.b * p.max_pages;
+        TileCursor cur;
+        cur.start(t0, t1, p, a.ctx_len);
+
+        while (cur.live) {
+            const int piece_no = cur.piece_no;
+            const int seg = cur.pc.s;
             bar_sync(1, kSoftmaxThreads);
             for (int col = st; col < RGP; col += kSoftmaxThreads) ms->m_ref[col] = -INFINITY;
             bar_sync(1, kSoftmaxThreads);
@@ -459,28 +566,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < kNa * 16; ++i) lpart[i] = 0.f;
             uint32_t page_bits = 0;
 
-            for (long long t = pc.ta; t < pc.te; ++t, ++J) {
+            while (cur.live && cur.piece_no == piece_no) {
+                const int t = cur.t;
                 // validity of my page for 32 tiles at a time (one load per lane)
-                const int tb = (int)((t - pc.ta) & 31);
+                const int tb = (t - cur.pc.ta) & 31;
                 if (tb == 0) {
-                    const long long tt = t + lane;
-                    const long long pg = 2 * tt + my_half;
-                    bool ok = false;
-                    if (tt < pc.te && pg < npages) {
-                        const int pid = pt[pg];
-                        ok = pid >= 0 && pid < a.num_pages;
+                    const int tt = t + lane;
+                    const int pg = 2 * tt + my_half;
+                    bool okp = false;
+                    if (tt < cur.pc.te && pg < (cur.pc.L + kPage - 1) / kPage) {
+                        const int pid = a.page_table[(size_t)(seg / p.Hkv) * p.max_pages + pg];
+                        okp = pid >= 0 && pid < a.num_pages;
                     }
-                    page_bits = __ballot_sync(0xffffffffu, ok);
+                    page_bits = __ballot_sync(0xffffffffu, okp);
                 }
-                const int nvalid = (int)min((long long)kTileKeys, (long long)pc.L - t * kTileKeys);
+                const int nvalid = min(kTileKeys, cur.pc.L - t * kTileKeys);
                 const bool page_ok = (page_bits >> tb) & 1u;
                 const bool valid = kl < nvalid && page_ok;
-                const bool got = mbar_wait(&ms->s_full, J & 1);
-                if (bar_sync_or(1, kSoftmaxThreads, bad || !got)) {
-                    bad = true;
-                    break;
-                }
-                tc_fence_after();
+                const bool first = cur.first();
+
+                // S^T(j) ready; P^T and O^T free once PV(j-1) has completed
+                if (!bad && !wait_all(&ms->s_full, j & 1)) bad = true;
+                if (!bad && j > 0 && !wait_all(&ms->pv_done, (j - 1) & 1)) bad = true;
+                if (!bad) tc_fence_after();
 
                 // pass 0: exponents with the current shifts (P^T written, sums added,
                 //         largest exponent voted across the CTA)
@@ -488,87 +596,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                 //         subtracted (exact undo)
                 // pass 2: exact column maxima move the shifts, then P^T and sums again
                 // The first tile of a range has no shifts yet and starts at pass 2.
-                bool slow = t == pc.ta;
+                float ex = -INFINITY;
                 const bool unmasked = __all_sync(0xffffffffu, valid) && R_seg >= 16 * ce;
-                for (int pass = slow ? 2 : 0; pass < 3; ++pass) {
-                    if (pass == 2) {
-                        // exact column maxima of this tile, then move the shifts
-#pragma unroll 1
-                        for (int cc = 0; cc < kNa; ++cc) {
-                            const int c = cb + cc;
-                            if (c >= ce) continue;
-                            uint32_t r[16];
-                            tmem_ld16(tl + 16 * c, r);
-                            tmem_wait_ld();
-                            const int lim = valid ? R_seg - 16 * c : 0;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                float y = j < lim ? __uint_as_float(r[j]) * sl2 : -INFINITY;
-                                y = warp_max(y);
-                                if (lane == 0) ms->col_red[quarter][16 * c + j] = y;
-                            }
-                        }
-                        bar_sync(1, kSoftmaxThreads);
-                        for (int col = st; col < RGP; col += kSoftmaxThreads) {
-                            const float cm = fmaxf(fmaxf(ms->col_red[0][col], ms->col_red[1][col]),
-                                                   fmaxf(ms->col_red[2][col], ms->col_red[3][col]));
-                            const float mo = ms->m_ref[col];
-                            const float mn = fmaxf(mo, cm);
-                            ms->alpha[col] = mn > mo ? ex2(mo - mn) : 1.f;
-                            ms->m_ref[col] = mn;
-                        }
-                        bar_sync(1, kSoftmaxThreads);
-#pragma unroll
-                        for (int cc = 0; cc < kNa; ++cc) {
-                            const int c = cb + cc;
-                            if (c >= ce) continue;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) lpart[cc * 16 + j] *= ms->alpha[16 * c + j];
-                        }
-                        if (t != pc.ta) {
-                            // O^T columns accumulated so far move with their shift
-#pragma unroll 1
-                            for (int cc = 0; cc < kNa; ++cc) {
-                                const int c = cb + cc;
-                                if (c >= ce) continue;
-                                bool any = false;
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) any |= ms->alpha[16 * c + j] != 1.f;
-                                if (!any) continue;
-#pragma unroll 1
-                                for (int h = 0; h < kChunks / 2; ++h) {
-                                    uint32_t r[16];
-                                    const uint32_t addr = tl + (h ? kColO1 : kColO0) + 16 * c;
-                                    tmem_ld16(addr, r);
-                                    tmem_wait_ld();
-#pragma unroll
-                                    for (int j = 0; j < 16; ++j)
-                                        r[j] = __float_as_uint(__uint_as_float(r[j]) * ms->alpha[16 * c + j]);
-                                    tmem_st16(addr, r);
-                                }
-                            }
-                            tmem_wait_st();
-                        }
-                    }
-                    float ex = -INFINITY;
-                    if (pass == 0 && unmasked) exp_pass(false, lpart, valid, 1.f, true, ex);
-                    else exp_pass(true, lpart, valid, pass == 1 ? -1.f : 1.f, pass != 1, ex);
-                    if (pass == 0) {
-                        ex = warp_max(ex);
-                        if (lane == 0) ms->ex_red[warp - 2] = ex;
-                        bar_sync(1, kSoftmaxThreads);
-#pragma unroll
-                        for (int w = 0; w < kSmWarps; ++w) ex = fmaxf(ex, ms->ex_red[w]);
-                        slow = ex > kTau;
-                        if (!slow) break;
-                    }
+                if (!bad && !first) {
+                    if (unmasked) exp_pass(false, lpart, valid, 1.f, true, ex);
+                    else exp_pass(true, lpart, valid, 1.f, true, ex);
                 }
+                // one barrier decides the path; a second one only when it says
+                // "slow", to tell a timeout (somewhere) from a shift update
+                const bool bad_now = bad || aborted(ms);
+                const bool slow = bar_sync_or(1, kSoftmaxThreads, bad_now || first || ex > kTau);
+                if (slow && bar_sync_or(1, kSoftmaxThreads, bad_now)) {
+                    bad = true;
+                    break;
+                }
+                if (slow) {
+                    if (!first) exp_pass(true, lpart, valid, -1.f, false, ex);  // pass 1
+                    // pass 2: exact column maxima of this tile, then move the shifts
+#pragma unroll 1
+                    for (int cc = 0; cc < nch; ++cc) {
+                        const int c = cb + cc;
+                        uint32_t r[16];
+                        tmem_ld16(tl + 16 * c, r);
+                        tmem_wait_ld_regs16(r);
+                        const int lim = valid ? R_seg - 16 * c : 0;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const float v = warp_max(k < lim ? __uint_as_float(r[k]) * sl2 : -INFINITY);
+                            if (lane == 0) ms->col_red[quarter][16 * c + k] = v;
+                        }
+                    }
+                    bar_sync(1, kSoftmaxThreads);
+                    for (int col = st; col < RGP; col += kSoftmaxThreads) {
+                        const float cm = fmaxf(fmaxf(ms->col_red[0][col], ms->col_red[1][col]),
+                                               fmaxf(ms->col_red[2][col], ms->col_red[3][col]));
+                        const float mo = ms->m_ref[col];
+                        const float mn = fmaxf(mo, cm);
+                        ms->alpha[col] = mn > mo ? ex2(mo - mn) : 1.f;
+                        ms->m_ref[col] = mn;
+                    }
+                    bar_sync(1, kSoftmaxThreads);
+#pragma unroll
+                    for (int cc = 0; cc < kNa; ++cc) {
+                        if (cc >= nch) continue;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) lpart[cc * 16 + k] *= ms->alpha[16 * (cb + cc) + k];
+                    }
+                    if (!first) {
+                        // O^T columns accumulated so far move with their shift
+#pragma unroll 1
+                        for (int cc = 0; cc < nch; ++cc) {
+                            const int c = cb + cc;
+                            bool any = false;
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) any |= ms->alpha[16 * c + k] != 1.f;
+                            if (!any) continue;
+#pragma unroll 1
+                            for (int part = 0; part < Lay::kDh * kParts; ++part) {
+                                const int h = part / kParts;
+                                uint32_t r[16];
+                                const uint32_t addr =
+                                    tl + (h ? Lay::kColO1 : Lay::kColO0) + (part % kParts) * RGP + 16 * c;
+                                tmem_ld16(addr, r);
+                                tmem_wait_ld_regs16(r);
+#pragma unroll
+                                for (int k = 0; k < 16; ++k)
+                                    r[k] = __float_as_uint(__uint_as_float(r[k]) * ms->alpha[16 * c + k]);
+                                tmem_st16(addr, r);
+                            }
+                        }
+                        tmem_wait_st();
+                    }
+                    exp_pass(true, lpart, valid, 1.f, true, ex);
+                }
+                // S^T is no longer read: the next tile's QK may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ms->s_free);
 
                 // keys past L inside the last (partial) page: their V rows hold
                 // whatever the pool has there; zero them so 0 * V stays 0
                 if (hf == 0 && (nvalid & (kPage - 1)) != 0 && kl >= nvalid &&
                     kl < ((nvalid + kPage - 1) & ~(kPage - 1)) && page_ok) {
-                    const uint32_t vbase = (uint32_t)J * (2 * kChunks) + kChunks;
+                    const uint32_t vbase = v_operand(j, n_tiles) * kChunks;
                     for (int c = 0; c < kChunks; ++c) {
                         const uint32_t ch = vbase + c;
                         if (!mbar_wait(&ms->full[ch % kNS], (ch / kNS) & 1)) {
@@ -582,54 +692,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ms->p_full);
+                bad = __any_sync(0xffffffffu, bad);  // the partial-page wait above is per lane
+                if (!bad && lane == 0) mbar_arrive(&ms->p_full);
+                ++j;
+                cur.step(p, a.ctx_len);
             }
-            if (bad) break;
 
             // ---------------------------------------------------------- epilogue
-            const bool got = mbar_wait(&ms->o_full, piece_no & 1);
-            if (bar_sync_or(1, kSoftmaxThreads, bad || !got)) {
+            // (also the consensus point for a timeout in the piece's last tile)
+            const bool got = !bad && mbar_wait(&ms->pv_done, (j - 1) & 1);
+            if (bar_sync_or(1, kSoftmaxThreads, bad || !got || aborted(ms))) {
                 bad = true;
                 break;
             }
             tc_fence_after();
+            // row sums: the partial sums of all 128 key lanes go through the P^T
+            // buffer (idle now that PV is done; RGP x 128 floats fit exactly)
+            float* red = reinterpret_cast<float*>(sP);
+            static_assert(RGP * 128 * 4 <= Lay::kPBytes || !BF16, "row-sum staging fits the P^T buffer");
+            static_assert(BF16 || RGP * 128 * 4 <= Lay::kPBytes + Lay::kNS * kChunkBytes, "row-sum staging");
 #pragma unroll
             for (int cc = 0; cc < kNa; ++cc) {
-                const int c = cb + cc;
-                if (c >= ce) continue;
+                if (cc >= nch) continue;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float v = warp_sum(lpart[cc * 16 + j]);
-                    if (lane == 0) ms->col_red[quarter][16 * c + j] = v;
-                }
+                for (int k = 0; k < 16; ++k) red[(16 * (cb + cc) + k) * 128 + kl] = lpart[cc * 16 + k];
             }
             bar_sync(1, kSoftmaxThreads);
-            float* slot = L.ws + slot_index(p, rg, cta, pc.s) * slot_floats(p);
+            float* slot = L.ws + slot_index(p, rg, cta, seg) * slot_floats(p);
             float* slot_m = slot + (size_t)RG * D;
             float* slot_l = slot_m + RG;
-            for (int col = st; col < R_seg; col += kSoftmaxThreads) {
-                slot_l[col] = ms->col_red[0][col] + ms->col_red[1][col] + ms->col_red[2][col] + ms->col_red[3][col];
-                slot_m[col] = ms->m_ref[col];
+            for (int col = warp - 4; col < R_seg; col += kSmWarps) {
+                const float4 v = reinterpret_cast<const float4*>(red + col * 128)[lane];
+                const float sum = warp_sum((v.x + v.y) + (v.z + v.w));
+                if (lane == 0) {
+                    slot_l[col] = sum;
+                    slot_m[col] = ms->m_ref[col];
+                }
             }
 #pragma unroll
             for (int cc = 0; cc < kNa; ++cc) {
+                if (cc >= nch) continue;
                 const int c = cb + cc;
-                if (c >= ce) continue;
 #pragma unroll
-                for (int h = 0; h < kChunks / 2; ++h) {
+                for (int h = 0; h < Lay::kDh; ++h) {
                     uint32_t r[16];
-                    tmem_ld16(tl + (h ? kColO1 : kColO0) + 16 * c, r);
-                    tmem_wait_ld();
+                    const uint32_t addr = tl + (h ? Lay::kColO1 : Lay::kColO0) + 16 * c;
+                    tmem_ld16(addr, r);
+                    if constexpr (Lay::kMerge) {
+                        // O = V^T.P_hi^T + V^T.P_lo^T
+                        uint32_t r2[16];
+                        tmem_ld16(addr + RGP, r2);
+                        tmem_wait_ld_regs16(r);
+                        tmem_wait_ld_regs16(r2);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = 16 * c + j;
-                        if (col < R_seg) slot[(size_t)col * D + h * 128 + kl] = __uint_as_float(r[j]);
+                        for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) + __uint_as_float(r2[k]));
+                    } else {
+                        tmem_wait_ld_regs16(r);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int col = 16 * c + k;
+                        if (col < R_seg) slot[(size_t)col * D + h * 128 + kl] = __uint_as_float(r[k]);
                     }
                 }
             }
             tc_fence_before();
-            ++piece_no;
         }
         if (bad) set_abort(ms, a.status);
     }
@@ -659,6 +786,7 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const CUten
 template <int D, bool BF16>
 cudaError_t launch_rgp(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                        const AttnLaunch& L, cudaStream_t stream) {
+    static_assert(kRowsMax == 144, "one instantiation per padded row count up to kRowsMax");
     switch (rgp) {
         case 16: return launch_one<D, BF16, 16>(tk, tv, tq, L, stream);
         case 32: return launch_one<D, BF16, 32>(tk, tv, tq, L, stream);
