@@ -1,17 +1,20 @@
 // attn_merge.cu -- tree block + log-sum-exp merge of tree-verify attention.
 //
-// One warp per output row (b, node i, head h).  The warp runs the softmax
+// One block per output row (b, node i, head h).  The warps share the softmax
 // over the tree keys j with bit j of anc_mask[b][i] set (the node's ancestors
-// and itself), then folds in the prefix partials (O, max, sum) that the
-// split-K prefix kernel left for this row's segment, and writes
-// out = O / sum and lse = ln(sum) + max.  Maxima are kept in the log2 domain
+// and itself) and the prefix partials (O, max, sum) that the split-K prefix
+// kernel left for this row's key segment; the block writes out = O / sum and
+// lse = ln(sum) + max.  Maxima are kept in the log2 domain
 // (scores pre-multiplied by log2 e), so every rescale is one exp2.
 //
-// The split partials are independent, so the warp reads their maxima and sums
-// with one lane per split, forms every split's weight once, and then adds the
-// weighted partial rows with several loads in flight instead of walking the
-// splits one dependent load at a time.
+// The partials are independent: their maxima are reduced first (one thread
+// per partial), then warp w adds the weighted partial rows w, w + 8, ... with
+// several 16-byte loads in flight per lane, and the eight warp sums are added
+// through shared memory.  A block reads about 40 partial rows of D floats, so
+// spreading them over eight warps keeps enough loads in flight to stream the
+// partials at memory speed instead of one dependent row at a time.
 #include "internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace lucetree {
 
@@ -28,8 +31,9 @@ __device__ inline float warp_max(float v) {
     return v;
 }
 
-constexpr int kRowsPerBlock = 4;
-constexpr int kBatch = 8;  // partial rows in flight per lane
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kUnroll = 2;  // partial rows per warp iteration (2 x D/32 floats per lane in flight)
 
 template <typename T, int D>
 __device__ inline void load_slice(const T* p, float (&out)[D / 32]) {
@@ -37,15 +41,26 @@ __device__ inline void load_slice(const T* p, float (&out)[D / 32]) {
     else load4_f32<T>(p, out);
 }
 
+template <int DPL>
+__device__ inline void load_partial(const float* op, float (&v)[DPL]) {
+    const float4 a = *reinterpret_cast<const float4*>(op);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    if constexpr (DPL == 8) {
+        const float4 b = *reinterpret_cast<const float4*>(op + 4);
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kRowsPerBlock * 32) merge_kernel(AttnLaunch L) {
+__global__ void __launch_bounds__(kThreads) merge_kernel(AttnLaunch L) {
     constexpr int DPL = D / 32;
+    __shared__ float s_o[kWarps][D];
+    __shared__ float s_red[kWarps];
+
     const lucetree_attn_args& a = L.a;
     const PlanDims& p = L.plan;
-    const int lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    const long long total_rows = (long long)p.B * p.N * p.Hq;
-    if (row >= total_rows) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = blockIdx.x;
     const int h = (int)(row % p.Hq);
     const int i = (int)((row / p.Hq) % p.N);
     const int b = (int)(row / ((long long)p.Hq * p.N));
@@ -54,131 +69,145 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) merge_kernel(AttnLaunch L)
     const int rl = (i - rg * p.rg.NPG) * p.G + (h % p.G);
     const int s = b * p.Hkv + g;
 
-    float qf[DPL];
-    load_slice<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)row * D + lane * DPL, qf);
-
-    // ---- tree block: keys of the node's ancestors and itself
-    uint64_t anc = a.anc_mask[(size_t)b * p.N + i];
-    if (p.N < 64) anc &= (1ull << p.N) - 1ull;
-    if (!((anc >> i) & 1ull) && lane == 0) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
-    float m = -INFINITY, l = 0.f, o[DPL];
+    // ---- tree block: keys of the node's ancestors and itself, the k-th such
+    // key (in node order) handled by warp k % kWarps with its own running
+    // max, sum and output slice
+    float o[DPL];
 #pragma unroll
     for (int x = 0; x < DPL; ++x) o[x] = 0.f;
-    const T* kt = reinterpret_cast<const T*>(a.k_tree);
-    const T* vt = reinterpret_cast<const T*>(a.v_tree);
-    while (anc) {
-        const int j = __ffsll((long long)anc) - 1;
-        anc &= anc - 1ull;
-        const size_t base = (((size_t)b * p.N + j) * p.Hkv + g) * D + lane * DPL;
-        float kf[DPL], vf[DPL];
-        load_slice<T, D>(kt + base, kf);
-        load_slice<T, D>(vt + base, vf);
-        float dot = 0.f;
+    float m_t = -INFINITY, l_t = 0.f;
+    {
+        float qf[DPL];
+        load_slice<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)row * D + lane * DPL, qf);
+        uint64_t anc = a.anc_mask[(size_t)b * p.N + i];
+        if (p.N < 64) anc &= (1ull << p.N) - 1ull;
+        if (!((anc >> i) & 1ull) && threadIdx.x == 0) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
+        const T* kt = reinterpret_cast<const T*>(a.k_tree);
+        const T* vt = reinterpret_cast<const T*>(a.v_tree);
+        int rank = 0;
+        while (anc) {
+            const int j = __ffsll((long long)anc) - 1;
+            anc &= anc - 1ull;
+            if ((rank++ % kWarps) != warp) continue;
+            const size_t base = (((size_t)b * p.N + j) * p.Hkv + g) * D + lane * DPL;
+            float kf[DPL], vf[DPL];
+            load_slice<T, D>(kt + base, kf);
+            load_slice<T, D>(vt + base, vf);
+            float dot = 0.f;
 #pragma unroll
-        for (int x = 0; x < DPL; ++x) dot = fmaf(qf[x], kf[x], dot);
-        const float sc = warp_sum(dot) * L.scale_log2;
-        const float mn = fmaxf(m, sc);
-        const float alpha = exp2f(m - mn), pj = exp2f(sc - mn);
-        l = l * alpha + pj;
+            for (int x = 0; x < DPL; ++x) dot = fmaf(qf[x], kf[x], dot);
+            const float sc = warp_sum(dot) * L.scale_log2;
+            const float mn = fmaxf(m_t, sc);
+            const float alpha = exp2f(m_t - mn), pj = exp2f(sc - mn);
+            l_t = l_t * alpha + pj;
 #pragma unroll
-        for (int x = 0; x < DPL; ++x) o[x] = fmaf(o[x], alpha, pj * vf[x]);
-        m = mn;
+            for (int x = 0; x < DPL; ++x) o[x] = fmaf(o[x], alpha, pj * vf[x]);
+            m_t = mn;
+        }
     }
 
     // ---- committed prefix: partials of every CTA that covered this segment
-    const int Lb = seq_len(a.ctx_len, b, p.max_pages, (i == 0 && h == 0 && lane == 0) ? a.status : nullptr);
+    // (this kernel is launched as a programmatic dependent of the prefix
+    // kernel: everything above overlaps its tail, nothing below may)
+    tc::griddep_wait();
+    const int Lb = seq_len(a.ctx_len, b, p.max_pages, (i == 0 && h == 0 && threadIdx.x == 0) ? a.status : nullptr);
+    int count = 0, c_lo = 0;
+    long long nT = 0;
     if (Lb > 0) {
-        const long long nT = total_tiles(p, a.ctx_len);
+        nT = total_tiles(p, a.ctx_len);
         const long long first = segment_offset(p, a.ctx_len, s);
         const long long last = first + tiles_of(Lb) - 1;
-        const int c_lo = cta_of_tile(first, nT, p.Cg), c_hi = cta_of_tile(last, nT, p.Cg);
-        const int count = c_hi - c_lo + 1;
-        const size_t sf = slot_floats(p);
-        const size_t slot0 = slot_index(p, rg, c_lo, s);
-        const float* ws = L.ws;
-        // with fewer tiles than CTAs some CTAs own no tile and write no partial
-        auto weight_of = [&](int k, float& mk, float& lk) {
-            const int c = c_lo + k;
-            mk = -INFINITY;
-            lk = 0.f;
-            if (k < count && cta_begin(c, nT, p.Cg) != cta_begin(c + 1, nT, p.Cg)) {
-                const float* slot = ws + (slot0 + k) * sf + (size_t)p.rg.RG * D;
-                mk = slot[rl];
-                lk = slot[p.rg.RG + rl];
-            }
-        };
-        // pass 1: the common shift and the sum, one lane per split
-        float mmax = m;
-        for (int k0 = 0; k0 < count; k0 += 32) {
-            float mk, lk;
-            weight_of(k0 + lane, mk, lk);
-            mmax = fmaxf(mmax, warp_max(mk));
-        }
-        const float a_tree = m > -INFINITY ? exp2f(m - mmax) : 0.f;
-        float lsum = 0.f;
-#pragma unroll
-        for (int x = 0; x < DPL; ++x) o[x] *= a_tree;
-        // pass 2: weighted partial rows, kBatch loads in flight
-        for (int k0 = 0; k0 < count; k0 += 32) {
-            float mk, lk;
-            weight_of(k0 + lane, mk, lk);
-            const float wk = mk > -INFINITY ? exp2f(mk - mmax) : 0.f;
-            lsum += wk * lk;
-            const int n = min(32, count - k0);
-            for (int e0 = 0; e0 < n; e0 += kBatch) {
-                float w[kBatch];
-                float part[kBatch][DPL];
-#pragma unroll
-                for (int e = 0; e < kBatch; ++e) {
-                    w[e] = __shfl_sync(0xffffffffu, wk, (e0 + e) & 31);
-                    if (e0 + e < n && w[e] != 0.f) {
-                        const float* op = ws + (slot0 + k0 + e0 + e) * sf + (size_t)rl * D + lane * DPL;
-                        if constexpr (DPL == 8) {
-                            const float4 v0 = *reinterpret_cast<const float4*>(op);
-                            const float4 v1 = *reinterpret_cast<const float4*>(op + 4);
-                            part[e][0] = v0.x; part[e][1] = v0.y; part[e][2] = v0.z; part[e][3] = v0.w;
-                            part[e][4] = v1.x; part[e][5] = v1.y; part[e][6] = v1.z; part[e][7] = v1.w;
-                        } else {
-                            const float4 v0 = *reinterpret_cast<const float4*>(op);
-                            part[e][0] = v0.x; part[e][1] = v0.y; part[e][2] = v0.z; part[e][3] = v0.w;
-                        }
-                    } else {
-                        w[e] = 0.f;
-#pragma unroll
-                        for (int x = 0; x < DPL; ++x) part[e][x] = 0.f;
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < kBatch; ++e)
-#pragma unroll
-                    for (int x = 0; x < DPL; ++x) o[x] = fmaf(part[e][x], w[e], o[x]);
-            }
-        }
-        l = l * a_tree + warp_sum(lsum);
-        m = mmax;
+        c_lo = cta_of_tile(first, nT, p.Cg);
+        count = cta_of_tile(last, nT, p.Cg) - c_lo + 1;
     }
+    const size_t sf = slot_floats(p);
+    const float* ws = L.ws + slot_index(p, rg, c_lo, s) * sf;
+    // with fewer tiles than CTAs some CTAs own no tile and write no partial
+    auto has_partial = [&](int k) {
+        return k < count && cta_begin(c_lo + k, nT, p.Cg) != cta_begin(c_lo + k + 1, nT, p.Cg);
+    };
 
-    const float inv = 1.f / l;
-    float* orow = a.out + (size_t)row * D + lane * DPL;
+    // pass 1: the common shift (maximum over the tree parts and every partial)
+    float mk_local = m_t;
+    for (int k = threadIdx.x; k < count; k += kThreads)
+        if (has_partial(k)) mk_local = fmaxf(mk_local, ws[k * sf + (size_t)p.rg.RG * D + rl]);
+    mk_local = warp_max(mk_local);
+    if (lane == 0) s_red[warp] = mk_local;
+    __syncthreads();
+    float mmax = -INFINITY;
 #pragma unroll
-    for (int x = 0; x < DPL; x += 4)
-        *reinterpret_cast<float4*>(orow + x) = make_float4(o[x] * inv, o[x + 1] * inv, o[x + 2] * inv, o[x + 3] * inv);
-    if (a.lse && lane == 0) a.lse[row] = (m + log2f(l)) * kLn2;
+    for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, s_red[w]);
+    const float a_tree = m_t > -INFINITY ? exp2f(m_t - mmax) : 0.f;
+#pragma unroll
+    for (int x = 0; x < DPL; ++x) o[x] *= a_tree;
+
+    // pass 2: weighted partial rows, warp w takes partials w, w + kWarps, ...
+    float lsum = l_t * a_tree;  // this warp's sums (the same in every lane)
+    for (int k0 = warp * kUnroll; k0 < count; k0 += kWarps * kUnroll) {
+        float w[kUnroll];
+        float part[kUnroll][DPL];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int k = k0 + u;
+            w[u] = 0.f;
+            if (has_partial(k)) {
+                const float* slot = ws + (size_t)k * sf;
+                const float mk = slot[(size_t)p.rg.RG * D + rl];
+                const float lk = slot[(size_t)p.rg.RG * D + p.rg.RG + rl];
+                w[u] = mk > -INFINITY ? exp2f(mk - mmax) : 0.f;
+                lsum += w[u] * lk;
+                load_partial<DPL>(slot + (size_t)rl * D + lane * DPL, part[u]);
+            } else {
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) part[u][x] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int x = 0; x < DPL; ++x) o[x] = fmaf(part[u][x], w[u], o[x]);
+    }
+#pragma unroll
+    for (int x = 0; x < DPL; ++x) s_o[warp][lane * DPL + x] = o[x];
+    __syncthreads();
+    if (lane == 0) s_red[warp] = lsum;  // every lane of a warp holds the same lsum
+    __syncthreads();
+
+    // ---- combine the warps' sums and write the row
+    float l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) l += s_red[w];
+    const float inv = 1.f / l;
+    float* orow = a.out + (size_t)row * D;
+    for (int d = threadIdx.x; d < D; d += kThreads) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += s_o[w][d];
+        orow[d] = v * inv;
+    }
+    if (a.lse && threadIdx.x == 0) a.lse[row] = (mmax + log2f(l)) * kLn2;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_merge(const AttnLaunch& L, cudaStream_t stream) {
     const long long rows = (long long)L.plan.B * L.plan.N * L.plan.Hq;
-    dim3 grid((unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock)), block(kRowsPerBlock * 32);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (L.a.dtype == LUCETREE_BF16) {
-        if (L.a.D == 256) merge_kernel<__nv_bfloat16, 256><<<grid, block, 0, stream>>>(L);
-        else merge_kernel<__nv_bfloat16, 128><<<grid, block, 0, stream>>>(L);
-    } else {
-        if (L.a.D == 256) merge_kernel<__half, 256><<<grid, block, 0, stream>>>(L);
-        else merge_kernel<__half, 128><<<grid, block, 0, stream>>>(L);
+        if (L.a.D == 256) return cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16, 256>, L);
+        return cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16, 128>, L);
     }
-    return cudaGetLastError();
+    if (L.a.D == 256) return cudaLaunchKernelEx(&cfg, merge_kernel<__half, 256>, L);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<__half, 128>, L);
 }
 
 }  // namespace lucetree

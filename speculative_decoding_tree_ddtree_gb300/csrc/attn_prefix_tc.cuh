@@ -236,6 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int R_seg = (min(p.N, i0 + p.rg.NPG) - i0) * p.G;
     const int RG = p.rg.RG;
 
+    // the merge kernel may start its blocks as SMs free up; it waits for this
+    // grid's completion before it reads the partials
+    if (threadIdx.x == 0) griddep_launch_dependents();
     const long long nT = total_tiles(p, a.ctx_len);
     const int t0 = nT ? (int)cta_begin(cta, nT, p.Cg) : 0, t1 = nT ? (int)cta_begin(cta + 1, nT, p.Cg) : 0;
     if (t0 >= t1) return;  // uniform across the CTA
