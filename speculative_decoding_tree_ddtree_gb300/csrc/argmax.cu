@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const float* __restric
                                                           unsigned* __restrict__ tickets) {
     __shared__ unsigned long long red[kThreads / 32];
     __shared__ bool is_last;
+    pdl_wait();
+    pdl_trigger();
     const int row = blockIdx.y, ch = blockIdx.x;
     const long long per = (((long long)vocab + chunks - 1) / chunks + 3) / 4 * 4;  // multiple of 4 elements
     const long long k0 = ch * per;
@@ -129,8 +131,8 @@ cudaError_t launch_argmax(const float* logits, int rows, int vocab, long long ro
     cudaError_t e = cudaMemsetAsync(tickets, 0, (size_t)rows * sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
     dim3 grid(chunks, rows);
-    argmax_kernel<<<grid, kThreads, 0, stream>>>(logits, vocab, row_stride, chunks, out_idx, part, tickets);
-    return cudaGetLastError();
+    return launch_pdl(argmax_kernel, grid, dim3(kThreads), 0, stream, logits, vocab, row_stride, chunks, out_idx,
+                      part, tickets);
 }
 
 }  // namespace lucetree

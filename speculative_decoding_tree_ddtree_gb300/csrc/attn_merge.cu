@@ -14,7 +14,6 @@
 // spreading them over eight warps keeps enough loads in flight to stream the
 // partials at memory speed instead of one dependent row at a time.
 #include "internal.cuh"
-#include "tc_ptx.cuh"
 
 namespace lucetree {
 
@@ -61,6 +60,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(AttnLaunch L) {
     const PlanDims& p = L.plan;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = blockIdx.x;
+    if (threadIdx.x == 0) pdl_trigger();
     const int h = (int)(row % p.Hq);
     const int i = (int)((row / p.Hq) % p.N);
     const int b = (int)(row / ((long long)p.Hq * p.N));
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(AttnLaunch L) {
     // ---- committed prefix: partials of every CTA that covered this segment
     // (this kernel is launched as a programmatic dependent of the prefix
     // kernel: everything above overlaps its tail, nothing below may)
-    tc::griddep_wait();
+    pdl_wait();
     const int Lb = seq_len(a.ctx_len, b, p.max_pages, (i == 0 && h == 0 && threadIdx.x == 0) ? a.status : nullptr);
     int count = 0, c_lo = 0;
     long long nT = 0;
@@ -191,23 +191,13 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(AttnLaunch L) {
 }  // namespace
 
 cudaError_t launch_attn_merge(const AttnLaunch& L, cudaStream_t stream) {
-    const long long rows = (long long)L.plan.B * L.plan.N * L.plan.Hq;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)rows);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const dim3 grid((unsigned)((long long)L.plan.B * L.plan.N * L.plan.Hq)), block(kThreads);
     if (L.a.dtype == LUCETREE_BF16) {
-        if (L.a.D == 256) return cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16, 256>, L);
-        return cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16, 128>, L);
+        if (L.a.D == 256) return launch_pdl(merge_kernel<__nv_bfloat16, 256>, grid, block, 0, stream, L);
+        return launch_pdl(merge_kernel<__nv_bfloat16, 128>, grid, block, 0, stream, L);
     }
-    if (L.a.D == 256) return cudaLaunchKernelEx(&cfg, merge_kernel<__half, 256>, L);
-    return cudaLaunchKernelEx(&cfg, merge_kernel<__half, 128>, L);
+    if (L.a.D == 256) return launch_pdl(merge_kernel<__half, 256>, grid, block, 0, stream, L);
+    return launch_pdl(merge_kernel<__half, 128>, grid, block, 0, stream, L);
 }
 
 }  // namespace lucetree

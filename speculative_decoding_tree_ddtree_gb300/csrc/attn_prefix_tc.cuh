@@ -236,9 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int R_seg = (min(p.N, i0 + p.rg.NPG) - i0) * p.G;
     const int RG = p.rg.RG;
 
-    // the merge kernel may start its blocks as SMs free up; it waits for this
-    // grid's completion before it reads the partials
-    if (threadIdx.x == 0) griddep_launch_dependents();
+    // inputs may come from the previous kernel on the stream (programmatic
+    // dependent launch): wait for it, then let the merge kernel start its
+    // blocks as SMs free up (it waits for this grid before reading partials)
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     const long long nT = total_tiles(p, a.ctx_len);
     const int t0 = nT ? (int)cta_begin(cta, nT, p.Cg) : 0, t1 = nT ? (int)cta_begin(cta + 1, nT, p.Cg) : 0;
     if (t0 >= t1) return;  // uniform across the CTA
@@ -782,8 +784,7 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const CUten
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<grid_ctas(L.plan), kThreads, Lay::kBytes, stream>>>(tk, tv, tq, L);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid_ctas(L.plan)), dim3(kThreads), Lay::kBytes, stream, tk, tv, tq, L);
 }
 
 template <int D, bool BF16>

@@ -197,4 +197,31 @@ cudaError_t launch_argmax(const float* logits, int rows, int vocab, long long ro
 
 int device_sm_count(int device);
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every library kernel is launched so that it
+// may start while the previous kernel on the stream finishes; it executes
+// pdl_wait() (wait until the previous grid has completed and its writes are
+// visible) before its first read of global memory, and pdl_trigger() to let
+// the next kernel start.  Completion stays transitive: a kernel completes only
+// after its own wait returned.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace lucetree

@@ -18,6 +18,8 @@ namespace {
 // needs its parent's mask) with shuffles instead of dependent global loads.
 __global__ void __launch_bounds__(128) build_anc_kernel(const int32_t* __restrict__ parent, int B, int N,
                                                         uint64_t* __restrict__ anc, uint32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (b >= B) return;
@@ -58,6 +60,8 @@ __global__ void __launch_bounds__(128) accept_kernel(const int32_t* __restrict__
                                                      const int32_t* __restrict__ argmax, int B, int N, int vocab,
                                                      int32_t* __restrict__ acc_nodes, int32_t* __restrict__ acc_len,
                                                      int32_t* __restrict__ bonus, uint32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (b >= B) return;
@@ -127,6 +131,8 @@ __global__ void __launch_bounds__(128) accept_kernel(const int32_t* __restrict__
 // V rows (all KV heads); the length update happens after the block has read
 // ctx_len_in, so ctx_len_out may alias it.
 __global__ void __launch_bounds__(256) commit_kernel(lucetree_commit_args c, int elem_bytes) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const int L = c.ctx_len_in[b];
     const int a = c.acc_len[b];
@@ -183,21 +189,18 @@ __global__ void __launch_bounds__(256) commit_kernel(lucetree_commit_args c, int
 
 cudaError_t launch_build_anc(const int32_t* parent, int B, int N, uint64_t* anc, uint32_t* status,
                              cudaStream_t stream) {
-    build_anc_kernel<<<(B + 3) / 4, 128, 0, stream>>>(parent, B, N, anc, status);
-    return cudaGetLastError();
+    return launch_pdl(build_anc_kernel, dim3((B + 3) / 4), dim3(128), 0, stream, parent, B, N, anc, status);
 }
 
 cudaError_t launch_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int B, int N,
                           int vocab, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus, uint32_t* status,
                           cudaStream_t stream) {
-    accept_kernel<<<(B + 3) / 4, 128, 0, stream>>>(parent, draft, argmax, B, N, vocab, acc_nodes, acc_len, bonus,
-                                                   status);
-    return cudaGetLastError();
+    return launch_pdl(accept_kernel, dim3((B + 3) / 4), dim3(128), 0, stream, parent, draft, argmax, B, N, vocab,
+                      acc_nodes, acc_len, bonus, status);
 }
 
 cudaError_t launch_commit(const lucetree_commit_args& c, cudaStream_t stream) {
-    commit_kernel<<<c.B, 256, 0, stream>>>(c, 2);
-    return cudaGetLastError();
+    return launch_pdl(commit_kernel, dim3(c.B), dim3(256), 0, stream, c, 2);
 }
 
 }  // namespace lucetree
