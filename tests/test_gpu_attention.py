@@ -67,6 +67,14 @@ def test_long_128k_b40_sampled(cuda_dev):
 
 
 @pytest.mark.slow
+def test_headline_128k_b22_sampled(cuda_dev):
+    # the workload bench.py times: one sequence, 131072 committed tokens on
+    # permuted pages, budget 22 (one row group of 132 rows per KV head)
+    cfg = W.HEADLINE_128K_B22
+    _check(cfg, cached_inputs(cfg), rows=W.sample_rows(cfg, 48))
+
+
+@pytest.mark.slow
 def test_paged_256k_sampled(cuda_dev):
     cfg = W.PAGED_256K
     _check(cfg, cached_inputs(cfg), rows=W.sample_rows(cfg, 32))
