@@ -194,6 +194,25 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Column maxima of a warp's 16 x 32 values (v[k] = column k in this lane):
+// recursive halving over the lane bits 16, 8, 4, 2 (a lane keeps the upper or
+// lower half of its columns by that bit and takes the maximum with its
+// partner's copy of the same half), then one exchange over bit 1.  Lanes 2c
+// and 2c+1 return the maximum of column c over all 32 lanes.
+__device__ __forceinline__ float col_max16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int m = 16, n = 8; m >= 2; m >>= 1, n >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float send = upper ? v[i] : v[i + n];
+            const float keep = upper ? v[i + n] : v[i];
+            v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, m));
+        }
+    }
+    return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     if constexpr (BF16) {
@@ -496,11 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One streaming pass over my chunks of S^T: P = 2^(s*scale*log2e - m)
         // with the current shifts; lpart += P (sign +1) or -= P (sign -1, the
         // exact undo of a pass made with the same shifts); optionally stores
-        // P^T (hi and, for bf16, lo) and tracks the largest exponent.
-        // kCheck = false: every key lane of the warp is valid and every column
-        // of its chunks is a real row, so no per-element masking is needed.
-        auto exp_pass = [&](const bool kCheck, float (&lpart)[kNa * 16], bool valid, float sign, bool write_p,
-                            float& ex) {
+        // P^T (hi and, for bf16, lo) and tracks the largest exponent.  Invalid
+        // keys and padding columns give P = 0.  (A separate unmasked copy of
+        // this pass for interior tiles measured slower: the extra code costs
+        // more in instruction fetch than the selects it saves.)
+        auto exp_pass = [&](float (&lpart)[kNa * 16], bool valid, float sign, bool write_p, float& ex) {
             // 8-column blocks b = 2*cc + hb; the TMEM load of block b+1 is in
             // flight while block b is computed
             constexpr int kBlocks = 2 * kNa;
@@ -525,14 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const float x = fmaf(__uint_as_float(r[k]), sl2, -mv[k]);
-                    if (kCheck) {
-                        const bool ok = 8 * hb + k < lim;
-                        if (ok) ex = fmaxf(ex, x);
-                        pv[k] = ok ? ex2(x) : 0.f;
-                    } else {
-                        ex = fmaxf(ex, x);
-                        pv[k] = ex2(x);
-                    }
+                    const bool ok = 8 * hb + k < lim;
+                    if (ok) ex = fmaxf(ex, x);
+                    pv[k] = ok ? ex2(x) : 0.f;
                     float& acc = lpart[cc * 16 + 8 * hb + k];
                     acc = fmaf(sign, pv[k], acc);
                 }
@@ -602,10 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // pass 2: exact column maxima move the shifts, then P^T and sums again
                 // The first tile of a range has no shifts yet and starts at pass 2.
                 float ex = -INFINITY;
-                const bool unmasked = __all_sync(0xffffffffu, valid) && R_seg >= 16 * ce;
                 if (!bad && !first) {
-                    if (unmasked) exp_pass(false, lpart, valid, 1.f, true, ex);
-                    else exp_pass(true, lpart, valid, 1.f, true, ex);
+                    exp_pass(lpart, valid, 1.f, true, ex);
                 }
                 // one barrier decides the path; a second one only when it says
                 // "slow", to tell a timeout (somewhere) from a shift update
@@ -616,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 if (slow) {
-                    if (!first) exp_pass(true, lpart, valid, -1.f, false, ex);  // pass 1
+                    if (!first) exp_pass(lpart, valid, -1.f, false, ex);  // pass 1
                     // pass 2: exact column maxima of this tile, then move the shifts
 #pragma unroll 1
                     for (int cc = 0; cc < nch; ++cc) {
@@ -625,11 +637,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld16(tl + 16 * c, r);
                         tmem_wait_ld_regs16(r);
                         const int lim = valid ? R_seg - 16 * c : 0;
+                        float v[16];
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const float v = warp_max(k < lim ? __uint_as_float(r[k]) * sl2 : -INFINITY);
-                            if (lane == 0) ms->col_red[quarter][16 * c + k] = v;
-                        }
+                        for (int k = 0; k < 16; ++k) v[k] = k < lim ? __uint_as_float(r[k]) * sl2 : -INFINITY;
+                        // maxima of the 16 columns over the warp's 32 key lanes
+                        const float cm = col_max16(v, lane);
+                        if ((lane & 1) == 0) ms->col_red[quarter][16 * c + (lane >> 1)] = cm;
                     }
                     bar_sync(1, kSoftmaxThreads);
                     for (int col = st; col < RGP; col += kSoftmaxThreads) {
@@ -672,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tmem_wait_st();
                     }
-                    exp_pass(true, lpart, valid, 1.f, true, ex);
+                    exp_pass(lpart, valid, 1.f, true, ex);
                 }
                 // S^T is no longer read: the next tile's QK may overwrite it
                 tc_fence_before();
