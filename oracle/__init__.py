@@ -52,6 +52,8 @@ def _load():
         lib.oracle_ancestor_matrix.argtypes = [P, i32, P]
         lib.oracle_ancestor_matrix.restype = None
         lib.oracle_upcast.argtypes = [i32, ctypes.c_uint16]
+        lib.oracle_lmhead_argmax.argtypes = [i32, i64, i64, i64, P, P, P, P, P, i32]
+        lib.oracle_lmhead_argmax.restype = i32
         lib.oracle_upcast.restype = f64
         _lib = lib
     return _lib
@@ -161,3 +163,22 @@ def commit(inp: dict, acc_nodes, acc_len, inplace: bool = False):
     if rc != 0:
         raise ValueError("commit touched a page outside the pool")
     return k_pool, v_pool, ctx
+
+
+def lmhead_argmax(hidden_bits, weight_bits, dtype: int, threads: int | None = None):
+    """argmax_v of sum_d hidden[r][d] * weight[v][d] in fp64 (lowest index on
+    ties), with each row's largest and second-largest logit.  hidden_bits
+    [rows][d_model] and weight_bits [vocab][d_model] are uint16 storage bits."""
+    h = _c(hidden_bits, np.uint16)
+    w = _c(weight_bits, np.uint16)
+    rows, d_model = h.shape
+    vocab = w.shape[0]
+    assert w.shape[1] == d_model
+    out = np.empty(rows, np.int32)
+    top1 = np.empty(rows, np.float64)
+    top2 = np.empty(rows, np.float64)
+    nt = threads or os.cpu_count() or 1
+    rc = _load().oracle_lmhead_argmax(dtype, rows, d_model, vocab, _p(h), _p(w), _p(out), _p(top1), _p(top2), nt)
+    if rc != 0:
+        raise RuntimeError("oracle_lmhead_argmax failed")
+    return out, top1, top2

@@ -324,3 +324,130 @@ int oracle_commit(int B, int N, int Hkv, int D, int page_size, const uint16_t* k
     }
     return 0;
 }
+
+/* ---- lm_head projection fused with the argmax ---------------------------------
+ *
+ * The target projects hidden states through its lm_head ("Lucebox Hub", section
+ * "Speculative decoding layer", the third DFlashTarget duty); the verify step
+ * needs only the argmax of each row's logits.  Definition, on the exactly
+ * upcast 16-bit inputs:
+ *     logit[r][v] = sum_d hidden[r][d] * weight[v][d]      (fp64)
+ *     out[r]      = the lowest v with the largest logit[r][v]
+ * top1[r] / top2[r] receive the largest and second-largest logit of row r (the
+ * second over the other vocabulary entries), so a caller can tell a clear winner
+ * from a near tie that another summation order could decide differently.
+ * The vocabulary is split over num_threads threads; each keeps, per row, its
+ * slice's best (value, lowest index) and two largest values, merged in slice
+ * order.  Returns 0, or -1 on bad sizes / allocation failure.
+ */
+typedef struct {
+    int dtype;
+    long rows, d_model, v0, v1;
+    const uint16_t* hidden;
+    const uint16_t* weight;
+    const double* hid;   /* upcast hidden [rows][d_model] */
+    double* best;        /* [rows] */
+    long* idx;           /* [rows] */
+    double* second;      /* [rows] */
+} lm_job;
+
+static void* lm_worker(void* arg) {
+    lm_job* j = (lm_job*)arg;
+    double* w = (double*)malloc(sizeof(double) * (size_t)j->d_model);
+    if (!w) return (void*)1;
+    for (long r = 0; r < j->rows; ++r) {
+        j->best[r] = -INFINITY;
+        j->second[r] = -INFINITY;
+        j->idx[r] = -1;
+    }
+    for (long v = j->v0; v < j->v1; ++v) {
+        const uint16_t* wr = j->weight + (size_t)v * (size_t)j->d_model;
+        for (long d = 0; d < j->d_model; ++d) w[d] = oracle_upcast(j->dtype, wr[d]);
+        for (long r = 0; r < j->rows; ++r) {
+            const double* h = j->hid + (size_t)r * (size_t)j->d_model;
+            double s = 0.0;
+            for (long d = 0; d < j->d_model; ++d) s += h[d] * w[d];
+            if (s > j->best[r]) {
+                j->second[r] = j->best[r];
+                j->best[r] = s;
+                j->idx[r] = v;
+            } else if (s > j->second[r]) {
+                j->second[r] = s;
+            }
+        }
+    }
+    free(w);
+    return NULL;
+}
+
+int oracle_lmhead_argmax(int dtype, long rows, long d_model, long vocab, const uint16_t* hidden,
+                         const uint16_t* weight, int32_t* out, double* top1, double* top2, int num_threads) {
+    if (rows <= 0 || d_model <= 0 || vocab <= 0) return -1;
+    if (num_threads < 1) num_threads = 1;
+    if (num_threads > vocab) num_threads = (int)vocab;
+    double* hid = (double*)malloc(sizeof(double) * (size_t)rows * (size_t)d_model);
+    lm_job* jobs = (lm_job*)calloc((size_t)num_threads, sizeof(lm_job));
+    pthread_t* th = (pthread_t*)calloc((size_t)num_threads, sizeof(pthread_t));
+    double* best = (double*)malloc(sizeof(double) * (size_t)rows * (size_t)num_threads);
+    double* second = (double*)malloc(sizeof(double) * (size_t)rows * (size_t)num_threads);
+    long* idx = (long*)malloc(sizeof(long) * (size_t)rows * (size_t)num_threads);
+    int err = (!hid || !jobs || !th || !best || !second || !idx) ? -1 : 0;
+    if (!err) {
+        for (long i = 0; i < rows * d_model; ++i) hid[i] = oracle_upcast(dtype, hidden[i]);
+        for (int t = 0; t < num_threads; ++t) {
+            lm_job* j = &jobs[t];
+            j->dtype = dtype;
+            j->rows = rows;
+            j->d_model = d_model;
+            j->v0 = vocab * t / num_threads;
+            j->v1 = vocab * (t + 1) / num_threads;
+            j->hidden = hidden;
+            j->weight = weight;
+            j->hid = hid;
+            j->best = best + (size_t)t * (size_t)rows;
+            j->idx = idx + (size_t)t * (size_t)rows;
+            j->second = second + (size_t)t * (size_t)rows;
+            if (pthread_create(&th[t], NULL, lm_worker, j) != 0) {
+                err = -1;
+                num_threads = t;
+                break;
+            }
+        }
+        for (int t = 0; t < num_threads; ++t) {
+            void* rv = NULL;
+            pthread_join(th[t], &rv);
+            if (rv) err = -1;
+        }
+    }
+    if (!err) {
+        /* merge the slices in vocabulary order: a later slice wins only if strictly greater */
+        for (long r = 0; r < rows; ++r) {
+            double b = -INFINITY, s2 = -INFINITY;
+            long bi = -1;
+            for (int t = 0; t < num_threads; ++t) {
+                const double tb = best[(size_t)t * (size_t)rows + r];
+                const double ts = second[(size_t)t * (size_t)rows + r];
+                const long ti = idx[(size_t)t * (size_t)rows + r];
+                if (ti < 0) continue;
+                if (tb > b) {
+                    s2 = b > ts ? b : ts;
+                    b = tb;
+                    bi = ti;
+                } else {
+                    const double c = tb > ts ? tb : ts;
+                    if (c > s2) s2 = c;
+                }
+            }
+            out[r] = (int32_t)bi;
+            if (top1) top1[r] = b;
+            if (top2) top2[r] = s2;
+        }
+    }
+    free(hid);
+    free(jobs);
+    free(th);
+    free(best);
+    free(second);
+    free(idx);
+    return err;
+}

@@ -367,3 +367,59 @@ def test_commit_then_verify_equals_extended_prefix():
         got = kp[pages, :, pos % 64, :]
         want = inp["k_tree"][b, acc[b, :len(pos)]]
         assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------- lm_head + argmax
+
+def _bits_to_f64(bits, dtype):
+    """Independent upcast through numpy's own float formats."""
+    bits = np.asarray(bits, np.uint16)
+    if dtype == oracle.BF16:
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return bits.view(np.float16).astype(np.float64)
+
+
+def test_lmhead_hand_example_ties_across_slices():
+    # hidden [1,0] / [0,1]; weight rows [1,0] [2,0] [0,3] [2,0] (bf16 bits)
+    h = np.array([[0x3F80, 0x0000], [0x0000, 0x3F80]], np.uint16)
+    w = np.array([[0x3F80, 0], [0x4000, 0], [0, 0x4040], [0x4000, 0]], np.uint16)
+    for threads in (1, 2, 3, 4):
+        idx, top1, top2 = oracle.lmhead_argmax(h, w, oracle.BF16, threads=threads)
+        # row 0: logits [1, 2, 0, 2] -> the tie between 1 and 3 goes to 1; second best is the tied 2
+        # row 1: logits [0, 0, 3, 0]
+        assert idx.tolist() == [1, 2]
+        assert top1.tolist() == [2.0, 3.0]
+        assert top2.tolist() == [2.0, 0.0]
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.F16])
+def test_lmhead_matches_numpy_matmul_argmax(dtype):
+    rng = np.random.default_rng(5)
+    rows, d_model, vocab = 9, 96, 1500
+    hf = rng.standard_normal((rows, d_model)).astype(np.float32)
+    wf = (0.05 * rng.standard_normal((vocab, d_model))).astype(np.float32)
+    if dtype == oracle.BF16:
+        hb, wb = W.f32_to_bf16_bits(hf), W.f32_to_bf16_bits(wf)
+    else:
+        hb, wb = W.f32_to_f16_bits(hf), W.f32_to_f16_bits(wf)
+    # a planted exact tie: row 2's best entry duplicated at a higher index
+    logits0 = _bits_to_f64(hb, dtype) @ _bits_to_f64(wb, dtype).T
+    best = int(np.argmax(logits0[2]))
+    wb[vocab - 1] = wb[best]
+    logits = _bits_to_f64(hb, dtype) @ _bits_to_f64(wb, dtype).T
+    idx, top1, top2 = oracle.lmhead_argmax(hb, wb, dtype, threads=5)
+    assert idx.tolist() == np.argmax(logits, axis=1).tolist()
+    srt = np.sort(logits, axis=1)
+    assert np.allclose(top1, srt[:, -1], rtol=1e-12, atol=1e-12)
+    assert np.allclose(top2, srt[:, -2], rtol=1e-12, atol=1e-12)
+    assert top1[2] == top2[2]  # the planted tie
+
+
+def test_lmhead_thread_count_does_not_change_the_result():
+    rng = np.random.default_rng(6)
+    hb = W.f32_to_bf16_bits(rng.standard_normal((5, 64)).astype(np.float32))
+    wb = W.f32_to_bf16_bits(rng.standard_normal((777, 64)).astype(np.float32))
+    ref = oracle.lmhead_argmax(hb, wb, oracle.BF16, threads=1)
+    for t in (2, 7, 64):
+        got = oracle.lmhead_argmax(hb, wb, oracle.BF16, threads=t)
+        assert all(np.array_equal(a, b) for a, b in zip(ref, got))

@@ -284,3 +284,43 @@ def sample_rows(cfg: VerifyConfig, count: int, seed: int = 1) -> np.ndarray:
     pick = set(rng.choice(total, size=max(0, count - 2), replace=False).tolist())
     pick.update({0, total - 1})
     return np.array(sorted(pick), dtype=np.int32)
+
+
+# ---------------------------------------------------------------- lm_head + argmax
+
+@dataclasses.dataclass(frozen=True)
+class LmHeadConfig:
+    """The projection of the verify rows' hidden states through the target's
+    lm_head, reduced to each row's argmax.  rows = B * (N + 1) (the root and
+    every tree node); the pages give no hidden size, d_model = 5120 is this
+    build's reading for a 27B-class target."""
+    name: str
+    rows: int
+    d_model: int
+    vocab: int
+    dtype: str = BF16
+    w_std: float = 0.02
+
+    def weight_bytes(self) -> int:
+        return self.vocab * self.d_model * 2
+
+
+LMHEAD_TINY = LmHeadConfig("lmhead-tiny", rows=9, d_model=256, vocab=4096, dtype=F16)
+LMHEAD_27B_B22 = LmHeadConfig("lmhead-27b-b22", rows=23, d_model=5120, vocab=151936)
+LMHEAD_27B_B40 = LmHeadConfig("lmhead-27b-b40", rows=41, d_model=5120, vocab=151936)
+LMHEAD_CONFIGS = {c.name: c for c in (LMHEAD_TINY, LMHEAD_27B_B22, LMHEAD_27B_B40)}
+
+
+def generate_lmhead(cfg: LmHeadConfig, seed: int = 0) -> dict:
+    """hidden [rows][d_model] ~ N(0, 1) and weight [vocab][d_model] ~ N(0, w_std^2),
+    both rounded to the dtype (16-bit storage bits)."""
+    rng = np.random.default_rng(seed * 7919 + _name_key(cfg.name))
+    hidden = _normal_bits(rng, (cfg.rows, cfg.d_model), cfg.dtype)
+    total = cfg.vocab * cfg.d_model
+    out = np.empty(total, dtype=np.uint16)
+    conv = f32_to_bf16_bits if cfg.dtype == BF16 else f32_to_f16_bits
+    chunk = 1 << 24
+    for s in range(0, total, chunk):
+        e = min(total, s + chunk)
+        out[s:e] = conv(np.float32(cfg.w_std) * rng.standard_normal(e - s, dtype=np.float32))
+    return dict(hidden=hidden, weight=out.reshape(cfg.vocab, cfg.d_model))
