@@ -398,9 +398,79 @@ def run_ours(args, cfg):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, cfg, acc_total)
+    if not args.no_lmhead:
+        # the lm_head row is measured apart from the step: the step takes the
+        # generator's logits, this call produces the argmax from hidden states
+        line["lmhead_argmax"] = measure_lmhead(args, dev, stream, rank, with_cpu=world == 1 and not args.no_cpu_baseline)
     print(json.dumps(line), flush=True)
     if dist.is_initialized():
         dist.destroy_process_group()
+    return 0
+
+
+def measure_lmhead(args, dev, stream, rank, with_cpu=True):
+    """The fused lm_head projection + argmax on the 27B-class workload (23 verify
+    rows, d_model 5120, vocabulary 151936, bf16): each call streams the
+    1.56 GB weight once, so it is timed alone with CUDA events on its stream
+    (the weight is larger than L2; nothing to flush).  Inputs are seeded
+    normals drawn on the device; parity is the tests' business."""
+    import torch
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    lc = W.LMHEAD_27B_B22
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242 + rank)
+    hidden = torch.randn(lc.rows, lc.d_model, device=dev, generator=g).to(torch.bfloat16)
+    weight = torch.empty(lc.vocab, lc.d_model, dtype=torch.bfloat16, device=dev)
+    for v0 in range(0, lc.vocab, 16384):
+        v1 = min(lc.vocab, v0 + 16384)
+        weight[v0:v1] = (torch.randn(v1 - v0, lc.d_model, device=dev, generator=g) * lc.w_std).to(torch.bfloat16)
+    out = torch.empty(lc.rows, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(LT.lucetree_lmhead_argmax_workspace(lc.rows), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        LT.lucetree_lmhead_argmax(hidden, weight, out, st, ws, stream=stream)
+    n = max(10, min(100, args.steps // 20))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize(dev)
+    for k in range(n):
+        evs[k][0].record(stream)
+        LT.lucetree_lmhead_argmax(hidden, weight, out, st, ws, stream=stream)
+        evs[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    nbytes = lc.weight_bytes() + lc.rows * lc.d_model * 2 + lc.rows * 4
+    peak, peak_kind = peak_hbm()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    res = {
+        "workload": f"{lc.name}: rows {lc.rows}, d_model {lc.d_model}, vocab {lc.vocab}, bf16",
+        "ms_per_call": ms, "calls_timed": n, "device_status": int(st.item()),
+        "tflops": 2.0 * lc.rows * lc.d_model * lc.vocab / (ms * 1e-3) / 1e12,
+        "roofline": {"bound": "hbm", "kernel": "lucetree_lmhead_argmax", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": nbytes},
+    }
+    if with_cpu:
+        import oracle
+        threads = os.cpu_count() or 1
+        hb = hidden.view(torch.int16).cpu().numpy().view(np.uint16)
+        wb = weight.view(torch.int16).cpu().numpy().view(np.uint16)
+        sample = 2
+        t0 = time.perf_counter()
+        oracle.lmhead_argmax(hb[:sample], wb, oracle.BF16, threads=threads)
+        cpu_ms = (time.perf_counter() - t0) * 1e3 * lc.rows / sample
+        res["cpu_baseline"] = {"ms_per_call": cpu_ms, "cores": threads, "kind": "oracle",
+                               "sample": f"{sample} of {lc.rows} rows over the full vocabulary, scaled to {lc.rows}"}
+    return res
+
+
+def run_lmhead_only(args):
+    import torch
+    from speculative_decoding_tree_ddtree_gb300.build import build
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    print(json.dumps({"lmhead_argmax": measure_lmhead(args, dev, stream, 0, with_cpu=False)}), flush=True)
     return 0
 
 
@@ -412,7 +482,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default=W.HEADLINE_128K_B22.name, choices=sorted(W.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-lmhead", action="store_true", help="skip the fused lm_head + argmax measurement")
+    ap.add_argument("--lmhead-only", action="store_true", help="time only the fused lm_head + argmax")
     args = ap.parse_args(argv)
+    if args.lmhead_only:
+        return run_lmhead_only(args)
     cfg = W.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)

@@ -19,7 +19,9 @@
  *   lucetree_accept       longest matching root path, greedy
  *   lucetree_commit       copy accepted K/V into the pool, advance lengths
  * plus lucetree_build_anc_mask, which turns a parent array into the ancestor
- * bitmasks verify_attn consumes.
+ * bitmasks verify_attn consumes, and lucetree_lmhead_argmax, which replaces
+ * the logits + lucetree_argmax pair by the lm_head projection with a fused
+ * argmax.
  *
  * Conventions for every call:
  *   - All array pointers are DEVICE pointers unless a parameter says "host".
@@ -214,6 +216,39 @@ typedef struct lucetree_commit_args {
  * [0, N)), BAD_PAGE, BAD_CTX; copying stops at the first bad entry.
  */
 LUCETREE_API lucetree_status lucetree_commit(const lucetree_commit_args* args, void* stream);
+
+/* Arguments of lucetree_lmhead_argmax. */
+typedef struct lucetree_lmhead_args {
+    int dtype;             /* LUCETREE_F16 / LUCETREE_BF16, both operands */
+    int rows;              /* R = B * (N + 1) verify rows (root + nodes), 1..256 */
+    int d_model;           /* hidden size, a positive multiple of 64 */
+    int vocab;             /* >= 1 */
+    const void* hidden;    /* [rows][d_model], 16-byte aligned */
+    const void* weight;    /* [vocab][d_model] lm_head weight, 16-byte aligned */
+    int32_t* out_idx;      /* [rows] */
+    float* out_logit;      /* [rows] the maximal logit (fp32 accumulation), or NULL */
+    uint32_t* status;
+} lucetree_lmhead_args;
+
+/* Workspace bytes lucetree_lmhead_argmax needs for `rows` rows (host output). */
+LUCETREE_API lucetree_status lucetree_lmhead_argmax_workspace(int rows, size_t* bytes);
+
+/*
+ * The target's lm_head projection fused with the argmax: out_idx[r] = the
+ * lowest v with sum_d hidden[r][d] * weight[v][d] maximal, without writing
+ * the logits.  The pages list projecting hidden states through the target's
+ * lm_head as one DFlashTarget duty ("Lucebox Hub", section "Speculative
+ * decoding 계층"); the fused form, its layout and its sizes are this
+ * library's.  Accumulation is fp32 on the tensor cores, so rows whose two
+ * best logits lie within that rounding may pick either (a NaN logit is
+ * outside the contract).  The workspace (256-byte aligned, see
+ * lucetree_lmhead_argmax_workspace) is cleared by the call itself.  Host
+ * errors: INVALID_ARG (null or misaligned pointers, sizes out of range),
+ * UNSUPPORTED (rows > 256, d_model not a multiple of 64), WORKSPACE.
+ * Device check: TIMEOUT.
+ */
+LUCETREE_API lucetree_status lucetree_lmhead_argmax(const lucetree_lmhead_args* args, void* workspace,
+                                                    size_t workspace_bytes, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 LUCETREE_API const char* lucetree_status_string(lucetree_status status);

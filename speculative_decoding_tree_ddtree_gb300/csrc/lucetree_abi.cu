@@ -123,6 +123,29 @@ lucetree_status lucetree_argmax(const float* logits, int rows, int vocab, long l
     return LUCETREE_OK;
 }
 
+lucetree_status lucetree_lmhead_argmax_workspace(int rows, size_t* bytes) {
+    if (!bytes || rows <= 0) return LUCETREE_ERR_INVALID_ARG;
+    if (lmhead_padded_rows(rows) < 0) return LUCETREE_ERR_UNSUPPORTED;
+    *bytes = lmhead_workspace_bytes(rows);
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_lmhead_argmax(const lucetree_lmhead_args* a, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+    if (!a) return LUCETREE_ERR_INVALID_ARG;
+    if (a->dtype != LUCETREE_F16 && a->dtype != LUCETREE_BF16) return LUCETREE_ERR_UNSUPPORTED;
+    if (!a->hidden || !a->weight || !a->out_idx || !a->status) return LUCETREE_ERR_INVALID_ARG;
+    if (a->rows <= 0 || a->d_model <= 0 || a->vocab <= 0) return LUCETREE_ERR_INVALID_ARG;
+    if (lmhead_padded_rows(a->rows) < 0 || a->d_model % 64 != 0) return LUCETREE_ERR_UNSUPPORTED;
+    if (!aligned16(a->hidden) || !aligned16(a->weight)) return LUCETREE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < lmhead_workspace_bytes(a->rows) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return LUCETREE_ERR_WORKSPACE;
+    if (launch_lmhead(*a, workspace, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LUCETREE_ERR_CUDA;
+    return LUCETREE_OK;
+}
+
 lucetree_status lucetree_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int B, int N,
                                 int vocab, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus, uint32_t* status,
                                 void* stream) {

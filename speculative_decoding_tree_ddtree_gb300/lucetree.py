@@ -39,6 +39,8 @@ EXPORTED = (
     "lucetree_status_string",
     "lucetree_abi_version",
     "lucetree_verify_attn_noalloc",
+    "lucetree_lmhead_argmax_workspace",
+    "lucetree_lmhead_argmax",
 )
 
 
@@ -69,6 +71,14 @@ class CommitArgs(ctypes.Structure):
     ]
 
 
+class LmHeadArgs(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int), ("rows", ctypes.c_int), ("d_model", ctypes.c_int), ("vocab", ctypes.c_int),
+        ("hidden", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("out_idx", ctypes.c_void_p),
+        ("out_logit", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -93,6 +103,8 @@ def load(path: str | None = None):
     lib.lucetree_status_string.restype = ctypes.c_char_p
     lib.lucetree_abi_version.argtypes = []
     lib.lucetree_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnArgs), P]
+    lib.lucetree_lmhead_argmax_workspace.argtypes = [I, ctypes.POINTER(SZ)]
+    lib.lucetree_lmhead_argmax.argtypes = [ctypes.POINTER(LmHeadArgs), P, SZ, P]
     for name in EXPORTED:
         if name not in ("lucetree_status_string", "lucetree_abi_version"):
             getattr(lib, name).restype = I
@@ -265,3 +277,27 @@ def lucetree_verify_attn_noalloc(q, k_pool, v_pool, page_table, ctx_len, k_tree,
     a.ctx_len, a.k_tree, a.v_tree, a.anc_mask = _ptr(ctx_len), _ptr(k_tree), _ptr(v_tree), _ptr(anc_mask)
     a.out, a.lse, a.status = _ptr(out), _ptr(lse), _ptr(status)
     _check(load().lucetree_verify_attn_noalloc(ctypes.byref(a), _stream(stream)))
+
+
+# ---------------------------------------------------------------- lm_head projection + argmax
+
+def lucetree_lmhead_argmax_workspace(rows: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().lucetree_lmhead_argmax_workspace(rows, ctypes.byref(n)))
+    return int(n.value)
+
+
+def lucetree_lmhead_argmax(hidden, weight, out_idx, status, workspace, out_logit=None, stream=None):
+    """hidden [rows][d_model] and weight [vocab][d_model] (both fp16 or both
+    bf16) -> out_idx int32 [rows]: the lowest vocabulary index of each row's
+    largest logit; optionally out_logit fp32 [rows] (that logit)."""
+    rows, d_model = hidden.shape
+    a = LmHeadArgs()
+    a.dtype = dtype_code(hidden)
+    if dtype_code(weight) != a.dtype:
+        raise LucetreeError("hidden and weight must share a dtype")
+    a.rows, a.d_model, a.vocab = rows, d_model, weight.shape[0]
+    a.hidden, a.weight = _ptr(hidden), _ptr(weight)
+    a.out_idx, a.out_logit, a.status = _ptr(out_idx), _ptr(out_logit), _ptr(status)
+    _check(load().lucetree_lmhead_argmax(ctypes.byref(a), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -55,6 +55,19 @@ def test_host_side_queries_without_gpu(lib):
     assert lt.lucetree_accept(None, None, None, 1, 1, 1, None, None, None, None, None) == 1
     assert lt.lucetree_verify_attn(None, None, 0, None) == 1
     assert lt.lucetree_commit(None, None) == 1
+    # lm_head + argmax: row count and d_model limits, checked on the host
+    assert lt.lucetree_lmhead_argmax_workspace(0, ctypes.byref(n)) == 1
+    assert lt.lucetree_lmhead_argmax_workspace(257, ctypes.byref(n)) == 2
+    assert lt.lucetree_lmhead_argmax_workspace(23, ctypes.byref(n)) == 0 and n.value >= 23 * 8 + 4
+    assert lt.lucetree_lmhead_argmax(None, None, 0, None) == 1
+    fake = 1 << 20  # never dereferenced: every case below fails validation first
+    for rows, d_model, want in ((300, 256, 2), (8, 100, 2), (0, 256, 1)):
+        a = LT.LmHeadArgs(dtype=LT.LUCETREE_BF16, rows=rows, d_model=d_model, vocab=1000,
+                          hidden=fake, weight=fake, out_idx=fake, out_logit=None, status=fake)
+        assert lt.lucetree_lmhead_argmax(ctypes.byref(a), None, 0, None) == want
+    a = LT.LmHeadArgs(dtype=LT.LUCETREE_BF16, rows=8, d_model=256, vocab=1000,
+                      hidden=fake, weight=fake, out_idx=fake, out_logit=None, status=fake)
+    assert lt.lucetree_lmhead_argmax(ctypes.byref(a), None, 0, None) == 3  # no workspace
 
 
 def test_binding_rejects_host_tensors():
