@@ -19,6 +19,7 @@ CPU oracle on the host cores on a bounded row sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -72,26 +73,32 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def prefix_kernel_sha() -> str:
+def kernel_sha(prefix: str = "attn_prefix") -> str:
+    """Hash of one kernel's sources (files starting with `prefix`) and the
+    shared device headers."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_tree_ddtree_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.startswith("attn_prefix") or fn in ("internal.cuh", "tc_ptx.cuh"):
+        if fn.startswith(prefix) or fn in ("internal.cuh", "tc_ptx.cuh"):
             with open(os.path.join(csrc, fn), "rb") as f:
                 h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """dram bytes per launch of the prefix kernel from the committed ncu summary,
-    or None when the kernel source changed since that capture."""
-    p = os.path.join(ROOT, "profiles", "attn_prefix_verify-128k-b22.md")
+def prefix_kernel_sha() -> str:
+    return kernel_sha("attn_prefix")
+
+
+def profiled_traffic(summary: str = "attn_prefix_verify-128k-b22.md", prefix: str = "attn_prefix"):
+    """dram bytes per launch of a kernel from its committed ncu summary, or None
+    when the kernel's sources changed since that capture."""
+    p = os.path.join(ROOT, "profiles", summary)
     try:
         txt = open(p).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s*\(source sha\s*([0-9a-f]+)\)", txt)
-    if not m or m.group(2) != prefix_kernel_sha():
+    if not m or m.group(2) != kernel_sha(prefix):
         return None
     return int(m.group(1))
 
@@ -417,6 +424,8 @@ def measure_lmhead(args, dev, stream, rank, with_cpu=True):
     import torch
     from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
     lc = W.LMHEAD_27B_B22
+    if getattr(args, "lmhead_vocab", None):
+        lc = dataclasses.replace(lc, name=f"{lc.name}-v{args.lmhead_vocab}", vocab=args.lmhead_vocab)
     g = torch.Generator(device=dev)
     g.manual_seed(4242 + rank)
     hidden = torch.randn(lc.rows, lc.d_model, device=dev, generator=g).to(torch.bfloat16)
@@ -446,7 +455,9 @@ def measure_lmhead(args, dev, stream, rank, with_cpu=True):
         "ms_per_call": ms, "calls_timed": n, "device_status": int(st.item()),
         "tflops": 2.0 * lc.rows * lc.d_model * lc.vocab / (ms * 1e-3) / 1e12,
         "roofline": {"bound": "hbm", "kernel": "lucetree_lmhead_argmax", "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": profiled_traffic("lmhead_argmax_lmhead-27b-b22.md", "lmhead")
+                     if lc.vocab == W.LMHEAD_27B_B22.vocab else None,
                      "algorithmic_bytes_per_launch": nbytes},
     }
     if with_cpu:
@@ -484,6 +495,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-lmhead", action="store_true", help="skip the fused lm_head + argmax measurement")
     ap.add_argument("--lmhead-only", action="store_true", help="time only the fused lm_head + argmax")
+    ap.add_argument("--lmhead-vocab", type=int, default=None,
+                    help="with --lmhead-only: a smaller vocabulary (profiler captures)")
     args = ap.parse_args(argv)
     if args.lmhead_only:
         return run_lmhead_only(args)

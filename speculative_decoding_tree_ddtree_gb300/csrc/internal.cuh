@@ -196,9 +196,6 @@ cudaError_t launch_argmax(const float* logits, int rows, int vocab, long long ro
                           void* ws, int device, cudaStream_t stream);
 
 int device_sm_count(int device);
-int lmhead_padded_rows(int rows);     // -1 when rows exceeds the largest instantiation
-size_t lmhead_workspace_bytes(int rows);
-cudaError_t launch_lmhead(const lucetree_lmhead_args& a, void* ws, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every library kernel is launched so that it

@@ -3,6 +3,7 @@
 #include <cuda.h>
 
 #include "lmhead_tc.cuh"
+#include "lmhead.h"
 
 namespace lucetree {
 

@@ -3,6 +3,7 @@
 #include <cstring>
 
 #include "internal.cuh"
+#include "lmhead.h"
 
 namespace lucetree {
 
