@@ -76,6 +76,8 @@ typedef enum lucetree_dtype {
 #define LUCETREE_DEV_BAD_TOKEN 0x8u  /* draft token outside [0, vocab) */
 #define LUCETREE_DEV_BAD_NODE 0x10u  /* accepted node id / count out of range, or a mask without self */
 #define LUCETREE_DEV_TIMEOUT 0x20u   /* a bounded wait inside a kernel gave up */
+#define LUCETREE_DEV_NONFINITE 0x40u /* an attention output is inf or NaN: non-finite inputs, or a bf16 V value
+                                        of magnitude >= 65536 (beyond the fp16 range of the on-chip PV product) */
 
 #define LUCETREE_PAGE_SIZE 64 /* tokens per KV page */
 #define LUCETREE_MAX_NODES 64 /* tree budget limit (one 64-bit ancestor mask per node) */

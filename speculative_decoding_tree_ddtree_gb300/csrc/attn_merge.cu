@@ -183,7 +183,9 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(AttnLaunch L) {
         float v = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) v += s_o[w][d];
-        orow[d] = v * inv;
+        v *= inv;
+        orow[d] = v;
+        if (!isfinite(v)) atomicOr(a.status, LUCETREE_DEV_NONFINITE);
     }
     if (a.lse && threadIdx.x == 0) a.lse[row] = (mmax + log2f(l)) * kLn2;
 }

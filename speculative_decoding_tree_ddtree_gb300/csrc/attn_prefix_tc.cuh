@@ -13,12 +13,15 @@
 // kernel on the SM side.
 //
 // TMEM (512 columns): S^T at columns [0, R), then O^T for d 0..127 and d
-// 128..255.  With bf16 operands P is split into hi and lo parts (below); when
-// TMEM and the MMA's N <= 256 allow it (R <= 96), P_hi^T and P_lo^T sit side
-// by side as one B operand so a single MMA of N = 2R reads V once and writes
-// both products into adjacent column ranges that the epilogue adds; for
-// larger R the two products are separate MMAs into one accumulator.  TMEM
-// lane l holds key l of S^T and output dim l (+128) of O^T.
+// 128..255.  TMEM lane l holds key l of S^T and output dim l (+128) of O^T.
+//
+// Operand precision.  QK runs on the input type (bf16 or fp16).  PV always
+// runs on fp16: P^T is written as fp16 (11 significant bits, enough for the
+// 2e-3 bar; bf16 P with its 8 bits is not), and bf16 V chunks are converted
+// to fp16 in shared memory once they land, which is exact for every bf16
+// value of magnitude below 65536 (the fp16 range; a larger one becomes inf
+// and the merge flags the row's non-finite output).  An MMA's A and B then
+// always share one type.
 //
 // Software pipeline.  The MMA warp issues QK(t+1) as soon as the softmax has
 // released S^T(t) (after its exponent vote), before PV(t); so the scores of
@@ -39,14 +42,17 @@
 //
 // Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2..3 idle (they
 // complete warpgroup 0, which hands most of its registers to the others),
-// 4..15 = softmax and epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and
+// 4..15 = softmax, V conversion and epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and
 // handles one third of the row tile's column chunks.  K and V stream through
-// a ring of 16 KB chunk slots ([128 keys][64 d], 128-byte swizzle), two TMA
-// boxes (one per 64-token page) per slot; an operand (one tile's K or V) is
-// D/64 consecutive chunks, and V chunk pairs always land in slots (2j, 2j+1)
-// so one MN-major descriptor covers 128 output dims.  Every wait is bounded; a
-// timeout sets LUCETREE_DEV_TIMEOUT, drains this CTA's own copies and MMAs
-// and returns.
+// a ring of 16 KB chunk slots, two TMA boxes of [64 keys][64 d] (128-byte
+// swizzle) per slot; an operand (one tile's K or V) is D/64 consecutive
+// chunks.  A K chunk is [128 keys][64 d] (one box per 64-token page: the
+// K-major A operand of QK for one 64-dim slice); a V chunk is [64 keys][128 d]
+// (one page, two adjacent 64-dim boxes: the MN-major A operand of PV for 128
+// output dims and 64 keys, the second box at a fixed 8 KB offset), so every
+// chunk is self-contained and the ring may have any number of slots.  Every
+// wait is bounded; a timeout sets LUCETREE_DEV_TIMEOUT, drains this CTA's own
+// copies and MMAs and returns.
 #pragma once
 
 #include "internal.cuh"
@@ -75,27 +81,19 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxSlots = 12;
 static_assert(3 * kRowsMax <= (int)kTmemCols, "S^T and two O^T halves in TMEM");
 
-// bf16 P keeps 8 significant bits, which alone puts ~1e-3 relative noise on
-// the output; with bf16 operands P is split into hi = bf16(p) and
-// lo = bf16(p - hi) and the PV contraction runs on both (P to ~2^-17).
-// fp16 P (11 bits) needs no split.
-template <int D, int RGP, bool SPLIT>
+template <int D, int RGP>
 struct Layout {
     static constexpr int kChunks = D / 64;
     static constexpr int kDh = D / 128;                 // O^T halves of 128 output dims
     static constexpr int kNch = RGP / 16;
     static constexpr int kQBytes = kChunks * RGP * 128;
-    static constexpr int kPOneBytes = RGP * 256;
-    static constexpr int kPBytes = kPOneBytes * (SPLIT ? 2 : 1);
-    // hi and lo of P as one B operand (N = 2R) when that fits the MMA and TMEM
-    static constexpr bool kMerge = SPLIT && 2 * RGP <= 256 && RGP + kDh * 2 * RGP <= (int)kTmemCols;
-    static constexpr int kPvN = kMerge ? 2 * RGP : RGP;  // N of the PV MMA
-    static constexpr uint32_t kColO0 = RGP;              // O^T, d 0..127
-    static constexpr uint32_t kColO1 = RGP + kPvN;       // O^T, d 128..255
-    static_assert(RGP + kDh * kPvN <= (int)kTmemCols, "TMEM columns");
+    static constexpr int kPBytes = RGP * 256;           // P^T [128 keys][RGP] fp16
+    static constexpr uint32_t kColO0 = RGP;             // O^T, d 0..127
+    static constexpr uint32_t kColO1 = 2 * RGP;         // O^T, d 128..255
+    static_assert(RGP + kDh * RGP <= (int)kTmemCols, "TMEM columns");
     static constexpr int kMiscBytes = 4096;
     static constexpr int kRaw = (kSmemLimit - 1024 - kQBytes - kPBytes - kMiscBytes) / kChunkBytes;
-    static constexpr int kNS = (kRaw > kMaxSlots ? kMaxSlots : kRaw) & ~1;
+    static constexpr int kNS = kRaw > kMaxSlots ? kMaxSlots : kRaw;
     static constexpr int kQOff = 0;
     static constexpr int kPOff = kQBytes;
     static constexpr int kSlotOff = ((kPOff + kPBytes + 1023) / 1024) * 1024;
@@ -113,6 +111,13 @@ struct Misc {
     alignas(16) float col_red[4][kRowsMax];
     uint64_t full[kMaxSlots];
     uint64_t empty[kMaxSlots];
+    // V chunks have their own barriers, indexed by V chunk number n (in V
+    // order) modulo kMaxSlots >= kNS: vfull[n % kMaxSlots] = landed,
+    // vready[n % kMaxSlots] = converted by the softmax warps.  full[slot] still
+    // completes one phase per fill (a plain arrive for V fills), so the K
+    // waits' parities keep counting fills.
+    uint64_t vfull[kMaxSlots];
+    uint64_t vready[kMaxSlots];
     uint64_t s_full, s_free, q_full, q_empty, p_full, pv_done, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -199,7 +204,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 // lower half of its columns by that bit and takes the maximum with its
 // partner's copy of the same half), then one exchange over bit 1.  Lanes 2c
 // and 2c+1 return the maximum of column c over all 32 lanes.
-__device__ __forceinline__ float col_max16(float (&v)[16], int lane) {
+// (col_sum16: the same pattern with additions.)
+template <bool kSum>
+__device__ __forceinline__ float col_reduce16(float (&v)[16], int lane) {
 #pragma unroll
     for (int m = 16, n = 8; m >= 2; m >>= 1, n >>= 1) {
         const bool upper = (lane & m) != 0;
@@ -207,21 +214,25 @@ __device__ __forceinline__ float col_max16(float (&v)[16], int lane) {
         for (int i = 0; i < n; ++i) {
             const float send = upper ? v[i] : v[i + n];
             const float keep = upper ? v[i + n] : v[i];
-            v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, m));
+            const float got = __shfl_xor_sync(0xffffffffu, send, m);
+            v[i] = kSum ? keep + got : fmaxf(keep, got);
         }
     }
-    return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return kSum ? v[0] + got : fmaxf(v[0], got);
+}
+__device__ __forceinline__ float col_max16(float (&v)[16], int lane) { return col_reduce16<false>(v, lane); }
+__device__ __forceinline__ float col_sum16(float (&v)[16], int lane) { return col_reduce16<true>(v, lane); }
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    if constexpr (BF16) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&v);
-    } else {
-        __half2 v = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
+// Two bf16 (one 32-bit word) -> two fp16 (round to nearest), exact for
+// magnitudes below 65536; larger magnitudes become inf.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return pack_half2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ void set_abort(Misc* ms, uint32_t* status) {
@@ -233,7 +244,7 @@ template <int D, bool BF16, int RGP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const AttnLaunch L) {
-    using Lay = Layout<D, RGP, BF16>;
+    using Lay = Layout<D, RGP>;
     constexpr int kChunks = Lay::kChunks;
     constexpr int kNch = Lay::kNch;
     constexpr int kNa = (kNch + kSmGroups - 1) / kSmGroups;  // column chunks per softmax warp (at most)
@@ -270,6 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNS; ++i) {
             mbar_init(&ms->full[i], 1);
             mbar_init(&ms->empty[i], 1);
+        }
+        for (int i = 0; i < kMaxSlots; ++i) {
+            mbar_init(&ms->vfull[i], 1);
+            mbar_init(&ms->vready[i], kSmWarps);
         }
         mbar_init(&ms->s_full, 1);
         mbar_init(&ms->s_free, kSmWarps);
@@ -310,23 +325,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================================================ TMA producer
         const int oob_row = a.num_pages * p.Hkv * kPage;  // first row past the pool: zero fill
         const uint64_t pol_stream = policy_evict_first();  // K/V are read once: do not keep them in L2
-        uint32_t chunk = 0;
+        uint32_t chunk = 0, vchunk = 0;
         int q_loads = 0;
         bool ok = true;
         // one operand (one tile's K or V): kChunks slots of two boxes each
-        auto issue = [&](const CUtensorMap* m, int row0, int row1) -> bool {
+        auto issue = [&](bool is_v, int row0, int row1) -> bool {
             for (int c = 0; c < kChunks; ++c) {
                 const int slot = chunk % kNS;
                 const bool w = mbar_wait(&ms->empty[slot], ((chunk / kNS) & 1) ^ 1);
                 if (!__all_sync(0xffffffffu, w)) return false;  // lanes agree on a timeout
                 if (lane == 0) {
                     uint8_t* dst = sSlots + slot * kChunkBytes;
-                    mbar_arrive_expect_tx(&ms->full[slot], kChunkBytes);
-                    tma_load_2d_hint(dst, m, 64 * c, row0, &ms->full[slot], pol_stream);
-                    tma_load_2d_hint(dst + 8192, m, 64 * c, row1, &ms->full[slot], pol_stream);
+                    uint64_t* bar = &ms->full[slot];
+                    if (is_v) {
+                        mbar_arrive(bar);  // this fill's phase of full[slot]; the data signal is vfull
+                        bar = &ms->vfull[vchunk % kMaxSlots];
+                    }
+                    mbar_arrive_expect_tx(bar, kChunkBytes);
+                    if (is_v) {
+                        // [64 keys of page c & 1][dims 128 * (c >> 1) .. +127]
+                        const int row = (c & 1) ? row1 : row0, x = 128 * (c >> 1);
+                        tma_load_2d_hint(dst, &tm_v, x, row, bar, pol_stream);
+                        tma_load_2d_hint(dst + 8192, &tm_v, x + 64, row, bar, pol_stream);
+                    } else {
+                        // [128 keys: page 0 then page 1][dims 64 * c .. +63]
+                        tma_load_2d_hint(dst, &tm_k, 64 * c, row0, bar, pol_stream);
+                        tma_load_2d_hint(dst + 8192, &tm_k, 64 * c, row1, bar, pol_stream);
+                    }
                 }
                 __syncwarp();
                 ++chunk;
+                vchunk += is_v ? 1u : 0u;
             }
             return true;
         };
@@ -378,20 +407,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int pid = __shfl_sync(0xffffffffu, pid_cur, 2 * (rel & 15) + h);
                 row[h] = pid >= 0 ? (pid * p.Hkv + cur.pc.s % p.Hkv) * kPage : oob_row;
             }
-            if (!(ok = issue(&tm_k, row[0], row[1]))) break;
-            if (have_v && !(ok = issue(&tm_v, v_row0, v_row1))) break;
+            if (!(ok = issue(false, row[0], row[1]))) break;
+            if (have_v && !(ok = issue(true, v_row0, v_row1))) break;
             v_row0 = row[0];
             v_row1 = row[1];
             have_v = true;
             cur.step(p, a.ctx_len);
         }
-        if (ok && have_v) ok = issue(&tm_v, v_row0, v_row1);
+        if (ok && have_v) ok = issue(true, v_row0, v_row1);
         if (!ok || aborted(ms)) {
             set_abort(ms, a.status);
             // wait (bounded) for this CTA's own copies still in flight
             if (lane == 0) {
+                // (full[] covers the K fills, vfull[] the V fills; each wait on a
+                // barrier whose phase already completed returns at once)
                 const uint32_t first = chunk > (uint32_t)kNS ? chunk - kNS : 0u;
                 for (uint32_t c = first; c < chunk; ++c) mbar_wait(&ms->full[c % kNS], (c / kNS) & 1, 200000000ll);
+                const uint32_t vfirst = vchunk > (uint32_t)kNS ? vchunk - kNS : 0u;
+                for (uint32_t c = vfirst; c < vchunk; ++c)
+                    mbar_wait(&ms->vfull[c % kMaxSlots], (c / kMaxSlots) & 1, 200000000ll);
                 if (q_loads > 0) mbar_wait(&ms->q_full, (q_loads - 1) & 1, 200000000ll);
             }
         }
@@ -399,9 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================================================ MMA issuer
         if (lane == 0) {
             const uint32_t id_qk = idesc_f16(128, RGP, kAB, 0, 0);
-            const uint32_t id_pv = idesc_f16(128, Lay::kPvN, kAB, 1, 1);
+            const uint32_t id_pv = idesc_f16(128, RGP, 0u, 1, 1);  // fp16 V and P
             constexpr uint64_t hi_k = desc_hi(16, 1024, kLayoutSwizzle128);
-            constexpr uint64_t hi_v = desc_hi(kChunkBytes, 1024, kLayoutSwizzle128);
+            constexpr uint64_t hi_v = desc_hi(8192, 1024, kLayoutSwizzle128);  // 2nd 64-dim box at +8 KB
             constexpr uint64_t hi_p = desc_hi(128, 2048, kLayoutInterleave);
             const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aS = smem_u32(sSlots);
             uint32_t chunk = 0, jq = 0, j = 0;
@@ -449,31 +483,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait(&ms->p_full, j & 1))) break;
                 tc_fence_after();
                 const bool first = pv.first();
+                // output dims 128h..128h+127: chunk 2h holds keys 0..63, chunk
+                // 2h+1 keys 64..127 (four 16-key steps each)
                 for (int h = 0; h < kChunks / 2 && ok; ++h) {
-                    const int slot = chunk % kNS;  // even; its pair is slot + 1
-                    ok = mbar_wait(&ms->full[slot], (chunk / kNS) & 1) &&
-                         mbar_wait(&ms->full[slot + 1], ((chunk + 1) / kNS) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
                     const uint32_t dO = tmem + (h ? Lay::kColO1 : Lay::kColO0);
+                    for (int kh = 0; kh < 2 && ok; ++kh) {
+                        const int slot = chunk % kNS;
+                        // landed and converted by the softmax warps
+                        const uint32_t vn = j * kChunks + 2 * h + kh;
+                        if (!(ok = mbar_wait(&ms->vready[vn % kMaxSlots], (vn / kMaxSlots) & 1))) break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t ad = make_desc(hi_v, aS + slot * kChunkBytes + ks * 2048);
-                        const uint64_t bd = make_desc(hi_p, aP + ks * 256);
-                        mma_f16_ss(dO, ad, bd, id_pv, !(first && ks == 0));
-                    }
-                    if constexpr (BF16 && !Lay::kMerge) {
-                        // the lo part of P against the same V, into the same accumulator
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
+                        for (int ks = 0; ks < 4; ++ks) {
                             const uint64_t ad = make_desc(hi_v, aS + slot * kChunkBytes + ks * 2048);
-                            const uint64_t bd = make_desc(hi_p, aP + Lay::kPOneBytes + ks * 256);
-                            mma_f16_ss(dO, ad, bd, id_pv, 1u);
+                            const uint64_t bd = make_desc(hi_p, aP + (4 * kh + ks) * 256);
+                            mma_f16_ss(dO, ad, bd, id_pv, !(first && kh == 0 && ks == 0));
                         }
+                        mma_commit(&ms->empty[slot]);
+                        ++chunk;
                     }
-                    mma_commit(&ms->empty[slot]);
-                    mma_commit(&ms->empty[slot + 1]);
-                    chunk += 2;
                 }
                 if (!ok) break;
                 mma_commit(&ms->pv_done);
@@ -509,13 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool w = mbar_wait(bar, parity);
             return __all_sync(0xffffffffu, w);
         };
-        // the O^T columns of chunk c: d-half h, product part (hi, lo when separate ranges)
-        constexpr int kParts = Lay::kMerge ? 2 : 1;
-
         // One streaming pass over my chunks of S^T: P = 2^(s*scale*log2e - m)
         // with the current shifts; lpart += P (sign +1) or -= P (sign -1, the
         // exact undo of a pass made with the same shifts); optionally stores
-        // P^T (hi and, for bf16, lo) and tracks the largest exponent.  Invalid
+        // P^T (fp16) and tracks the largest exponent.  Invalid
         // keys and padding columns give P = 0.  (A separate unmasked copy of
         // this pass for interior tiles measured slower: the extra code costs
         // more in instruction fetch than the selects it saves.)
@@ -554,19 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nb = 2 * c + hb;
                     uint32_t w[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) w[k] = pack2<BF16>(pv[2 * k], pv[2 * k + 1]);
+                    for (int k = 0; k < 4; ++k) w[k] = pack_half2(pv[2 * k], pv[2 * k + 1]);
                     *reinterpret_cast<uint4*>(sP + nb * 2048 + kl * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                    if constexpr (BF16) {
-                        // residual p - bf16(p): bf16 keeps the top 16 bits of the fp32 pattern
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float h0 = __uint_as_float(w[k] << 16);
-                            const float h1 = __uint_as_float(w[k] & 0xFFFF0000u);
-                            w[k] = pack2<true>(pv[2 * k] - h0, pv[2 * k + 1] - h1);
-                        }
-                        *reinterpret_cast<uint4*>(sP + Lay::kPOneBytes + nb * 2048 + kl * 16) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
-                    }
                 }
             }
         };
@@ -670,11 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int k = 0; k < 16; ++k) any |= ms->alpha[16 * c + k] != 1.f;
                             if (!any) continue;
 #pragma unroll 1
-                            for (int part = 0; part < Lay::kDh * kParts; ++part) {
-                                const int h = part / kParts;
+                            for (int h = 0; h < Lay::kDh; ++h) {
                                 uint32_t r[16];
-                                const uint32_t addr =
-                                    tl + (h ? Lay::kColO1 : Lay::kColO0) + (part % kParts) * RGP + 16 * c;
+                                const uint32_t addr = tl + (h ? Lay::kColO1 : Lay::kColO0) + 16 * c;
                                 tmem_ld16(addr, r);
                                 tmem_wait_ld_regs16(r);
 #pragma unroll
@@ -692,26 +704,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ms->s_free);
 
-                // keys past L inside the last (partial) page: their V rows hold
-                // whatever the pool has there; zero them so 0 * V stays 0
-                if (hf == 0 && (nvalid & (kPage - 1)) != 0 && kl >= nvalid &&
-                    kl < ((nvalid + kPage - 1) & ~(kPage - 1)) && page_ok) {
+                tc_fence_before();
+                fence_proxy_async_smem();  // P^T stores -> tensor-core reads
+                if (!bad && lane == 0) mbar_arrive(&ms->p_full);
+
+                // V(j), chunk by chunk as it lands: bf16 -> fp16 in place, rows of
+                // keys at or past L zeroed (the pool holds arbitrary data there and
+                // 0 * NaN would poison O^T).  Thread st owns the 16-byte units
+                // st, st + 384, st + 768 of a chunk; unit u holds 8 dims of key
+                // 64 * (c & 1) + (u % 512) / 8 (each 8 KB box is [64 keys][128 B];
+                // the swizzle permutes units only within a key's row).
+                if (!bad) {
                     const uint32_t vbase = v_operand(j, n_tiles) * kChunks;
                     for (int c = 0; c < kChunks; ++c) {
-                        const uint32_t ch = vbase + c;
-                        if (!mbar_wait(&ms->full[ch % kNS], (ch / kNS) & 1)) {
+                        const uint32_t vn = j * kChunks + c;
+                        if (!wait_all(&ms->vfull[vn % kMaxSlots], (vn / kMaxSlots) & 1)) {
                             bad = true;
                             break;
                         }
-                        uint8_t* row = sSlots + (ch % kNS) * kChunkBytes + (kl >> 6) * 8192 + (kl & 63) * 128;
+                        uint4* base = reinterpret_cast<uint4*>(sSlots + ((vbase + c) % kNS) * kChunkBytes);
+                        const int nv = nvalid - 64 * (c & 1);  // valid keys of this chunk's page
+                        if (BF16 || nv < 64) {
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) reinterpret_cast<uint4*>(row)[u] = make_uint4(0, 0, 0, 0);
+                            for (int i = 0; i < 3; ++i) {
+                                const int u = st + kSoftmaxThreads * i;
+                                if (u < 1024) {
+                                    const bool kv = ((u & 511) >> 3) < nv;
+                                    uint4 x = make_uint4(0, 0, 0, 0);
+                                    if (kv) {
+                                        x = base[u];
+                                        if constexpr (BF16) {
+                                            x.x = bf16x2_to_f16x2(x.x);
+                                            x.y = bf16x2_to_f16x2(x.y);
+                                            x.z = bf16x2_to_f16x2(x.z);
+                                            x.w = bf16x2_to_f16x2(x.w);
+                                        }
+                                    }
+                                    if (BF16 || !kv) base[u] = x;
+                                }
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ms->vready[vn % kMaxSlots]);
                     }
                 }
-                tc_fence_before();
-                fence_proxy_async_smem();
-                bad = __any_sync(0xffffffffu, bad);  // the partial-page wait above is per lane
-                if (!bad && lane == 0) mbar_arrive(&ms->p_full);
                 ++j;
                 cur.step(p, a.ctx_len);
             }
@@ -724,28 +761,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // row sums: the partial sums of all 128 key lanes go through the P^T
-            // buffer (idle now that PV is done; RGP x 128 floats fit exactly)
-            float* red = reinterpret_cast<float*>(sP);
-            static_assert(RGP * 128 * 4 <= Lay::kPBytes || !BF16, "row-sum staging fits the P^T buffer");
-            static_assert(BF16 || RGP * 128 * 4 <= Lay::kPBytes + Lay::kNS * kChunkBytes, "row-sum staging");
+            // row sums: the warp's 32 key lanes by a butterfly reduce-scatter,
+            // then the four lane quarters through shared memory
 #pragma unroll
             for (int cc = 0; cc < kNa; ++cc) {
                 if (cc >= nch) continue;
+                float v[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) red[(16 * (cb + cc) + k) * 128 + kl] = lpart[cc * 16 + k];
+                for (int k = 0; k < 16; ++k) v[k] = lpart[cc * 16 + k];
+                const float cs = col_sum16(v, lane);
+                if ((lane & 1) == 0) ms->col_red[quarter][16 * (cb + cc) + (lane >> 1)] = cs;
             }
             bar_sync(1, kSoftmaxThreads);
             float* slot = L.ws + slot_index(p, rg, cta, seg) * slot_floats(p);
             float* slot_m = slot + (size_t)RG * D;
             float* slot_l = slot_m + RG;
-            for (int col = warp - 4; col < R_seg; col += kSmWarps) {
-                const float4 v = reinterpret_cast<const float4*>(red + col * 128)[lane];
-                const float sum = warp_sum((v.x + v.y) + (v.z + v.w));
-                if (lane == 0) {
-                    slot_l[col] = sum;
-                    slot_m[col] = ms->m_ref[col];
-                }
+            for (int col = st; col < R_seg; col += kSoftmaxThreads) {
+                slot_l[col] = (ms->col_red[0][col] + ms->col_red[1][col]) + (ms->col_red[2][col] + ms->col_red[3][col]);
+                slot_m[col] = ms->m_ref[col];
             }
 #pragma unroll
             for (int cc = 0; cc < kNa; ++cc) {
@@ -756,17 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[16];
                     const uint32_t addr = tl + (h ? Lay::kColO1 : Lay::kColO0) + 16 * c;
                     tmem_ld16(addr, r);
-                    if constexpr (Lay::kMerge) {
-                        // O = V^T.P_hi^T + V^T.P_lo^T
-                        uint32_t r2[16];
-                        tmem_ld16(addr + RGP, r2);
-                        tmem_wait_ld_regs16(r);
-                        tmem_wait_ld_regs16(r2);
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) + __uint_as_float(r2[k]));
-                    } else {
-                        tmem_wait_ld_regs16(r);
-                    }
+                    tmem_wait_ld_regs16(r);
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
                         const int col = 16 * c + k;
@@ -789,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool BF16, int RGP>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq, const AttnLaunch& L,
                        cudaStream_t stream) {
-    using Lay = Layout<D, RGP, BF16>;
+    using Lay = Layout<D, RGP>;
     auto kern = prefix_tc_kernel<D, BF16, RGP>;
     static bool configured = false;
     if (!configured) {

@@ -27,6 +27,7 @@ DEV_BAD_CTX = 0x4
 DEV_BAD_TOKEN = 0x8
 DEV_BAD_NODE = 0x10
 DEV_TIMEOUT = 0x20
+DEV_NONFINITE = 0x40
 
 EXPORTED = (
     "lucetree_verify_attn_workspace",

@@ -46,6 +46,30 @@ def test_small_ragged_batch_both_dtypes(cuda_dev, dtype, D):
     _check(cfg, W.generate(cfg, seed=21))
 
 
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("D", [128, 256])
+def test_several_key_segments_per_cta(cuda_dev, dtype, D):
+    # 700 tiles over the SMs: most CTAs cross key-segment boundaries, so a
+    # segment's epilogue runs while the next segment's K/V are already landing
+    cfg = W.VerifyConfig("multiseg", ctx=(4000, 3000, 2000, 4100, 130, 5000, 64, 3333), Hq=16, Hkv=4, D=D,
+                         dtype=dtype, N=9, tree="random", branch_cap=3, vocab=512, paged="permuted", spare_pages=4)
+    inp = W.generate(cfg, seed=31)
+    _check(cfg, inp, rows=W.sample_rows(cfg, 160))
+
+
+def test_bf16_v_beyond_fp16_range_is_flagged_nonfinite(cuda_dev):
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    cfg = W.VerifyConfig("vrange", ctx=(300,), Hq=4, Hkv=2, D=128, dtype=W.BF16, N=3, vocab=64)
+    inp = W.generate(cfg, seed=8)
+    d = to_device(inp, cfg)
+    _, _, status = run_attention(d, cfg)
+    assert status == 0
+    page = int(inp["page_table"][0, 2])  # committed position 130 of sequence 0
+    d["v_pool"][page, 1, 2, 5] = 1.0e5
+    _, _, status = run_attention(d, cfg)
+    assert status & LT.DEV_NONFINITE
+
+
 @pytest.mark.parametrize("N,shape", [(1, "chain"), (8, "chain"), (22, "random"), (40, "random"), (64, "random"),
                                      (64, "chain")])
 def test_budgets_cover_row_groups(cuda_dev, N, shape):
