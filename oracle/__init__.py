@@ -55,6 +55,10 @@ def _load():
         lib.oracle_lmhead_argmax.argtypes = [i32, i64, i64, i64, P, P, P, P, P, i32]
         lib.oracle_lmhead_argmax.restype = i32
         lib.oracle_upcast.restype = f64
+        lib.oracle_delta_tree.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P]
+        lib.oracle_delta_tree.restype = i32
+        lib.oracle_delta_commit.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P]
+        lib.oracle_delta_commit.restype = i32
         _lib = lib
     return _lib
 
@@ -182,3 +186,43 @@ def lmhead_argmax(hidden_bits, weight_bits, dtype: int, threads: int | None = No
     if rc != 0:
         raise RuntimeError("oracle_lmhead_argmax failed")
     return out, top1, top2
+
+
+def _delta_dims(inp: dict):
+    B, N, Hk, dk = inp["q"].shape
+    Hv, dv = inp["v"].shape[2], inp["v"].shape[3]
+    return B, N, Hk, Hv, dk, dv
+
+
+def delta_tree(inp: dict, dtype: int) -> np.ndarray:
+    """Gated delta rule along each node's root path from the committed state:
+    S_i = alpha_i (I - beta_i k_i k_i^T) S_parent + beta_i k_i v_i^T, o_i = S_i^T q_i.
+    inp: q, k [B][N][Hk][dk] and v [B][N][Hv][dv] (uint16 bits), alpha, beta
+    [B][N][Hv] float32, parent [B][N] int32, state [B][Hv][dk][dv] float32.
+    Returns out [B][N][Hv][dv] float64."""
+    B, N, Hk, Hv, dk, dv = _delta_dims(inp)
+    q, k, v = (_c(inp[x], np.uint16) for x in ("q", "k", "v"))
+    al, be = _c(inp["alpha"], np.float32), _c(inp["beta"], np.float32)
+    par, st = _c(inp["parent"], np.int32), _c(inp["state"], np.float32)
+    out = np.empty((B, N, Hv, dv), np.float64)
+    rc = _load().oracle_delta_tree(dtype, B, N, Hk, Hv, dk, dv, _p(q), _p(k), _p(v), _p(al), _p(be), _p(par),
+                                   _p(st), _p(out))
+    if rc != 0:
+        raise ValueError("oracle_delta_tree: bad parent array or sizes")
+    return out
+
+
+def delta_commit(inp: dict, dtype: int, acc_nodes, acc_len) -> np.ndarray:
+    """The committed state after the recurrence along acc_nodes[b][:acc_len[b]]
+    (root-to-leaf order) from inp["state"]: [B][Hv][dk][dv] float64."""
+    B, N, Hk, Hv, dk, dv = _delta_dims(inp)
+    k, v = _c(inp["k"], np.uint16), _c(inp["v"], np.uint16)
+    al, be = _c(inp["alpha"], np.float32), _c(inp["beta"], np.float32)
+    an, ln = _c(acc_nodes, np.int32), _c(acc_len, np.int32)
+    st = _c(inp["state"], np.float32)
+    out = np.empty((B, Hv, dk, dv), np.float64)
+    rc = _load().oracle_delta_commit(dtype, B, N, Hk, Hv, dk, dv, _p(k), _p(v), _p(al), _p(be), _p(an), _p(ln),
+                                     _p(st), _p(out))
+    if rc != 0:
+        raise ValueError("oracle_delta_commit: bad accepted path or sizes")
+    return out

@@ -451,3 +451,149 @@ int oracle_lmhead_argmax(int dtype, long rows, long d_model, long vocab, const u
     free(idx);
     return err;
 }
+
+/*
+ * Tree-aware recurrent-state step (gated delta rule).  The pages name a
+ * tree-aware SSM (DeltaNet) rollback kernel among the DFlash components
+ * ("Lucebox Hub", section "Speculative decoding layer (DFlash / DDTree /
+ * DSpark)") for targets that mix DeltaNet and attention layers, but give no
+ * formula.  Reading taken: the gated delta rule with one state S [dk][dv] per
+ * value head,
+ *     S_i = alpha_i (I - beta_i k_i k_i^T) S_parent(i) + beta_i k_i v_i^T,
+ *     o_i = S_i^T q_i,
+ * where the root's S (parent -1) is the committed state and value head h
+ * reads query/key head h / (Hv / Hk).  Each node's output follows from the
+ * recurrence run from the committed state along that node's root path (found
+ * by walking parent[]), one node at a time; the commit runs it along the
+ * accepted path and stores the result, so rejected nodes leave no trace.
+ */
+static int delta_path(const int32_t* parent, int N, int i, int* path) {
+    int n = 0;
+    for (int j = i; j != -1; j = parent[j]) {
+        if (j < -1 || j >= N || n >= N) return -1;
+        if (j != i && j >= path[n - 1]) return -1; /* parents come before children */
+        path[n++] = j;
+    }
+    /* root first */
+    for (int a = 0, b = n - 1; a < b; ++a, --b) {
+        const int t = path[a];
+        path[a] = path[b];
+        path[b] = t;
+    }
+    return n;
+}
+
+/* S <- alpha (I - beta k k^T) S + beta k v^T, S [dk][dv] row-major */
+static void delta_update(int dk, int dv, double* S, const double* k, const double* v, double alpha, double beta,
+                         double* u) {
+    for (int j = 0; j < dv; ++j) {
+        double s = 0.0;
+        for (int r = 0; r < dk; ++r) s += k[r] * S[(size_t)r * dv + j];
+        u[j] = s; /* (k^T S)_j */
+    }
+    for (int r = 0; r < dk; ++r)
+        for (int j = 0; j < dv; ++j) {
+            double* x = &S[(size_t)r * dv + j];
+            *x = alpha * (*x - beta * k[r] * u[j]) + beta * k[r] * v[j];
+        }
+}
+
+static void delta_load(int dtype, const uint16_t* src, int n, double* dst) {
+    for (int x = 0; x < n; ++x) dst[x] = oracle_upcast(dtype, src[x]);
+}
+
+/*
+ * q, k [B][N][Hk][dk], v [B][N][Hv][dv] (16-bit bits of dtype), alpha, beta
+ * [B][N][Hv], parent [B][N], state [B][Hv][dk][dv] (fp32) -> out [B][N][Hv][dv].
+ * Returns 0, or -1 on a bad parent array / sizes / allocation failure.
+ */
+int oracle_delta_tree(int dtype, int B, int N, int Hk, int Hv, int dk, int dv, const uint16_t* q,
+                      const uint16_t* k, const uint16_t* v, const float* alpha, const float* beta,
+                      const int32_t* parent, const float* state, double* out) {
+    if (B < 1 || N < 1 || Hk < 1 || Hv < 1 || Hv % Hk != 0 || dk < 1 || dv < 1) return -1;
+    const int G = Hv / Hk;
+    double* S = (double*)malloc(sizeof(double) * (size_t)dk * dv);
+    double* u = (double*)malloc(sizeof(double) * (size_t)dv);
+    double* kk = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* qq = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* vv = (double*)malloc(sizeof(double) * (size_t)dv);
+    int* path = (int*)malloc(sizeof(int) * (size_t)N);
+    int err = (!S || !u || !kk || !qq || !vv || !path) ? -1 : 0;
+    for (int b = 0; b < B && !err; ++b)
+        for (int h = 0; h < Hv && !err; ++h) {
+            const int hk = h / G;
+            for (int i = 0; i < N && !err; ++i) {
+                const int n = delta_path(parent + (size_t)b * N, N, i, path);
+                if (n < 0) {
+                    err = -1;
+                    break;
+                }
+                const float* s0 = state + ((size_t)b * Hv + h) * (size_t)dk * dv;
+                for (size_t x = 0; x < (size_t)dk * dv; ++x) S[x] = s0[x];
+                for (int t = 0; t < n; ++t) {
+                    const size_t node = (size_t)b * N + path[t];
+                    delta_load(dtype, k + (node * Hk + hk) * dk, dk, kk);
+                    delta_load(dtype, v + (node * Hv + h) * dv, dv, vv);
+                    delta_update(dk, dv, S, kk, vv, alpha[node * Hv + h], beta[node * Hv + h], u);
+                }
+                const size_t node = (size_t)b * N + i;
+                delta_load(dtype, q + (node * Hk + hk) * dk, dk, qq);
+                double* o = out + (node * Hv + h) * dv;
+                for (int j = 0; j < dv; ++j) {
+                    double s = 0.0;
+                    for (int r = 0; r < dk; ++r) s += qq[r] * S[(size_t)r * dv + j];
+                    o[j] = s;
+                }
+            }
+        }
+    free(S);
+    free(u);
+    free(kk);
+    free(qq);
+    free(vv);
+    free(path);
+    return err;
+}
+
+/*
+ * The commit: state_out[b][h] = the recurrence run from state_in[b][h] over
+ * acc_nodes[b][0 .. acc_len[b]) in order.  Returns 0, or -1 on an accepted
+ * count or node outside the tree.
+ */
+int oracle_delta_commit(int dtype, int B, int N, int Hk, int Hv, int dk, int dv, const uint16_t* k,
+                        const uint16_t* v, const float* alpha, const float* beta, const int32_t* acc_nodes,
+                        const int32_t* acc_len, const float* state_in, double* state_out) {
+    if (B < 1 || N < 1 || Hk < 1 || Hv < 1 || Hv % Hk != 0 || dk < 1 || dv < 1) return -1;
+    const int G = Hv / Hk;
+    double* u = (double*)malloc(sizeof(double) * (size_t)dv);
+    double* kk = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* vv = (double*)malloc(sizeof(double) * (size_t)dv);
+    int err = (!u || !kk || !vv) ? -1 : 0;
+    for (int b = 0; b < B && !err; ++b) {
+        const int a = acc_len[b];
+        if (a < 0 || a > N) {
+            err = -1;
+            break;
+        }
+        for (int h = 0; h < Hv; ++h) {
+            const size_t base = ((size_t)b * Hv + h) * (size_t)dk * dv;
+            double* S = state_out + base;
+            for (size_t x = 0; x < (size_t)dk * dv; ++x) S[x] = state_in[base + x];
+            for (int t = 0; t < a && !err; ++t) {
+                const int n = acc_nodes[(size_t)b * N + t];
+                if (n < 0 || n >= N) {
+                    err = -1;
+                    break;
+                }
+                const size_t node = (size_t)b * N + n;
+                delta_load(dtype, k + (node * Hk + h / G) * dk, dk, kk);
+                delta_load(dtype, v + (node * Hv + h) * dv, dv, vv);
+                delta_update(dk, dv, S, kk, vv, alpha[node * Hv + h], beta[node * Hv + h], u);
+            }
+        }
+    }
+    free(u);
+    free(kk);
+    free(vv);
+    return err;
+}

@@ -4,13 +4,17 @@ CPU), exhaustive checks of the 16-bit upcasts, and brute-force enumeration of
 root paths.  Each pin targets a mistake that could plausibly hide in the
 oracle (a dropped mask term, a wrong GQA head, a wrong page index, a reversed
 path, a wrong tie rule)."""
+import json
 import math
+import os
 
 import numpy as np
 import pytest
 
 import oracle
 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
 # ---------------------------------------------------------------- helpers
@@ -423,3 +427,123 @@ def test_lmhead_thread_count_does_not_change_the_result():
     for t in (2, 7, 64):
         got = oracle.lmhead_argmax(hb, wb, oracle.BF16, threads=t)
         assert all(np.array_equal(a, b) for a, b in zip(ref, got))
+
+
+# ---------------------------------------------------------------- gated delta rule (tree-aware recurrent state)
+
+def _f16(x):
+    return np.asarray(x, np.float16).view(np.uint16)
+
+
+def _delta_case(q, k, v, alpha, beta, parent, state):
+    """One sequence, one key head, one value head: q, k [N][dk], v [N][dv]."""
+    q, k, v = (np.asarray(a, np.float64) for a in (q, k, v))
+    N = q.shape[0]
+    return dict(q=_f16(q).reshape(1, N, 1, -1), k=_f16(k).reshape(1, N, 1, -1), v=_f16(v).reshape(1, N, 1, -1),
+                alpha=np.asarray(alpha, np.float32).reshape(1, N, 1), beta=np.asarray(beta, np.float32).reshape(1, N, 1),
+                parent=np.asarray(parent, np.int32).reshape(1, N),
+                state=np.asarray(state, np.float32).reshape(1, 1, q.shape[1], v.shape[1]))
+
+
+def test_delta_hand_example_golden():
+    g = json.load(open(os.path.join(GOLDEN, "delta_rule_hand_example.json")))
+    inp = _delta_case(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["parent"], g["state"])
+    out = oracle.delta_tree(inp, oracle.F16)[0, :, 0, :]
+    assert np.array_equal(out, np.asarray(g["out"], np.float64))
+    N = len(g["parent"])
+    for c in g["commits"]:
+        path = c["path"]
+        acc = np.full((1, N), -1, np.int32)
+        acc[0, :len(path)] = path
+        st = oracle.delta_commit(inp, oracle.F16, acc, np.array([len(path)], np.int32))[0, 0]
+        assert np.array_equal(st, np.asarray(c["state"], np.float64)), path
+
+
+def test_delta_no_write_no_decay_is_a_matrix_vector_product():
+    cfg = W.DeltaConfig("pin-nowrite", B=2, N=9, Hk=2, Hv=4, dk=16, dv=8, dtype=W.F16)
+    inp = W.generate_delta(cfg, seed=3)
+    inp["beta"][:] = 0.0
+    inp["alpha"][:] = 1.0
+    out = oracle.delta_tree(inp, oracle.F16)
+    q = inp["q"].view(np.float16).astype(np.float64)
+    for b in range(2):
+        for h in range(4):
+            ref = q[b, :, h // 2, :] @ inp["state"][b, h].astype(np.float64)
+            assert np.allclose(out[b, :, h, :], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_delta_pure_decay_multiplies_the_path_gates():
+    cfg = W.DeltaConfig("pin-decay", B=1, N=12, Hk=1, Hv=2, dk=8, dv=8, dtype=W.F16, tree="random", branch_cap=3)
+    inp = W.generate_delta(cfg, seed=4)
+    inp["beta"][:] = 0.0
+    out = oracle.delta_tree(inp, oracle.F16)
+    anc = oracle.ancestor_matrix(inp["parent"][0])  # anc[i][j]: j is i or an ancestor of i
+    q = inp["q"].view(np.float16).astype(np.float64)
+    for h in range(2):
+        base = q[0, :, 0, :] @ inp["state"][0, h].astype(np.float64)
+        gate = np.array([np.prod(inp["alpha"][0, anc[i].astype(bool), h].astype(np.float64)) for i in range(12)])
+        assert np.allclose(out[0, :, h, :], gate[:, None] * base, rtol=1e-12, atol=1e-14)
+
+
+def test_delta_full_write_at_a_basis_key_reads_back_the_value():
+    # beta = 1 and k = e_m replace row m of the state by v (whatever alpha is),
+    # so reading with q = e_m returns v exactly
+    cfg = W.DeltaConfig("pin-write", B=1, N=16, Hk=1, Hv=1, dk=8, dv=8, dtype=W.F16, tree="random", branch_cap=2)
+    inp = W.generate_delta(cfg, seed=5)
+    rng = np.random.default_rng(5)
+    m = rng.integers(0, 8, size=16)
+    e = np.zeros((16, 8))
+    e[np.arange(16), m] = 1.0
+    inp["k"][0, :, 0, :] = _f16(e)
+    inp["q"][0, :, 0, :] = _f16(e)
+    inp["beta"][:] = 1.0
+    out = oracle.delta_tree(inp, oracle.F16)[0, :, 0, :]
+    assert np.array_equal(out, inp["v"][0, :, 0, :].view(np.float16).astype(np.float64))
+
+
+def test_delta_relabelling_the_tree_permutes_the_outputs():
+    cfg = W.DeltaConfig("pin-relabel", B=1, N=10, Hk=1, Hv=2, dk=8, dv=4, dtype=W.F16, tree="random", branch_cap=3)
+    inp = W.generate_delta(cfg, seed=6)
+    par = inp["parent"][0]
+    # another topological order: by depth, then by reversed index
+    depth = np.zeros(10, int)
+    for i in range(10):
+        depth[i] = 0 if par[i] < 0 else depth[par[i]] + 1
+    order = sorted(range(10), key=lambda i: (depth[i], -i))
+    new_of = {old: new for new, old in enumerate(order)}
+    p2 = np.array([-1 if par[o] < 0 else new_of[par[o]] for o in order], np.int32)
+    inp2 = dict(inp)
+    for key in ("q", "k", "v", "alpha", "beta"):
+        inp2[key] = np.ascontiguousarray(inp[key][:, order])
+    inp2["parent"] = p2[None, :]
+    a = oracle.delta_tree(inp, oracle.F16)
+    b = oracle.delta_tree(inp2, oracle.F16)
+    assert np.array_equal(a[:, order], b)
+
+
+def test_delta_commit_reads_back_the_node_output_and_empty_commit_keeps_the_state():
+    cfg = W.DeltaConfig("pin-commit", B=2, N=12, Hk=1, Hv=2, dk=8, dv=8, dtype=W.F16, tree="random", branch_cap=3)
+    inp = W.generate_delta(cfg, seed=7)
+    out = oracle.delta_tree(inp, oracle.F16)
+    q = inp["q"].view(np.float16).astype(np.float64)
+    for i in range(12):
+        acc = np.full((2, 12), -1, np.int32)
+        lens = np.zeros(2, np.int32)
+        for b in range(2):
+            anc = oracle.ancestor_matrix(inp["parent"][b])
+            path = [j for j in range(12) if anc[i, j]]  # ancestors in index order = root-to-leaf
+            acc[b, :len(path)] = path
+            lens[b] = len(path)
+        st = oracle.delta_commit(inp, oracle.F16, acc, lens)
+        for b in range(2):
+            for h in range(2):
+                assert np.allclose(q[b, i, 0] @ st[b, h], out[b, i, h], rtol=1e-12, atol=1e-13)
+    none = oracle.delta_commit(inp, oracle.F16, np.zeros((2, 12), np.int32), np.zeros(2, np.int32))
+    assert np.array_equal(none, inp["state"].astype(np.float64))
+
+
+def test_delta_rejects_a_bad_parent():
+    inp = W.generate_delta(W.DeltaConfig("pin-bad", N=4, Hk=1, Hv=1, dk=4, dv=4, dtype=W.F16), seed=1)
+    inp["parent"] = np.array([[-1, 0, 3, 1]], np.int32)
+    with pytest.raises(ValueError):
+        oracle.delta_tree(inp, oracle.F16)

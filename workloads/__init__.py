@@ -324,3 +324,61 @@ def generate_lmhead(cfg: LmHeadConfig, seed: int = 0) -> dict:
         e = min(total, s + chunk)
         out[s:e] = conv(np.float32(cfg.w_std) * rng.standard_normal(e - s, dtype=np.float32))
     return dict(hidden=hidden, weight=out.reshape(cfg.vocab, cfg.d_model))
+
+
+# ----------------------------------------------------------------------------- recurrent-state (delta rule) step
+
+@dataclasses.dataclass(frozen=True)
+class DeltaConfig:
+    """The tree-verify step of a gated-delta-rule (DeltaNet-style) layer of a
+    hybrid target: one recurrent state [dk][dv] per value head, advanced along
+    every tree node's root path.  The pages give no layer shape; 16 query/key
+    heads, 32 value heads and 128-dim heads are this build's reading for a
+    27B-class hybrid target."""
+    name: str
+    B: int = 1
+    N: int = 22
+    Hk: int = 16
+    Hv: int = 32
+    dk: int = 128
+    dv: int = 128
+    dtype: str = BF16
+    tree: str = "random"
+    branch_cap: Optional[int] = 4
+
+    def state_bytes(self) -> int:
+        return self.B * self.Hv * self.dk * self.dv * 4
+
+
+DELTA_TINY = DeltaConfig("delta-tiny-b8", B=1, N=8, Hk=2, Hv=4, dtype=F16, branch_cap=None)
+DELTA_27B_B22 = DeltaConfig("delta-27b-b22")
+DELTA_27B_B40 = DeltaConfig("delta-27b-b40", N=40)
+DELTA_27B_B64_CHAIN = DeltaConfig("delta-27b-b64-chain", N=64, tree="chain")
+DELTA_CONFIGS = {c.name: c for c in (DELTA_TINY, DELTA_27B_B22, DELTA_27B_B40, DELTA_27B_B64_CHAIN)}
+
+
+def generate_delta(cfg: DeltaConfig, seed: int = 0) -> dict:
+    """Seeded inputs of one delta-rule tree step:
+    q, k [B][N][Hk][dk]: normal vectors scaled to unit length, then rounded to
+    the dtype (as the layer feeds L2-normalised queries and keys);
+    v [B][N][Hv][dv] ~ N(0, 1) rounded to the dtype; alpha = exp(-0.1 *
+    softplus(z)) and beta = sigmoid(z) for z ~ N(0, 1), float32 [B][N][Hv];
+    parent [B][N] as for the attention trees; state [B][Hv][dk][dv] ~ N(0, 0.1^2)
+    float32 (the committed state)."""
+    rng = np.random.default_rng(seed * 7919 + _name_key(cfg.name))
+    conv = f32_to_bf16_bits if cfg.dtype == BF16 else f32_to_f16_bits
+
+    def unit(shape):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        x /= np.linalg.norm(x, axis=-1, keepdims=True)
+        return conv(x)
+
+    q = unit((cfg.B, cfg.N, cfg.Hk, cfg.dk))
+    k = unit((cfg.B, cfg.N, cfg.Hk, cfg.dk))
+    v = conv(rng.standard_normal((cfg.B, cfg.N, cfg.Hv, cfg.dv), dtype=np.float32))
+    z = rng.standard_normal((cfg.B, cfg.N, cfg.Hv), dtype=np.float32)
+    alpha = np.exp(-0.1 * np.log1p(np.exp(z))).astype(np.float32)
+    beta = (1.0 / (1.0 + np.exp(-rng.standard_normal((cfg.B, cfg.N, cfg.Hv), dtype=np.float32)))).astype(np.float32)
+    parent = np.stack([random_parents(rng, cfg.N, cfg.tree, cfg.branch_cap) for _ in range(cfg.B)]).astype(np.int32)
+    state = (0.1 * rng.standard_normal((cfg.B, cfg.Hv, cfg.dk, cfg.dv), dtype=np.float32)).astype(np.float32)
+    return dict(q=q, k=k, v=v, alpha=alpha, beta=beta, parent=parent, state=state)
