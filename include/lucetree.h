@@ -21,7 +21,9 @@
  * plus lucetree_build_anc_mask, which turns a parent array into the ancestor
  * bitmasks verify_attn consumes, and lucetree_lmhead_argmax, which replaces
  * the logits + lucetree_argmax pair by the lm_head projection with a fused
- * argmax.
+ * argmax.  For targets with recurrent (gated delta rule) layers,
+ * lucetree_delta_tree advances a layer's state along the tree and
+ * lucetree_delta_commit keeps the accepted node's state.
  *
  * Conventions for every call:
  *   - All array pointers are DEVICE pointers unless a parameter says "host".
@@ -251,6 +253,49 @@ LUCETREE_API lucetree_status lucetree_lmhead_argmax_workspace(int rows, size_t* 
  */
 LUCETREE_API lucetree_status lucetree_lmhead_argmax(const lucetree_lmhead_args* args, void* workspace,
                                                     size_t workspace_bytes, void* stream);
+
+/* Arguments of lucetree_delta_tree and lucetree_delta_commit. */
+typedef struct lucetree_delta_args {
+    int dtype;               /* LUCETREE_F16 / LUCETREE_BF16: q, k, v */
+    int B, N;                /* sequences; tree nodes 1..64 */
+    int Hk, Hv;              /* query/key heads, value heads (Hv % Hk == 0) */
+    int dk, dv;              /* head dims: dk = 128, dv a positive multiple of 8 */
+    const void* q;           /* [B][N][Hk][dk]; tree pass only */
+    const void* k;           /* [B][N][Hk][dk] */
+    const void* v;           /* [B][N][Hv][dv] */
+    const float* alpha;      /* [B][N][Hv] decay gate */
+    const float* beta;       /* [B][N][Hv] write strength */
+    const int32_t* parent;   /* [B][N], parent[i] in [-1, i); tree pass only */
+    float* state;            /* [B][Hv][dk][dv]: read by the tree pass, updated by the commit */
+    float* out;              /* [B][N][Hv][dv]; tree pass only */
+    const int32_t* acc_nodes; /* [B][N] accepted path, root first (lucetree_accept); commit only */
+    const int32_t* acc_len;   /* [B]; commit only */
+    uint32_t* status;        /* device status word, required */
+} lucetree_delta_args;
+
+/*
+ * One gated-delta-rule (DeltaNet-style) layer over the draft tree.  The pages
+ * name a tree-aware DeltaNet rollback kernel for targets that mix DeltaNet
+ * and attention layers ("Lucebox Hub", section "Speculative decoding 계층
+ * (DFlash / DDTree / DSpark)") without a formula.  This library reads it as
+ * follows.  For value head h (query/key head h / (Hv / Hk)), with the
+ * committed state as the root's state:
+ *     S_i = alpha_i (I - beta_i k_i k_i^T) S_parent(i) + beta_i k_i v_i^T
+ *     out_i = S_i^T q_i        (fp32; the state is read, never written)
+ * Layouts are row-major; q, k, v 8-byte and state 16-byte aligned.  Host
+ * errors: INVALID_ARG, UNSUPPORTED (dk != 128, dv % 8, N > 64).  Device
+ * check: BAD_PARENT (that node is then treated as a root child).
+ */
+LUCETREE_API lucetree_status lucetree_delta_tree(const lucetree_delta_args* args, void* stream);
+
+/*
+ * The rollback: state[b] <- the recurrence above run from state[b] over
+ * acc_nodes[b][0 .. acc_len[b]) in order, i.e. the accepted node's state.
+ * Rejected nodes never touch it; acc_len[b] = 0 leaves it bit for bit.
+ * Device check: BAD_NODE (count outside [0, N] or node outside [0, N): that
+ * sequence's state is left unchanged).
+ */
+LUCETREE_API lucetree_status lucetree_delta_commit(const lucetree_delta_args* args, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 LUCETREE_API const char* lucetree_status_string(lucetree_status status);

@@ -4,6 +4,7 @@
 
 #include "internal.cuh"
 #include "lmhead.h"
+#include "delta.h"
 
 namespace lucetree {
 
@@ -144,6 +145,34 @@ lucetree_status lucetree_lmhead_argmax(const lucetree_lmhead_args* a, void* work
         return LUCETREE_ERR_WORKSPACE;
     if (launch_lmhead(*a, workspace, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return LUCETREE_ERR_CUDA;
+    return LUCETREE_OK;
+}
+
+static lucetree_status delta_check(const lucetree_delta_args* a, bool tree) {
+    if (!a) return LUCETREE_ERR_INVALID_ARG;
+    if (a->dtype != LUCETREE_F16 && a->dtype != LUCETREE_BF16) return LUCETREE_ERR_UNSUPPORTED;
+    if (a->B < 1 || a->N < 1 || a->Hk < 1 || a->Hv < 1 || a->Hv % a->Hk != 0 || a->B > 65535 || a->Hv > 65535)
+        return LUCETREE_ERR_INVALID_ARG;
+    if (a->dk != 128 || a->dv < 8 || a->dv % 8 != 0 || a->N > 64) return LUCETREE_ERR_UNSUPPORTED;
+    if (!a->k || !a->v || !a->alpha || !a->beta || !a->state || !a->status) return LUCETREE_ERR_INVALID_ARG;
+    if (tree && (!a->q || !a->parent || !a->out)) return LUCETREE_ERR_INVALID_ARG;
+    if (!tree && (!a->acc_nodes || !a->acc_len)) return LUCETREE_ERR_INVALID_ARG;
+    auto al = [](const void* p, uintptr_t m) { return (reinterpret_cast<uintptr_t>(p) & (m - 1)) == 0; };
+    if (!al(a->k, 8) || !al(a->state, 16) || (tree && !al(a->q, 8))) return LUCETREE_ERR_INVALID_ARG;
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_delta_tree(const lucetree_delta_args* a, void* stream) {
+    const lucetree_status st = delta_check(a, true);
+    if (st != LUCETREE_OK) return st;
+    if (launch_delta_tree(*a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LUCETREE_ERR_CUDA;
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_delta_commit(const lucetree_delta_args* a, void* stream) {
+    const lucetree_status st = delta_check(a, false);
+    if (st != LUCETREE_OK) return st;
+    if (launch_delta_commit(*a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LUCETREE_ERR_CUDA;
     return LUCETREE_OK;
 }
 

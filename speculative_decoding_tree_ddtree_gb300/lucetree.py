@@ -42,6 +42,8 @@ EXPORTED = (
     "lucetree_verify_attn_noalloc",
     "lucetree_lmhead_argmax_workspace",
     "lucetree_lmhead_argmax",
+    "lucetree_delta_tree",
+    "lucetree_delta_commit",
 )
 
 
@@ -80,6 +82,17 @@ class LmHeadArgs(ctypes.Structure):
     ]
 
 
+class DeltaArgs(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int), ("B", ctypes.c_int), ("N", ctypes.c_int), ("Hk", ctypes.c_int),
+        ("Hv", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("parent", ctypes.c_void_p),
+        ("state", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("acc_nodes", ctypes.c_void_p), ("acc_len", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -106,6 +119,8 @@ def load(path: str | None = None):
     lib.lucetree_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnArgs), P]
     lib.lucetree_lmhead_argmax_workspace.argtypes = [I, ctypes.POINTER(SZ)]
     lib.lucetree_lmhead_argmax.argtypes = [ctypes.POINTER(LmHeadArgs), P, SZ, P]
+    lib.lucetree_delta_tree.argtypes = [ctypes.POINTER(DeltaArgs), P]
+    lib.lucetree_delta_commit.argtypes = [ctypes.POINTER(DeltaArgs), P]
     for name in EXPORTED:
         if name not in ("lucetree_status_string", "lucetree_abi_version"):
             getattr(lib, name).restype = I
@@ -302,3 +317,33 @@ def lucetree_lmhead_argmax(hidden, weight, out_idx, status, workspace, out_logit
     a.out_idx, a.out_logit, a.status = _ptr(out_idx), _ptr(out_logit), _ptr(status)
     _check(load().lucetree_lmhead_argmax(ctypes.byref(a), _ptr(workspace),
                                          workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ---------------------------------------------------------------- recurrent-state (delta rule) step
+
+def _delta_args(q, k, v, alpha, beta, state, status, parent=None, out=None, acc_nodes=None, acc_len=None):
+    B, N, Hk, dk = k.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    a = DeltaArgs()
+    a.dtype = dtype_code(k)
+    if dtype_code(v) != a.dtype or (q is not None and dtype_code(q) != a.dtype):
+        raise LucetreeError("q, k and v must share a dtype")
+    a.B, a.N, a.Hk, a.Hv, a.dk, a.dv = B, N, Hk, Hv, dk, dv
+    a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
+    a.alpha, a.beta, a.parent = _ptr(alpha), _ptr(beta), _ptr(parent)
+    a.state, a.out, a.status = _ptr(state), _ptr(out), _ptr(status)
+    a.acc_nodes, a.acc_len = _ptr(acc_nodes), _ptr(acc_len)
+    return a
+
+
+def lucetree_delta_tree(q, k, v, alpha, beta, parent, state, out, status, stream=None):
+    """out[b][i][h] = S_i^T q_i with S_i the gated-delta-rule state along node
+    i's root path from state[b][h] (fp32); the state is only read."""
+    a = _delta_args(q, k, v, alpha, beta, state, status, parent=parent, out=out)
+    _check(load().lucetree_delta_tree(ctypes.byref(a), _stream(stream)))
+
+
+def lucetree_delta_commit(k, v, alpha, beta, acc_nodes, acc_len, state, status, stream=None):
+    """state[b][h] <- the recurrence along acc_nodes[b][:acc_len[b]] (in place)."""
+    a = _delta_args(None, k, v, alpha, beta, state, status, acc_nodes=acc_nodes, acc_len=acc_len)
+    _check(load().lucetree_delta_commit(ctypes.byref(a), _stream(stream)))

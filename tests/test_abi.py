@@ -68,6 +68,15 @@ def test_host_side_queries_without_gpu(lib):
     a = LT.LmHeadArgs(dtype=LT.LUCETREE_BF16, rows=8, d_model=256, vocab=1000,
                       hidden=fake, weight=fake, out_idx=fake, out_logit=None, status=fake)
     assert lt.lucetree_lmhead_argmax(ctypes.byref(a), None, 0, None) == 3  # no workspace
+    # delta-rule step: shape limits and required pointers, checked on the host
+    assert lt.lucetree_delta_tree(None, None) == 1 and lt.lucetree_delta_commit(None, None) == 1
+    for (dk, dv, N, want) in ((64, 128, 8, 2), (128, 12, 8, 2), (128, 128, 65, 2), (128, 128, 0, 1)):
+        d = LT.DeltaArgs(dtype=LT.LUCETREE_BF16, B=1, N=N, Hk=1, Hv=2, dk=dk, dv=dv, q=fake, k=fake, v=fake,
+                         alpha=fake, beta=fake, parent=fake, state=fake, out=fake, status=fake)
+        assert lt.lucetree_delta_tree(ctypes.byref(d), None) == want
+    d = LT.DeltaArgs(dtype=LT.LUCETREE_BF16, B=1, N=8, Hk=1, Hv=2, dk=128, dv=128, k=fake, v=fake,
+                     alpha=fake, beta=fake, state=fake, status=fake)
+    assert lt.lucetree_delta_commit(ctypes.byref(d), None) == 1  # no accepted path given
 
 
 def test_binding_rejects_host_tensors():
