@@ -409,6 +409,9 @@ def run_ours(args, cfg):
         # the lm_head row is measured apart from the step: the step takes the
         # generator's logits, this call produces the argmax from hidden states
         line["lmhead_argmax"] = measure_lmhead(args, dev, stream, rank, with_cpu=world == 1 and not args.no_cpu_baseline)
+    if not args.no_delta:
+        # the recurrent-state row of hybrid targets, measured apart from the attention step
+        line["delta_rule"] = measure_delta(args, dev, stream, rank, with_cpu=world == 1 and not args.no_cpu_baseline)
     print(json.dumps(line), flush=True)
     if dist.is_initialized():
         dist.destroy_process_group()
@@ -474,6 +477,109 @@ def measure_lmhead(args, dev, stream, rank, with_cpu=True):
     return res
 
 
+def measure_delta(args, dev, stream, rank, with_cpu=True):
+    """The recurrent-state (gated delta rule) tree pass and its commit on the
+    27B-class hybrid-layer workload (22-node tree, 16 q/k and 32 v heads of
+    128 dims, fp32 state), timed alone with CUDA events on their stream.  The
+    commit replays the deepest root path.  Inputs are the seeded workload."""
+    import torch
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    dc = W.DELTA_27B_B22
+    inp = W.generate_delta(dc, seed=rank)
+    tdt = torch.bfloat16
+    d = {k: torch.from_numpy(np.ascontiguousarray(inp[k]).view(np.int16)).view(tdt).to(dev) for k in ("q", "k", "v")}
+    for k in ("alpha", "beta", "state", "parent"):
+        d[k] = torch.from_numpy(np.ascontiguousarray(inp[k])).to(dev)
+    out = torch.empty(dc.B, dc.N, dc.Hv, dc.dv, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    par = inp["parent"][0]
+    depth = np.zeros(dc.N, int)
+    for i in range(dc.N):
+        depth[i] = 0 if par[i] < 0 else depth[par[i]] + 1
+    path, i = [], int(np.argmax(depth))
+    while i >= 0:
+        path.append(i)
+        i = int(par[i])
+    path = path[::-1]
+    acc = np.full((dc.B, dc.N), -1, np.int32)
+    acc[0, :len(path)] = path
+    acc_d = torch.from_numpy(acc).to(dev)
+    len_d = torch.tensor([len(path)], dtype=torch.int32, device=dev)
+    state_work = d["state"].clone()
+
+    def tree():
+        LT.lucetree_delta_tree(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["state"], out, st,
+                               stream=stream)
+
+    def commit():
+        LT.lucetree_delta_commit(d["k"], d["v"], d["alpha"], d["beta"], acc_d, len_d, state_work, st, stream=stream)
+
+    def timed(fn, n):
+        # a few microseconds of GPU work per call: the calls are captured in a
+        # CUDA graph (20 per graph) and replayed, so host-side argument
+        # marshalling does not leak into the device time
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(20):
+                fn()
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / (20 * n)
+
+    n = max(20, min(200, args.steps // 10))
+    tree_ms, commit_ms = timed(tree, n), timed(commit, n)
+    qkv = dc.B * dc.N * (2 * dc.Hk * dc.dk + dc.Hv * dc.dv) * 2 + dc.B * dc.N * dc.Hv * 8 + dc.B * dc.N * 4
+    tree_bytes = dc.state_bytes() + qkv + dc.B * dc.N * dc.Hv * dc.dv * 4
+    a = len(path)
+    commit_bytes = 2 * dc.state_bytes() + dc.B * a * (dc.Hk * dc.dk + dc.Hv * dc.dv) * 2 + dc.B * a * dc.Hv * 8
+    peak, peak_kind = peak_hbm()
+    res = {
+        "workload": f"{dc.name}: B {dc.B}, N {dc.N} (random tree, depth {int(depth.max()) + 1}), Hk {dc.Hk}, "
+                    f"Hv {dc.Hv}, dk {dc.dk}, dv {dc.dv}, bf16 q/k/v, fp32 state; commit of {a} nodes",
+        "tree_ms_per_call": tree_ms, "commit_ms_per_call": commit_ms, "calls_timed": 20 * n,
+        "timing": "CUDA graph of 20 calls replayed; device time per call",
+        "device_status": int(st.item()),
+        "roofline": {"bound": "latency", "kernel": "lucetree_delta_tree",
+                     "achieved": tree_bytes / (tree_ms * 1e-3) / 1e9, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": tree_bytes / (tree_ms * 1e-3) / 1e9 / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": tree_bytes},
+        "commit_roofline": {"bound": "latency", "kernel": "lucetree_delta_commit",
+                            "achieved": commit_bytes / (commit_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                            "frac": commit_bytes / (commit_ms * 1e-3) / 1e9 / peak,
+                            "algorithmic_bytes_per_launch": commit_bytes},
+    }
+    if with_cpu:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.delta_tree(inp, oracle.BF16)
+        oracle.delta_commit(inp, oracle.BF16, acc, np.array([a], np.int32))
+        res["cpu_baseline"] = {"ms_per_call": (time.perf_counter() - t0) * 1e3, "cores": 1, "kind": "oracle",
+                               "sample": "the whole workload: tree pass plus commit, one thread"}
+    return res
+
+
+def run_delta_only(args):
+    import torch
+    from speculative_decoding_tree_ddtree_gb300.build import build
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    print(json.dumps({"delta_rule": measure_delta(args, dev, stream, 0, with_cpu=False)}), flush=True)
+    return 0
+
+
 def run_lmhead_only(args):
     import torch
     from speculative_decoding_tree_ddtree_gb300.build import build
@@ -497,9 +603,13 @@ def main(argv=None):
     ap.add_argument("--lmhead-only", action="store_true", help="time only the fused lm_head + argmax")
     ap.add_argument("--lmhead-vocab", type=int, default=None,
                     help="with --lmhead-only: a smaller vocabulary (profiler captures)")
+    ap.add_argument("--no-delta", action="store_true", help="skip the recurrent-state (delta rule) measurement")
+    ap.add_argument("--delta-only", action="store_true", help="time only the recurrent-state tree pass and commit")
     args = ap.parse_args(argv)
     if args.lmhead_only:
         return run_lmhead_only(args)
+    if args.delta_only:
+        return run_delta_only(args)
     cfg = W.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)

@@ -7,7 +7,6 @@
 
 namespace lucetree {
 
-int delta_tree_columns(int N);       // state columns per CTA of the tree pass (8 or 4)
 size_t delta_tree_smem_bytes(int N);  // dynamic shared memory of the tree pass
 cudaError_t launch_delta_tree(const lucetree_delta_args& a, cudaStream_t stream);
 cudaError_t launch_delta_commit(const lucetree_delta_args& a, cudaStream_t stream);

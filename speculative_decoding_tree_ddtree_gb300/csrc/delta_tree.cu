@@ -5,21 +5,25 @@
 // parent p (p = -1: the committed state S_root) gives
 //     S_i = alpha_i (I - beta_i k_i k_i^T) S_p + beta_i k_i v_i^T,
 //     o_i = S_i^T q_i.
-// Column j of S only ever mixes with column j, so a CTA owns C columns of one
-// (sequence, value head) and keeps that slice of every node's state in shared
-// memory ([node][C][dk], column-major so a lane's four rows are one 16-byte
-// load).  With u = k^T S_p and w = q^T S_p (one warp reduction for both),
+// Column j of S only ever mixes with column j, so a CTA owns C = 8 columns of
+// one (sequence, value head).  With u = k^T S_p and w = q^T S_p (one warp
+// reduction for both),
 //     d_j = beta (v_j - alpha u_j),   o_j = alpha w_j + (q . k) d_j,
 //     S_i[r][j] = alpha S_p[r][j] + k_r d_j.
-// Nodes are processed level by level (all nodes of one depth in parallel,
-// one warp per node; a level only reads states of the level above), so the
-// chain is the tree's depth, not its size.  Everything a level reads
-// (q, k, the v slice, alpha, beta) is staged in shared memory by the prologue.
 //
-// The commit replays the accepted path (acc_nodes[b][0 .. acc_len[b])) from
-// the committed state, one warp per (sequence, head, C columns) with the slice
-// in registers, and writes the state back in place: rejected nodes never touch
-// it.  dk = 128 (lane l owns rows 4l .. 4l+3).
+// Tree pass: every node lies on the root path of some leaf, so each warp
+// takes leaves in turn and replays the leaf's root path from the committed
+// state with the state slice in registers (lane l owns rows 4l .. 4l+3),
+// writing every node's output on the way.  A node on the paths of several
+// leaves is recomputed by the same instruction sequence from the same inputs,
+// so the repeated writes carry identical values.  Nothing but inputs lives in
+// shared memory (q, k, the v slice, the gates, staged once), so every CTA of
+// a head fits on the chip at once; the cost is the sum of the leaves' depths
+// per CTA, and a chain is a single replay.
+//
+// The commit replays the accepted path (acc_nodes[b][0 .. acc_len[b])) the
+// same way and writes the state back in place: rejected nodes never touch it.
+// dk = 128.
 #include "internal.cuh"
 #include "delta.h"
 
@@ -28,8 +32,10 @@ namespace lucetree {
 namespace {
 
 constexpr int kDk = 128;
-constexpr int kWarps = 8;
+constexpr int kC = 8;                 // state columns per CTA
+constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxN = 64;
 
 // Sum of each of V values over the warp's 32 lanes, scattered: recursive
 // halving over the top log2(V) lane bits, then a butterfly over the rest.
@@ -66,239 +72,342 @@ __device__ __forceinline__ float to_f32(uint16_t b) {
     else return __half2float(__ushort_as_half(b));
 }
 
-template <int C>
-struct TreeSmem {
-    static constexpr size_t bytes(int N) {
-        return (size_t)(N + 1) * C * kDk * 4      // states: N nodes + the committed one
-               + (size_t)2 * N * kDk * 4          // q, k (fp32)
-               + (size_t)N * C * 4                // v slice
-               + (size_t)2 * N * 4                // alpha, beta
-               + (size_t)4 * 64 * 4 + 16;         // parent, order, level starts, flags
-    }
-};
-
-template <bool BF16, int C>
-__global__ void __launch_bounds__(kThreads) delta_tree_kernel(lucetree_delta_args a) {
-    extern __shared__ __align__(16) float sm[];
-    const int N = a.N, Hv = a.Hv, Hk = a.Hk, dv = a.dv;
-    const int slice = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int hk = h / (Hv / Hk), c0 = slice * C;
-    float* st = sm;                                    // [N + 1][C][kDk]; slot N = committed state
-    float* sq = st + (size_t)(N + 1) * C * kDk;        // [N][kDk]
-    float* sk = sq + (size_t)N * kDk;                  // [N][kDk]
-    float* sv = sk + (size_t)N * kDk;                  // [N][C]
-    float* sal = sv + (size_t)N * C;                   // [N]
-    float* sbe = sal + N;                              // [N]
-    int* spar = reinterpret_cast<int*>(sbe + N);       // [64]
-    int* sord = spar + 64;                             // [64] nodes by depth
-    int* slvl = sord + 64;                             // [65] level starts
-    int* sflag = slvl + 65;                            // [64] has children; [0..] reused
-    __shared__ int n_levels;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    pdl_wait();
-    if (threadIdx.x == 0) pdl_trigger();
-
-    // ---- prologue: tree, inputs, committed state slice
-    for (int i = threadIdx.x; i < N; i += kThreads) {
-        int p = a.parent[(size_t)b * N + i];
-        if (p < -1 || p >= i) {
-            atomicOr(a.status, LUCETREE_DEV_BAD_PARENT);
-            p = -1;
-        }
-        spar[i] = p;
-        sflag[i] = 0;
-    }
-    {
-        const uint16_t* q = reinterpret_cast<const uint16_t*>(a.q);
-        const uint16_t* k = reinterpret_cast<const uint16_t*>(a.k);
-        for (int e = threadIdx.x; e < N * kDk; e += kThreads) {
-            const int i = e / kDk, r = e % kDk;
-            const size_t off = (((size_t)b * N + i) * Hk + hk) * kDk + r;
-            sq[e] = to_f32<BF16>(q[off]);
-            sk[e] = to_f32<BF16>(k[off]);
-        }
-        const uint16_t* v = reinterpret_cast<const uint16_t*>(a.v);
-        for (int e = threadIdx.x; e < N * C; e += kThreads) {
-            const int i = e / C, j = e % C;
-            sv[e] = to_f32<BF16>(v[(((size_t)b * N + i) * Hv + h) * dv + c0 + j]);
-        }
-        for (int i = threadIdx.x; i < N; i += kThreads) {
-            sal[i] = a.alpha[((size_t)b * N + i) * Hv + h];
-            sbe[i] = a.beta[((size_t)b * N + i) * Hv + h];
-        }
-        const float* s0 = a.state + ((size_t)b * Hv + h) * kDk * dv + c0;
-        float* root = st + (size_t)N * C * kDk;
-        for (int e = threadIdx.x; e < kDk * (C / 4); e += kThreads) {
-            const int r = e / (C / 4), j4 = 4 * (e % (C / 4));
-            const float4 x = *reinterpret_cast<const float4*>(s0 + (size_t)r * dv + j4);
-            root[(j4 + 0) * kDk + r] = x.x;
-            root[(j4 + 1) * kDk + r] = x.y;
-            root[(j4 + 2) * kDk + r] = x.z;
-            root[(j4 + 3) * kDk + r] = x.w;
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        // depth by parent (parents precede children), then a counting sort
-        int depth[64], cnt[65];
-        int maxd = 0;
-        for (int d = 0; d <= N; ++d) cnt[d] = 0;
-        for (int i = 0; i < N; ++i) {
-            const int p = spar[i];
-            depth[i] = p < 0 ? 0 : depth[p] + 1;
-            if (p >= 0) sflag[p] = 1;
-            maxd = max(maxd, depth[i]);
-            ++cnt[depth[i]];
-        }
-        slvl[0] = 0;
-        for (int d = 0; d <= maxd; ++d) slvl[d + 1] = slvl[d] + cnt[d];
-        for (int d = 0; d <= maxd; ++d) cnt[d] = slvl[d];
-        for (int i = 0; i < N; ++i) sord[cnt[depth[i]]++] = i;
-        n_levels = maxd + 1;
-    }
-    __syncthreads();
-
-    // ---- levels
-    constexpr int V = 2 * C;
-    constexpr int kGroup = 32 / V;  // lanes holding the same reduced value
-    const int nl = n_levels;
-    for (int lv = 0; lv < nl; ++lv) {
-        for (int x = slvl[lv] + warp; x < slvl[lv + 1]; x += kWarps) {
-            const int i = sord[x];
-            const int p = spar[i];
-            const float* sp = st + (size_t)(p < 0 ? N : p) * C * kDk;
-            const float4 k4 = *reinterpret_cast<const float4*>(sk + (size_t)i * kDk + 4 * lane);
-            const float4 q4 = *reinterpret_cast<const float4*>(sq + (size_t)i * kDk + 4 * lane);
-            float part[V];
-#pragma unroll
-            for (int j = 0; j < C; ++j) {
-                const float4 s4 = *reinterpret_cast<const float4*>(sp + (size_t)j * kDk + 4 * lane);
-                part[j] = k4.x * s4.x + k4.y * s4.y + k4.z * s4.z + k4.w * s4.w;
-                part[C + j] = q4.x * s4.x + q4.y * s4.y + q4.z * s4.z + q4.w * s4.w;
-            }
-            const float qk = warp_sum(q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w);
-            const float red = reduce_scatter<V>(part, lane);      // u_j (idx < C) or w_{idx - C}
-            const int idx = lane / kGroup;
-            const float w = __shfl_sync(0xffffffffu, red, (lane + C * kGroup) & 31);
-            const float al = sal[i], be = sbe[i];
-            float d = 0.f;
-            if (idx < C) {
-                d = be * (sv[i * C + idx] - al * red);
-                if (lane % kGroup == 0)
-                    a.out[(((size_t)b * N + i) * Hv + h) * dv + c0 + idx] = al * w + qk * d;
-            }
-            if (sflag[i]) {
-                float* si = st + (size_t)i * C * kDk;
-#pragma unroll
-                for (int j = 0; j < C; ++j) {
-                    const float dj = __shfl_sync(0xffffffffu, d, j * kGroup);
-                    const float4 s4 = *reinterpret_cast<const float4*>(sp + (size_t)j * kDk + 4 * lane);
-                    float4 n4;
-                    n4.x = fmaf(k4.x, dj, al * s4.x);
-                    n4.y = fmaf(k4.y, dj, al * s4.y);
-                    n4.z = fmaf(k4.z, dj, al * s4.z);
-                    n4.w = fmaf(k4.w, dj, al * s4.w);
-                    *reinterpret_cast<float4*>(si + (size_t)j * kDk + 4 * lane) = n4;
-                }
-            }
-        }
-        __syncthreads();
-    }
+template <bool BF16>
+__device__ __forceinline__ float4 load4(const uint16_t* p) {  // four 16-bit values, 8-byte aligned
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    return make_float4(to_f32<BF16>((uint16_t)(x.x & 0xFFFFu)), to_f32<BF16>((uint16_t)(x.x >> 16)),
+                       to_f32<BF16>((uint16_t)(x.y & 0xFFFFu)), to_f32<BF16>((uint16_t)(x.y >> 16)));
 }
 
-// One warp per (slice, head, sequence); the state slice stays in registers.
-template <bool BF16, int C>
-__global__ void __launch_bounds__(32) delta_commit_kernel(lucetree_delta_args a) {
-    const int N = a.N, Hv = a.Hv, Hk = a.Hk, dv = a.dv;
-    const int slice = blockIdx.x, h = blockIdx.y, b = blockIdx.z, lane = threadIdx.x;
-    const int hk = h / (Hv / Hk), c0 = slice * C;
-    pdl_wait();
-    if (lane == 0) pdl_trigger();
-    int n_acc = a.acc_len[b];
-    if (n_acc < 0 || n_acc > N) {
-        if (lane == 0 && slice == 0 && h == 0) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
-        return;
+// Staged inputs of one CTA: per node the key (and query) rows, the CTA's v
+// columns, the gates and q . k.
+struct Stage {
+    float* k;     // [N][kDk]
+    float* q;     // [N][kDk] (tree pass only)
+    float* v;     // [N][vs], this warp's first column at v[0]
+    int vs;       // row stride of v
+    float* al;    // [N]
+    float* be;    // [N]
+    float* qk;    // [N] (tree pass only)
+};
+
+// dynamic shared memory: k (and q) rows, ncol v columns, the gates (and q . k)
+__host__ __device__ constexpr size_t stage_bytes(int N, bool with_q, int ncol) {
+    return (size_t)N * kDk * 4 * (with_q ? 2 : 1) + (size_t)N * (ncol + (with_q ? 3 : 2)) * 4;
+}
+
+// One node of the recurrence on the warp's register state S[m][j] = S[4l+m][c0+j].
+// With EMIT, also returns the node's output column (on lanes 4j, j < 8).
+template <bool EMIT>
+__device__ __forceinline__ float delta_step(float (&S)[4][kC], const Stage& sg, int n, int lane) {
+    const float4 k4 = *reinterpret_cast<const float4*>(sg.k + (size_t)n * kDk + 4 * lane);
+    const float kr[4] = {k4.x, k4.y, k4.z, k4.w};
+    constexpr int V = EMIT ? 2 * kC : kC;
+    float part[V];
+#pragma unroll
+    for (int j = 0; j < kC; ++j) part[j] = kr[0] * S[0][j] + kr[1] * S[1][j] + kr[2] * S[2][j] + kr[3] * S[3][j];
+    if constexpr (EMIT) {
+        const float4 q4 = *reinterpret_cast<const float4*>(sg.q + (size_t)n * kDk + 4 * lane);
+#pragma unroll
+        for (int j = 0; j < kC; ++j)
+            part[kC + j] = q4.x * S[0][j] + q4.y * S[1][j] + q4.z * S[2][j] + q4.w * S[3][j];
     }
-    if (n_acc == 0) return;  // nothing accepted: the committed state stays as it is
-    float* s0 = a.state + ((size_t)b * Hv + h) * kDk * dv + c0;
-    float S[4][C];
+    constexpr int kGroup = 32 / V;
+    const float red = reduce_scatter<V>(part, lane);  // u_{lane / kGroup} (or w_{lane / kGroup - kC})
+    const int idx = lane / kGroup;
+    const float al = sg.al[n], be = sg.be[n];
+    float d = 0.f, o = 0.f;
+    if (idx < kC) d = be * (sg.v[n * sg.vs + idx] - al * red);
+    if constexpr (EMIT) {
+        const float w = __shfl_sync(0xffffffffu, red, (lane + kC * kGroup) & 31);
+        o = al * w + sg.qk[n] * d;
+    }
+#pragma unroll
+    for (int j = 0; j < kC; ++j) {
+        const float dj = __shfl_sync(0xffffffffu, d, j * kGroup);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) S[m][j] = fmaf(kr[m], dj, al * S[m][j]);
+    }
+    return o;
+}
+
+__device__ __forceinline__ void load_state(float (&S)[4][kC], const float* s0, int dv, int lane) {
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int j4 = 0; j4 < C; j4 += 4) {
+        for (int j4 = 0; j4 < kC; j4 += 4) {
             const float4 x = *reinterpret_cast<const float4*>(s0 + (size_t)(4 * lane + m) * dv + j4);
             S[m][j4] = x.x;
             S[m][j4 + 1] = x.y;
             S[m][j4 + 2] = x.z;
             S[m][j4 + 3] = x.w;
         }
+}
+
+// Stage the inputs of nodes list[0 .. n) (list = nullptr: nodes 0 .. n) into
+// sg: k (and q) rows, v columns c0 .. c0 + sg.vs (those below dv), the gates.
+// Each thread issues kB loads before it stores any, so the staging costs one
+// or two memory round trips rather than one per element group.
+template <bool BF16, bool WITH_Q>
+__device__ void stage_inputs(const lucetree_delta_args& a, const Stage& sg, const int* list, int n, int b, int h,
+                             int hk, int c0) {
+    constexpr int kB = 8;
     const uint16_t* kp = reinterpret_cast<const uint16_t*>(a.k);
+    const uint16_t* qp = reinterpret_cast<const uint16_t*>(a.q);
     const uint16_t* vp = reinterpret_cast<const uint16_t*>(a.v);
-    constexpr int kGroup = 32 / C;
-    for (int t = 0; t < n_acc; ++t) {
-        const int i = a.acc_nodes[(size_t)b * N + t];
-        if (i < 0 || i >= N) {
-            if (lane == 0 && slice == 0 && h == 0) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
-            return;  // the state is left as it was
+    const int total = n * (kDk / 4);
+    for (int e0 = threadIdx.x; e0 < total; e0 += kB * kThreads) {
+        uint2 xk[kB], xq[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const int e = e0 + u * kThreads;
+            if (e < total) {
+                const int t = e / (kDk / 4), r = 4 * (e % (kDk / 4));
+                const size_t off = (((size_t)b * a.N + (list ? list[t] : t)) * a.Hk + hk) * kDk + r;
+                xk[u] = *reinterpret_cast<const uint2*>(kp + off);
+                if constexpr (WITH_Q) xq[u] = *reinterpret_cast<const uint2*>(qp + off);
+            }
         }
-        const size_t node = (size_t)b * N + i;
-        const uint2 kb = *reinterpret_cast<const uint2*>(kp + (node * Hk + hk) * kDk + 4 * lane);
-        const float kr[4] = {to_f32<BF16>((uint16_t)(kb.x & 0xFFFFu)), to_f32<BF16>((uint16_t)(kb.x >> 16)),
-                             to_f32<BF16>((uint16_t)(kb.y & 0xFFFFu)), to_f32<BF16>((uint16_t)(kb.y >> 16))};
-        float part[C];
 #pragma unroll
-        for (int j = 0; j < C; ++j) part[j] = kr[0] * S[0][j] + kr[1] * S[1][j] + kr[2] * S[2][j] + kr[3] * S[3][j];
-        const float u = reduce_scatter<C>(part, lane);  // u_{lane / kGroup}
-        const float al = a.alpha[node * Hv + h], be = a.beta[node * Hv + h];
-        const float d = be * (to_f32<BF16>(vp[(node * Hv + h) * dv + c0 + lane / kGroup]) - al * u);
-#pragma unroll
-        for (int j = 0; j < C; ++j) {
-            const float dj = __shfl_sync(0xffffffffu, d, j * kGroup);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) S[m][j] = fmaf(kr[m], dj, al * S[m][j]);
+        for (int u = 0; u < kB; ++u) {
+            const int e = e0 + u * kThreads;
+            if (e < total) {
+                const int t = e / (kDk / 4), r = 4 * (e % (kDk / 4));
+                auto cvt = [](uint2 x) {
+                    return make_float4(to_f32<BF16>((uint16_t)(x.x & 0xFFFFu)), to_f32<BF16>((uint16_t)(x.x >> 16)),
+                                       to_f32<BF16>((uint16_t)(x.y & 0xFFFFu)), to_f32<BF16>((uint16_t)(x.y >> 16)));
+                };
+                *reinterpret_cast<float4*>(sg.k + (size_t)t * kDk + r) = cvt(xk[u]);
+                if constexpr (WITH_Q) *reinterpret_cast<float4*>(sg.q + (size_t)t * kDk + r) = cvt(xq[u]);
+            }
         }
     }
+    const int tv = n * sg.vs;
+    for (int e0 = threadIdx.x; e0 < tv + 2 * n; e0 += 4 * kThreads) {
+        float x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * kThreads;
+            x[u] = 0.f;
+            if (e < tv) {
+                const int t = e / sg.vs, j = e % sg.vs;
+                if (c0 + j < a.dv)
+                    x[u] = to_f32<BF16>(vp[(((size_t)b * a.N + (list ? list[t] : t)) * a.Hv + h) * a.dv + c0 + j]);
+            } else if (e < tv + 2 * n) {
+                const int t = (e - tv) >> 1;
+                const size_t g = ((size_t)b * a.N + (list ? list[t] : t)) * a.Hv + h;
+                x[u] = ((e - tv) & 1) ? a.beta[g] : a.alpha[g];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * kThreads;
+            if (e < tv) sg.v[e] = x[u];
+            else if (e < tv + 2 * n) (((e - tv) & 1) ? sg.be : sg.al)[(e - tv) >> 1] = x[u];
+        }
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) delta_tree_kernel(lucetree_delta_args a) {
+    extern __shared__ __align__(16) float sm[];
+    __shared__ int spar[kMaxN], sleaf[kMaxN], schild[kMaxN], spath[kWarps][kMaxN], splen[kWarps];
+    __shared__ __align__(16) float sroot[kC * kDk];  // committed state slice, [column][row]
+    __shared__ int n_leaves;
+    const int N = a.N, Hv = a.Hv, dv = a.dv;
+    const int slice = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int hk = h / (Hv / a.Hk), c0 = slice * kC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Stage sg;
+    sg.k = sm;
+    sg.q = sg.k + (size_t)N * kDk;
+    sg.v = sg.q + (size_t)N * kDk;
+    sg.vs = kC;
+    sg.al = sg.v + (size_t)N * kC;
+    sg.be = sg.al + N;
+    sg.qk = sg.be + N;
+
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
+
+    // ---- tree (invalid parents become root children), committed slice, inputs
+    const float* s0 = a.state + ((size_t)b * Hv + h) * kDk * dv + c0;
+    {
+        // kDk rows x kC columns: two 16-byte loads per thread, stored column-major
+        float4 x[kC * kDk / 4 / kThreads];
+#pragma unroll
+        for (int u = 0; u < kC * kDk / 4 / kThreads; ++u) {
+            const int e = threadIdx.x + u * kThreads, r = e / (kC / 4), j4 = 4 * (e % (kC / 4));
+            x[u] = *reinterpret_cast<const float4*>(s0 + (size_t)r * dv + j4);
+        }
+        for (int i = threadIdx.x; i < N; i += kThreads) {
+            int p = a.parent[(size_t)b * N + i];
+            if (p < -1 || p >= i) {
+                atomicOr(a.status, LUCETREE_DEV_BAD_PARENT);
+                p = -1;
+            }
+            spar[i] = p;
+            schild[i] = 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kC * kDk / 4 / kThreads; ++u) {
+            const int e = threadIdx.x + u * kThreads, r = e / (kC / 4), j4 = 4 * (e % (kC / 4));
+            sroot[(j4 + 0) * kDk + r] = x[u].x;
+            sroot[(j4 + 1) * kDk + r] = x[u].y;
+            sroot[(j4 + 2) * kDk + r] = x[u].z;
+            sroot[(j4 + 3) * kDk + r] = x[u].w;
+        }
+    }
+    stage_inputs<BF16, true>(a, sg, nullptr, N, b, h, hk, c0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < N; i += kThreads)
+        if (spar[i] >= 0) schild[spar[i]] = 1;
+    __syncthreads();
+    if (warp == 0) {
+        int cnt = 0;
+        for (int base = 0; base < N; base += 32) {
+            const int i = base + lane;
+            const bool leaf = i < N && !schild[i];
+            const unsigned m = __ballot_sync(0xffffffffu, leaf);
+            if (leaf) sleaf[cnt + __popc(m & ((1u << lane) - 1u))] = i;
+            cnt += __popc(m);
+        }
+        if (lane == 0) n_leaves = cnt;
+    }
+    for (int i = warp; i < N; i += kWarps) {
+        const float4 q4 = *reinterpret_cast<const float4*>(sg.q + (size_t)i * kDk + 4 * lane);
+        const float4 k4 = *reinterpret_cast<const float4*>(sg.k + (size_t)i * kDk + 4 * lane);
+        const float qk = warp_sum(q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w);
+        if (lane == 0) sg.qk[i] = qk;
+    }
+    __syncthreads();
+
+    // ---- one leaf's root path per warp at a time
+    int* path = spath[warp];
+    for (int x = warp; x < n_leaves; x += kWarps) {
+        if (lane == 0) {
+            int len = 0;
+            for (int j = sleaf[x]; j >= 0 && len < kMaxN; j = spar[j]) path[len++] = j;  // leaf first
+            splen[warp] = len;
+        }
+        __syncwarp();
+        float S[4][kC];
+#pragma unroll
+        for (int j = 0; j < kC; ++j) {
+            const float4 x4 = *reinterpret_cast<const float4*>(sroot + j * kDk + 4 * lane);
+            S[0][j] = x4.x;
+            S[1][j] = x4.y;
+            S[2][j] = x4.z;
+            S[3][j] = x4.w;
+        }
+        for (int t = splen[warp] - 1; t >= 0; --t) {
+            const int n = path[t];
+            const float o = delta_step<true>(S, sg, n, lane);
+            if ((lane & 1) == 0 && lane < 2 * kC) a.out[(((size_t)b * N + n) * Hv + h) * dv + c0 + (lane >> 1)] = o;
+        }
+        __syncwarp();
+    }
+}
+
+// The commit: a CTA covers kWarps column slices of one (sequence, head),
+// stages the accepted path's inputs once, and each warp replays the path on
+// its slice in registers and writes it back.
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) delta_commit_kernel(lucetree_delta_args a) {
+    extern __shared__ __align__(16) float sm[];
+    __shared__ int snode[kMaxN];
+    __shared__ int s_bad;
+    const int N = a.N, Hv = a.Hv, dv = a.dv;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int hk = h / (Hv / a.Hk), cb = blockIdx.x * kWarps * kC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool report = blockIdx.x == 0 && h == 0 && threadIdx.x == 0;
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
+    // the state slice first: its loads overlap the path's
+    const int c0 = cb + warp * kC;
+    float* s0 = a.state + ((size_t)b * Hv + h) * kDk * dv + (c0 < dv ? c0 : 0);
+    float S[4][kC];
+    load_state(S, s0, dv, lane);
+    const int n_acc = a.acc_len[b];
+    if (n_acc < 0 || n_acc > N) {
+        if (report) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
+        return;
+    }
+    if (n_acc == 0) return;  // nothing accepted: the committed state stays as it is
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    for (int t = threadIdx.x; t < n_acc; t += kThreads) {
+        const int i = a.acc_nodes[(size_t)b * N + t];
+        const bool ok = i >= 0 && i < N;
+        if (!ok) s_bad = 1;
+        snode[t] = ok ? i : 0;
+    }
+    __syncthreads();
+    if (s_bad) {  // uniform: leave this sequence's state as it was
+        if (report) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
+        return;
+    }
+    Stage sg;
+    sg.k = sm;
+    sg.q = nullptr;
+    sg.v = sg.k + (size_t)N * kDk;
+    sg.vs = kWarps * kC;
+    sg.al = sg.v + (size_t)N * kWarps * kC;
+    sg.be = sg.al + N;
+    sg.qk = nullptr;
+    stage_inputs<BF16, false>(a, sg, snode, n_acc, b, h, hk, cb);
+    __syncthreads();
+    if (c0 >= dv) return;
+    Stage mine = sg;
+    mine.v = sg.v + warp * kC;
+    for (int t = 0; t < n_acc; ++t) delta_step<false>(S, mine, t, lane);
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int j4 = 0; j4 < C; j4 += 4)
+        for (int j4 = 0; j4 < kC; j4 += 4)
             *reinterpret_cast<float4*>(s0 + (size_t)(4 * lane + m) * dv + j4) =
                 make_float4(S[m][j4], S[m][j4 + 1], S[m][j4 + 2], S[m][j4 + 3]);
 }
 
-template <bool BF16, int C>
-cudaError_t launch_tree_c(const lucetree_delta_args& a, cudaStream_t stream) {
-    auto kern = delta_tree_kernel<BF16, C>;
-    const size_t smem = TreeSmem<C>::bytes(a.N);
-    static size_t configured = 0;  // largest dynamic shared memory size set so far
-    if (smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
-    return launch_pdl(kern, dim3(a.dv / C, a.Hv, a.B), dim3(kThreads), smem, stream, a);
+template <typename K>
+cudaError_t set_smem(K kern, size_t smem, size_t& configured) {
+    if (smem <= configured) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) configured = smem;
+    return e;
+}
+
+template <bool BF16>
+cudaError_t launch_tree_t(const lucetree_delta_args& a, cudaStream_t stream) {
+    static size_t configured = 0;
+    const size_t smem = delta_tree_smem_bytes(a.N);
+    cudaError_t e = set_smem(delta_tree_kernel<BF16>, smem, configured);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(delta_tree_kernel<BF16>, dim3(a.dv / kC, a.Hv, a.B), dim3(kThreads), smem, stream, a);
+}
+
+template <bool BF16>
+cudaError_t launch_commit_t(const lucetree_delta_args& a, cudaStream_t stream) {
+    static size_t configured = 0;
+    const size_t smem = stage_bytes(a.N, false, kWarps * kC);
+    cudaError_t e = set_smem(delta_commit_kernel<BF16>, smem, configured);
+    if (e != cudaSuccess) return e;
+    const int per_cta = kWarps * kC;
+    return launch_pdl(delta_commit_kernel<BF16>, dim3((a.dv + per_cta - 1) / per_cta, a.Hv, a.B), dim3(kThreads),
+                      smem, stream, a);
 }
 
 }  // namespace
 
-int delta_tree_columns(int N) { return N <= 26 ? 8 : 4; }
-
-size_t delta_tree_smem_bytes(int N) {
-    return delta_tree_columns(N) == 8 ? TreeSmem<8>::bytes(N) : TreeSmem<4>::bytes(N);
-}
+size_t delta_tree_smem_bytes(int N) { return stage_bytes(N, true, kC); }
 
 cudaError_t launch_delta_tree(const lucetree_delta_args& a, cudaStream_t stream) {
-    const bool bf = a.dtype == LUCETREE_BF16;
-    if (delta_tree_columns(a.N) == 8) return bf ? launch_tree_c<true, 8>(a, stream) : launch_tree_c<false, 8>(a, stream);
-    return bf ? launch_tree_c<true, 4>(a, stream) : launch_tree_c<false, 4>(a, stream);
+    return a.dtype == LUCETREE_BF16 ? launch_tree_t<true>(a, stream) : launch_tree_t<false>(a, stream);
 }
 
 cudaError_t launch_delta_commit(const lucetree_delta_args& a, cudaStream_t stream) {
-    constexpr int C = 8;
-    const dim3 grid(a.dv / C, a.Hv, a.B);
-    if (a.dtype == LUCETREE_BF16) return launch_pdl(delta_commit_kernel<true, C>, grid, dim3(32), 0, stream, a);
-    return launch_pdl(delta_commit_kernel<false, C>, grid, dim3(32), 0, stream, a);
+    return a.dtype == LUCETREE_BF16 ? launch_commit_t<true>(a, stream) : launch_commit_t<false>(a, stream);
 }
 
 }  // namespace lucetree
