@@ -412,6 +412,8 @@ def run_ours(args, cfg):
     if not args.no_delta:
         # the recurrent-state row of hybrid targets, measured apart from the attention step
         line["delta_rule"] = measure_delta(args, dev, stream, rank, with_cpu=world == 1 and not args.no_cpu_baseline)
+    if not args.no_stage:
+        line["stage_pages"] = measure_stage(args, dev, stream, rank)
     print(json.dumps(line), flush=True)
     if dist.is_initialized():
         dist.destroy_process_group()
@@ -569,6 +571,71 @@ def measure_delta(args, dev, stream, rank, with_cpu=True):
     return res
 
 
+def measure_stage(args, dev, stream, rank):
+    """Host-resident cold pages: a quarter of the 128K-token sequence's pages
+    (512 pages of [4 heads][64][256] bf16, K and V: 128 MiB) staged from
+    page-locked host pools into device pool pages, timed with CUDA events on
+    the stream, against a plain pinned host-to-device copy of the same bytes
+    (the link's copy rate, measured here)."""
+    import torch
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    cfg = W.HEADLINE_128K_B22
+    n = (cfg.ctx[0] // W.PAGE) // 4
+    shape = (n, cfg.Hkv, W.PAGE, cfg.D)
+    g = torch.Generator()
+    g.manual_seed(777 + rank)
+    host_k = torch.randint(-32768, 32767, shape, dtype=torch.int16, generator=g).pin_memory()
+    host_v = torch.randint(-32768, 32767, shape, dtype=torch.int16, generator=g).pin_memory()
+    pool_k = torch.empty((n + 64,) + shape[1:], dtype=torch.int16, device=dev)
+    pool_v = torch.empty_like(pool_k)
+    src = torch.arange(n, dtype=torch.int32, device=dev)
+    dst = torch.randperm(n + 64, generator=g)[:n].to(torch.int32).to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    nbytes = 2 * host_k.numel() * 2
+
+    def stage():
+        LT.lucetree_stage_pages(host_k, host_v, src, dst, pool_k, pool_v, st, stream=stream)
+
+    def copy():
+        pool_k[:n].copy_(host_k, non_blocking=True)
+        pool_v[:n].copy_(host_v, non_blocking=True)
+
+    res = {}
+    for name, fn in (("stage", stage), ("h2d_copy", copy)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+            torch.cuda.synchronize(dev)
+            for e0, e1 in evs:
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = float(np.median([e0.elapsed_time(e1) for e0, e1 in evs]))
+    gbs = nbytes / (res["stage"] * 1e-3) / 1e9
+    peak = nbytes / (res["h2d_copy"] * 1e-3) / 1e9
+    return {
+        "workload": f"{n} cold pages of {cfg.Hkv}x{W.PAGE}x{cfg.D} bf16, K and V ({nbytes / 2**20:.0f} MiB), "
+                    "page-locked host pools -> device pool pages",
+        "ms_per_call": res["stage"], "device_status": int(st.item()),
+        "roofline": {"bound": "host link", "kernel": "lucetree_stage_pages", "achieved": gbs, "peak": peak,
+                     "peak_kind": "measured here: pinned host-to-device copy of the same bytes", "unit": "GB/s",
+                     "frac": gbs / peak, "algorithmic_bytes_per_launch": nbytes},
+    }
+
+
+def run_stage_only(args):
+    import torch
+    from speculative_decoding_tree_ddtree_gb300.build import build
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    print(json.dumps({"stage_pages": measure_stage(args, dev, stream, 0)}), flush=True)
+    return 0
+
+
 def run_delta_only(args):
     import torch
     from speculative_decoding_tree_ddtree_gb300.build import build
@@ -605,11 +672,15 @@ def main(argv=None):
                     help="with --lmhead-only: a smaller vocabulary (profiler captures)")
     ap.add_argument("--no-delta", action="store_true", help="skip the recurrent-state (delta rule) measurement")
     ap.add_argument("--delta-only", action="store_true", help="time only the recurrent-state tree pass and commit")
+    ap.add_argument("--no-stage", action="store_true", help="skip the host-resident page staging measurement")
+    ap.add_argument("--stage-only", action="store_true", help="time only the host-resident page staging")
     args = ap.parse_args(argv)
     if args.lmhead_only:
         return run_lmhead_only(args)
     if args.delta_only:
         return run_delta_only(args)
+    if args.stage_only:
+        return run_stage_only(args)
     cfg = W.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)

@@ -23,7 +23,8 @@
  * the logits + lucetree_argmax pair by the lm_head projection with a fused
  * argmax.  For targets with recurrent (gated delta rule) layers,
  * lucetree_delta_tree advances a layer's state along the tree and
- * lucetree_delta_commit keeps the accepted node's state.
+ * lucetree_delta_commit keeps the accepted node's state.  For KV pages kept
+ * in host memory, lucetree_stage_pages brings them into the device pool.
  *
  * Conventions for every call:
  *   - All array pointers are DEVICE pointers unless a parameter says "host".
@@ -296,6 +297,38 @@ LUCETREE_API lucetree_status lucetree_delta_tree(const lucetree_delta_args* args
  * sequence's state is left unchanged).
  */
 LUCETREE_API lucetree_status lucetree_delta_commit(const lucetree_delta_args* args, void* stream);
+
+/* Arguments of lucetree_stage_pages. */
+typedef struct lucetree_stage_args {
+    int Hkv, D;               /* pool geometry: one page of one tensor is [Hkv][64][D] 16-bit values */
+    int n;                    /* pages to stage (0: nothing to do) */
+    const void* host_k;       /* host-resident pools [host_pages][Hkv][64][D]: page-locked HOST memory */
+    const void* host_v;
+    int host_pages;
+    const int32_t* src;       /* [n] host page ids (device array) */
+    const int32_t* dst;       /* [n] device pool page ids to fill (device array), distinct */
+    const int32_t* table_idx; /* [n] flat page-table positions (b * max_pages + page) to set to dst, or NULL */
+    int32_t* page_table;      /* [table_len] (device), required with table_idx */
+    int table_len;
+    void* k_pool;             /* device pools [num_pages][Hkv][64][D] */
+    void* v_pool;
+    int num_pages;
+    uint32_t* status;
+} lucetree_stage_args;
+
+/*
+ * Host-resident cold pages: copy host pages src[i] of both pools into device
+ * pool pages dst[i] and, with table_idx, set page_table[table_idx[i]] =
+ * dst[i], so that lucetree_verify_attn reads them like any resident page.
+ * The pages keep cold 64-token KV chunks in host memory ("Lucebox Hub",
+ * section "KVFlash"); the choice of pages and the free-page bookkeeping are
+ * the caller's.  The kernel reads the host pools directly (zero copy over
+ * the CPU-GPU link); byte-exact.  Host errors: INVALID_ARG (null or
+ * misaligned pointers, host pools that are not page-locked host memory,
+ * sizes).  Device check: BAD_PAGE (an id or table position out of range:
+ * that page is skipped).
+ */
+LUCETREE_API lucetree_status lucetree_stage_pages(const lucetree_stage_args* args, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 LUCETREE_API const char* lucetree_status_string(lucetree_status status);

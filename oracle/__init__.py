@@ -226,3 +226,22 @@ def delta_commit(inp: dict, dtype: int, acc_nodes, acc_len) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle_delta_commit: bad accepted path or sizes")
     return out
+
+
+def stage_pages(host_k, host_v, src, dst, k_pool, v_pool, table_idx=None, page_table=None):
+    """Host-resident KV pages brought back into the device pool.  The pages
+    keep cold 64-token chunks in host memory ("Lucebox Hub", section
+    "KVFlash"); bringing page src[i] back means pool[dst[i]] = host[src[i]]
+    for K and V, and page_table.flat[table_idx[i]] = dst[i] when a table is
+    given.  Returns new (k_pool, v_pool, page_table) arrays; inputs untouched."""
+    kp, vp = np.array(k_pool, copy=True), np.array(v_pool, copy=True)
+    for s_, d_ in zip(np.asarray(src).tolist(), np.asarray(dst).tolist()):
+        kp[d_] = host_k[s_]
+        vp[d_] = host_v[s_]
+    pt = None
+    if page_table is not None:
+        pt = np.array(page_table, copy=True)
+        flat = pt.reshape(-1)
+        for t, d_ in zip(np.asarray(table_idx).tolist(), np.asarray(dst).tolist()):
+            flat[t] = d_
+    return kp, vp, pt

@@ -5,6 +5,7 @@
 #include "internal.cuh"
 #include "lmhead.h"
 #include "delta.h"
+#include "stage.h"
 
 namespace lucetree {
 
@@ -173,6 +174,30 @@ lucetree_status lucetree_delta_commit(const lucetree_delta_args* a, void* stream
     const lucetree_status st = delta_check(a, false);
     if (st != LUCETREE_OK) return st;
     if (launch_delta_commit(*a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LUCETREE_ERR_CUDA;
+    return LUCETREE_OK;
+}
+
+lucetree_status lucetree_stage_pages(const lucetree_stage_args* a, void* stream) {
+    if (!a) return LUCETREE_ERR_INVALID_ARG;
+    if (a->n < 0 || a->Hkv < 1 || a->D < 8 || a->D % 8 != 0 || a->host_pages < 0 || a->num_pages < 1)
+        return LUCETREE_ERR_INVALID_ARG;
+    if (a->n == 0) return LUCETREE_OK;
+    if (!a->host_k || !a->host_v || !a->src || !a->dst || !a->k_pool || !a->v_pool || !a->status)
+        return LUCETREE_ERR_INVALID_ARG;
+    if (a->table_idx && (!a->page_table || a->table_len < 1)) return LUCETREE_ERR_INVALID_ARG;
+    if (!aligned16(a->host_k) || !aligned16(a->host_v) || !aligned16(a->k_pool) || !aligned16(a->v_pool))
+        return LUCETREE_ERR_INVALID_ARG;
+    // the host pools must be page-locked host memory mapped for the device
+    void* hk = nullptr;
+    void* hv = nullptr;
+    if (cudaHostGetDevicePointer(&hk, const_cast<void*>(a->host_k), 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&hv, const_cast<void*>(a->host_v), 0) != cudaSuccess) {
+        cudaGetLastError();  // the failed query leaves a (non-sticky) error behind: clear it
+        return LUCETREE_ERR_INVALID_ARG;
+    }
+    if (!aligned16(hk) || !aligned16(hv)) return LUCETREE_ERR_INVALID_ARG;
+    if (launch_stage_pages(*a, hk, hv, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LUCETREE_ERR_CUDA;
     return LUCETREE_OK;
 }
 

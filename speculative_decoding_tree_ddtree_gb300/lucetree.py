@@ -44,6 +44,7 @@ EXPORTED = (
     "lucetree_lmhead_argmax",
     "lucetree_delta_tree",
     "lucetree_delta_commit",
+    "lucetree_stage_pages",
 )
 
 
@@ -93,6 +94,17 @@ class DeltaArgs(ctypes.Structure):
     ]
 
 
+class StageArgs(ctypes.Structure):
+    _fields_ = [
+        ("Hkv", ctypes.c_int), ("D", ctypes.c_int), ("n", ctypes.c_int),
+        ("host_k", ctypes.c_void_p), ("host_v", ctypes.c_void_p), ("host_pages", ctypes.c_int),
+        ("src", ctypes.c_void_p), ("dst", ctypes.c_void_p), ("table_idx", ctypes.c_void_p),
+        ("page_table", ctypes.c_void_p), ("table_len", ctypes.c_int),
+        ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("num_pages", ctypes.c_int),
+        ("status", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -121,6 +133,7 @@ def load(path: str | None = None):
     lib.lucetree_lmhead_argmax.argtypes = [ctypes.POINTER(LmHeadArgs), P, SZ, P]
     lib.lucetree_delta_tree.argtypes = [ctypes.POINTER(DeltaArgs), P]
     lib.lucetree_delta_commit.argtypes = [ctypes.POINTER(DeltaArgs), P]
+    lib.lucetree_stage_pages.argtypes = [ctypes.POINTER(StageArgs), P]
     for name in EXPORTED:
         if name not in ("lucetree_status_string", "lucetree_abi_version"):
             getattr(lib, name).restype = I
@@ -347,3 +360,29 @@ def lucetree_delta_commit(k, v, alpha, beta, acc_nodes, acc_len, state, status, 
     """state[b][h] <- the recurrence along acc_nodes[b][:acc_len[b]] (in place)."""
     a = _delta_args(None, k, v, alpha, beta, state, status, acc_nodes=acc_nodes, acc_len=acc_len)
     _check(load().lucetree_delta_commit(ctypes.byref(a), _stream(stream)))
+
+
+# ---------------------------------------------------------------- host-resident pages
+
+def _host_ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    if t.is_cuda or not t.is_pinned():
+        raise LucetreeError("host pools must be page-locked host tensors")
+    if not t.is_contiguous():
+        raise LucetreeError("lucetree takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def lucetree_stage_pages(host_k, host_v, src, dst, k_pool, v_pool, status, table_idx=None, page_table=None,
+                         stream=None):
+    """Copy host pages src[i] (page-locked host pools [host_pages][Hkv][64][D])
+    into device pool pages dst[i]; with table_idx, page_table.view(-1)[table_idx[i]] = dst[i]."""
+    a = StageArgs()
+    a.Hkv, a.D = k_pool.shape[1], k_pool.shape[3]
+    a.n = src.numel()
+    a.host_k, a.host_v, a.host_pages = _host_ptr(host_k), _host_ptr(host_v), host_k.shape[0]
+    a.src, a.dst, a.table_idx = _ptr(src), _ptr(dst), _ptr(table_idx)
+    a.page_table = _ptr(page_table)
+    a.table_len = page_table.numel() if page_table is not None else 0
+    a.k_pool, a.v_pool, a.num_pages = _ptr(k_pool), _ptr(v_pool), k_pool.shape[0]
+    a.status = _ptr(status)
+    _check(load().lucetree_stage_pages(ctypes.byref(a), _stream(stream)))

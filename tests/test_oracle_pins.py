@@ -547,3 +547,19 @@ def test_delta_rejects_a_bad_parent():
     inp["parent"] = np.array([[-1, 0, 3, 1]], np.int32)
     with pytest.raises(ValueError):
         oracle.delta_tree(inp, oracle.F16)
+
+
+# ---------------------------------------------------------------- host-resident pages
+
+def test_stage_pages_hand_example():
+    host_k = np.arange(3 * 2, dtype=np.uint16).reshape(3, 2) + 100   # 3 host pages of 2 values
+    host_v = host_k + 1000
+    pool_k = np.zeros((4, 2), np.uint16)
+    pool_v = np.zeros((4, 2), np.uint16)
+    table = np.array([[0, -1, 3], [1, -1, -1]], np.int32)
+    kp, vp, pt = oracle.stage_pages(host_k, host_v, [2, 0], [1, 2], pool_k, pool_v, table_idx=[1, 4],
+                                    page_table=table)
+    assert kp.tolist() == [[0, 0], [104, 105], [100, 101], [0, 0]]
+    assert vp.tolist() == [[0, 0], [1104, 1105], [1100, 1101], [0, 0]]
+    assert pt.tolist() == [[0, 1, 3], [1, 2, -1]]
+    assert pool_k.sum() == 0 and table[0, 1] == -1  # inputs untouched
