@@ -222,6 +222,33 @@ typedef struct lucetree_commit_args {
  */
 LUCETREE_API lucetree_status lucetree_commit(const lucetree_commit_args* args, void* stream);
 
+/* V storage formats of lucetree_verify_attn_vq (K stays in the args' dtype). */
+#define LUCETREE_V_SAME 0 /* V in the args' 16-bit dtype (lucetree_verify_attn) */
+#define LUCETREE_V_INT8 1 /* int8 codes [num_pages][Hkv][64][D], value = code * 2^(e - 127) */
+#define LUCETREE_V_INT4 2 /* int4 codes [num_pages][Hkv][64][D / 2], two per byte, low nibble = even dim */
+
+/*
+ * lucetree_verify_attn with V held quantised: asymmetric K/V storage, K in
+ * the 16-bit dtype and V as small integer codes with one power-of-two scale
+ * per token and head.  The pages list KV quantisation, TQ3_0 and asymmetric
+ * K/V quantisation among the project's components ("Lucebox Hub", section
+ * "Speculative decoding 계층"; pytorch.kr Lucebox introduction, section
+ * "Lucebox의 최적화 구성요소") without defining a format.  This one is the
+ * library's own:
+ *   - a->v_pool holds the codes (format v_format): int8 in [-127, 127], or
+ *     two's-complement int4 in [-7, 7];
+ *   - v_exp [num_pages][Hkv][64] holds one exponent byte e per token and KV
+ *     head (16-byte aligned); the value is code * 2^(e - 127), e = 0 means 0.
+ * Every such value with e in [103, 135] is exact in fp16, which is the
+ * on-chip type of the PV product; elsewhere precision or range is lost.  The
+ * tree's own V (a->v_tree) stays in the 16-bit dtype.  Head dim 256 only.
+ * Errors as lucetree_verify_attn, plus UNSUPPORTED (v_format, D != 256) and
+ * INVALID_ARG (v_exp null or misaligned).
+ */
+LUCETREE_API lucetree_status lucetree_verify_attn_vq(const lucetree_attn_args* args, int v_format,
+                                                     const uint8_t* v_exp, void* workspace, size_t workspace_bytes,
+                                                     void* stream);
+
 /* Arguments of lucetree_lmhead_argmax. */
 typedef struct lucetree_lmhead_args {
     int dtype;             /* LUCETREE_F16 / LUCETREE_BF16, both operands */

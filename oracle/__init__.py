@@ -245,3 +245,39 @@ def stage_pages(host_k, host_v, src, dst, k_pool, v_pool, table_idx=None, page_t
         for t, d_ in zip(np.asarray(table_idx).tolist(), np.asarray(dst).tolist()):
             flat[t] = d_
     return kp, vp, pt
+
+
+V_INT8, V_INT4 = 1, 2
+
+
+def dequant_v(codes, v_exp, v_format: int, dtype: int) -> np.ndarray:
+    """Quantised V of the asymmetric K/V storage (the pages list K/V
+    quantisation and asymmetric K/V quantisation without a format; this is
+    the library's own): value = code * 2^(e - 127) with one exponent byte e
+    per token and head (e = 0: zero).  codes: uint8 [..][64][D] (int8, two's
+    complement) or [..][64][D/2] (int4 pairs, low nibble = even dim);
+    v_exp: uint8 [..][64].  Returns the values as 16-bit storage bits of dtype;
+    every value is exact there (7 significant bits at most), which is checked."""
+    codes = np.asarray(codes, np.uint8)
+    if v_format == V_INT8:
+        q = codes.view(np.int8).astype(np.float64)
+    elif v_format == V_INT4:
+        lo = (codes & 0x0F).astype(np.int64)
+        hi = (codes >> 4).astype(np.int64)
+        lo = np.where(lo >= 8, lo - 16, lo)
+        hi = np.where(hi >= 8, hi - 16, hi)
+        q = np.stack([lo, hi], axis=-1).reshape(codes.shape[:-1] + (2 * codes.shape[-1],)).astype(np.float64)
+    else:
+        raise ValueError(v_format)
+    e = np.asarray(v_exp, np.int64)
+    scale = np.where(e == 0, 0.0, np.ldexp(1.0, e - 127))
+    val = q * scale[..., None]
+    if dtype == BF16:
+        bits32 = val.astype(np.float32).view(np.uint32)
+        if np.any(bits32 & 0xFFFF) or not np.array_equal(bits32.view(np.float32).astype(np.float64), val):
+            raise ValueError("value not exact in bf16")
+        return (bits32 >> 16).astype(np.uint16)
+    h = val.astype(np.float16)
+    if not np.array_equal(h.astype(np.float64), val):
+        raise ValueError("value not exact in fp16")
+    return h.view(np.uint16)

@@ -69,11 +69,33 @@ cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
+    // quantised V: codes as bytes [rows][D or D/2] (one 64-token page x 128 dims per box, no
+    // swizzle: the softmax warps expand them), exponents [num_pages * Hkv][64] one page per box
+    const int vq = L.v_format == LUCETREE_V_INT8 ? 1 : (L.v_format == LUCETREE_V_INT4 ? 2 : 0);
+    CUtensorMap tve = tv;
+    if (vq) {
+        const cuuint64_t row_bytes = vq == 1 ? (cuuint64_t)a.D : (cuuint64_t)a.D / 2;
+        const cuuint64_t c_dims[2] = {row_bytes, (cuuint64_t)a.num_pages * a.Hkv * kPage};
+        const cuuint64_t c_strides[1] = {row_bytes};
+        const cuuint32_t c_box[2] = {vq == 1 ? 128u : 64u, (cuuint32_t)kPage};
+        if (enc(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.v_pool), c_dims, c_strides, c_box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        const cuuint64_t e_dims[2] = {(cuuint64_t)kPage, (cuuint64_t)a.num_pages * a.Hkv};
+        const cuuint64_t e_strides[1] = {(cuuint64_t)kPage};
+        const cuuint32_t e_box[2] = {(cuuint32_t)kPage, 1};
+        if (enc(&tve, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(L.v_exp), e_dims, e_strides, e_box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+
     const int rgp = (p.rg.RG + 15) / 16 * 16;
     if (a.dtype == LUCETREE_BF16)
-        return a.D == 256 ? launch_prefix_tc_bf16_256(rgp, tk, tv, tq, L, stream)
+        return a.D == 256 ? launch_prefix_tc_bf16_256(rgp, vq, tk, tv, tq, tve, L, stream)
                           : launch_prefix_tc_bf16_128(rgp, tk, tv, tq, L, stream);
-    return a.D == 256 ? launch_prefix_tc_f16_256(rgp, tk, tv, tq, L, stream)
+    return a.D == 256 ? launch_prefix_tc_f16_256(rgp, vq, tk, tv, tq, tve, L, stream)
                       : launch_prefix_tc_f16_128(rgp, tk, tv, tq, L, stream);
 }
 

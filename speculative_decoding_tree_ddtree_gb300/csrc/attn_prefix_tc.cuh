@@ -91,7 +91,7 @@ struct Layout {
     static constexpr uint32_t kColO0 = RGP;             // O^T, d 0..127
     static constexpr uint32_t kColO1 = 2 * RGP;         // O^T, d 128..255
     static_assert(RGP + kDh * RGP <= (int)kTmemCols, "TMEM columns");
-    static constexpr int kMiscBytes = 4096;
+    static constexpr int kMiscBytes = 5632;
     static constexpr int kRaw = (kSmemLimit - 1024 - kQBytes - kPBytes - kMiscBytes) / kChunkBytes;
     static constexpr int kNS = kRaw > kMaxSlots ? kMaxSlots : kRaw;
     static constexpr int kQOff = 0;
@@ -106,6 +106,9 @@ struct Layout {
 };
 
 struct Misc {
+    // quantised V: the per-token exponents of V chunk n at [n % kMaxSlots]; each row is a
+    // TMA destination, which must be 128-byte aligned (the misc region is 1024-aligned)
+    alignas(128) uint8_t vexp[kMaxSlots][128];
     alignas(16) float m_ref[kRowsMax];
     alignas(16) float alpha[kRowsMax];
     alignas(16) float col_red[4][kRowsMax];
@@ -122,7 +125,19 @@ struct Misc {
     uint32_t tmem_base;
     int abort_flag;
 };
-static_assert(sizeof(Misc) <= 4096, "misc region");
+static_assert(sizeof(Misc) <= 5632, "misc region");
+static_assert(offsetof(Misc, vexp) == 0 && sizeof(Misc::vexp[0]) % 128 == 0, "128-byte aligned TMA destinations");
+
+// Quantised V (VQ = 1: int8 codes, VQ = 2: int4 codes two per byte, low
+// nibble first), value = code * 2^(e - 127) with one exponent byte e per
+// token.  A V chunk's codes ([64 keys][128 dims]) land at the back of its
+// 16 KB slot and are expanded to the fp16 operand over the whole slot.
+template <int VQ>
+struct VCodes {
+    static constexpr int kRowBytes = VQ == 1 ? 128 : 64;       // one key's 128 dims
+    static constexpr int kBytes = kRowBytes * kPage;             // 8 KB / 4 KB
+    static constexpr int kOff = kChunkBytes - kBytes;
+};
 
 // A key segment's share of this CTA's tiles.  Tile indices are 32-bit: the
 // host refuses shapes whose flat tile count reaches 2^31.
@@ -240,10 +255,11 @@ __device__ __forceinline__ void set_abort(Misc* ms, uint32_t* status) {
 }
 __device__ __forceinline__ bool aborted(Misc* ms) { return *(volatile int*)&ms->abort_flag != 0; }
 
-template <int D, bool BF16, int RGP>
+template <int D, bool BF16, int RGP, int VQ>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_q, const AttnLaunch L) {
+                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_ve,
+                     const AttnLaunch L) {
     using Lay = Layout<D, RGP>;
     constexpr int kChunks = Lay::kChunks;
     constexpr int kNch = Lay::kNch;
@@ -313,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_q);
+        if (VQ) prefetch_tensormap(&tm_ve);
     }
     tc_fence_before();
     __syncthreads();
@@ -341,14 +358,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive(bar);  // this fill's phase of full[slot]; the data signal is vfull
                         bar = &ms->vfull[vchunk % kMaxSlots];
                     }
-                    mbar_arrive_expect_tx(bar, kChunkBytes);
-                    if (is_v) {
+                    if (VQ && is_v) {
+                        // codes of [64 keys of page c & 1][dims 128 * (c >> 1) .. +127] and the
+                        // page's per-token exponents
+                        const int row = (c & 1) ? row1 : row0;
+                        mbar_arrive_expect_tx(bar, VCodes<VQ>::kBytes + kPage);
+                        tma_load_2d_hint(dst + VCodes<VQ>::kOff, &tm_v, VCodes<VQ>::kRowBytes * (c >> 1), row, bar,
+                                         pol_stream);
+                        tma_load_2d_hint(ms->vexp[vchunk % kMaxSlots], &tm_ve, 0, row / kPage, bar, pol_stream);
+                    } else if (is_v) {
                         // [64 keys of page c & 1][dims 128 * (c >> 1) .. +127]
+                        mbar_arrive_expect_tx(bar, kChunkBytes);
                         const int row = (c & 1) ? row1 : row0, x = 128 * (c >> 1);
                         tma_load_2d_hint(dst, &tm_v, x, row, bar, pol_stream);
                         tma_load_2d_hint(dst + 8192, &tm_v, x + 64, row, bar, pol_stream);
                     } else {
                         // [128 keys: page 0 then page 1][dims 64 * c .. +63]
+                        mbar_arrive_expect_tx(bar, kChunkBytes);
                         tma_load_2d_hint(dst, &tm_k, 64 * c, row0, bar, pol_stream);
                         tma_load_2d_hint(dst + 8192, &tm_k, 64 * c, row1, bar, pol_stream);
                     }
@@ -718,13 +744,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t vbase = v_operand(j, n_tiles) * kChunks;
                     for (int c = 0; c < kChunks; ++c) {
                         const uint32_t vn = j * kChunks + c;
-                        if (!wait_all(&ms->vfull[vn % kMaxSlots], (vn / kMaxSlots) & 1)) {
+                        const bool landed = wait_all(&ms->vfull[vn % kMaxSlots], (vn / kMaxSlots) & 1);
+                        if (!VQ && !landed) {
                             bad = true;
                             break;
                         }
                         uint4* base = reinterpret_cast<uint4*>(sSlots + ((vbase + c) % kNS) * kChunkBytes);
                         const int nv = nvalid - 64 * (c & 1);  // valid keys of this chunk's page
-                        if (BF16 || nv < 64) {
+                        if constexpr (VQ != 0) {
+                            // output unit u: box u / 512 (dims 64 * box ..), key row r, 16-byte unit
+                            // p of the swizzled row = logical 8-dim group p ^ (r % 8); its codes
+                            // are read for every unit first, since the fp16 output overwrites them
+                            const uint8_t* codes = reinterpret_cast<const uint8_t*>(base) + VCodes<VQ>::kOff;
+                            const uint8_t* ex = ms->vexp[vn % kMaxSlots];
+                            uint2 cw[3];
+                            float sc[3];
+#pragma unroll
+                            for (int i = 0; i < 3; ++i) {
+                                const int u = st + kSoftmaxThreads * i;
+                                cw[i] = make_uint2(0, 0);
+                                sc[i] = 0.f;
+                                if (landed && u < 1024) {
+                                    const int r = (u & 511) >> 3, d0 = 64 * (u >> 9) + 8 * ((u & 7) ^ (r & 7));
+                                    if (r < nv) {
+                                        if constexpr (VQ == 1)
+                                            cw[i] = *reinterpret_cast<const uint2*>(codes + r * 128 + d0);
+                                        else
+                                            cw[i].x = *reinterpret_cast<const uint32_t*>(codes + r * 64 + d0 / 2);
+                                        sc[i] = __uint_as_float((uint32_t)ex[r] << 23);  // 2^(e - 127)
+                                    }
+                                }
+                            }
+                            // every softmax warp arrives, also after a timed-out wait: the OR
+                            // tells all of them to leave together
+                            if (bar_sync_or(1, kSoftmaxThreads, !landed)) {
+                                bad = true;
+                                break;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 3; ++i) {
+                                const int u = st + kSoftmaxThreads * i;
+                                if (u < 1024) {
+                                    float f[8];
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        int q;
+                                        if constexpr (VQ == 1)
+                                            q = (int)(int8_t)(((e < 4 ? cw[i].x : cw[i].y) >> (8 * (e & 3))) & 0xFFu);
+                                        else
+                                            q = ((int)(cw[i].x << (28 - 4 * e))) >> 28;
+                                        f[e] = (float)q * sc[i];
+                                    }
+                                    base[u] = make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]),
+                                                         pack_half2(f[4], f[5]), pack_half2(f[6], f[7]));
+                                }
+                            }
+                        } else if (BF16 || nv < 64) {
 #pragma unroll
                             for (int i = 0; i < 3; ++i) {
                                 const int u = st + kSoftmaxThreads * i;
@@ -809,46 +884,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, bool BF16, int RGP>
-cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq, const AttnLaunch& L,
-                       cudaStream_t stream) {
+template <int D, bool BF16, int RGP, int VQ>
+cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq, const CUtensorMap& tve,
+                       const AttnLaunch& L, cudaStream_t stream) {
     using Lay = Layout<D, RGP>;
-    auto kern = prefix_tc_kernel<D, BF16, RGP>;
+    auto kern = prefix_tc_kernel<D, BF16, RGP, VQ>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    return launch_pdl(kern, dim3(grid_ctas(L.plan)), dim3(kThreads), Lay::kBytes, stream, tk, tv, tq, L);
+    return launch_pdl(kern, dim3(grid_ctas(L.plan)), dim3(kThreads), Lay::kBytes, stream, tk, tv, tq, tve, L);
 }
 
-template <int D, bool BF16>
+// tve: the per-token exponents of quantised V (VQ != 0); unused otherwise
+template <int D, bool BF16, int VQ = 0>
 cudaError_t launch_rgp(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                       const AttnLaunch& L, cudaStream_t stream) {
+                       const CUtensorMap& tve, const AttnLaunch& L, cudaStream_t stream) {
     static_assert(kRowsMax == 144, "one instantiation per padded row count up to kRowsMax");
     switch (rgp) {
-        case 16: return launch_one<D, BF16, 16>(tk, tv, tq, L, stream);
-        case 32: return launch_one<D, BF16, 32>(tk, tv, tq, L, stream);
-        case 48: return launch_one<D, BF16, 48>(tk, tv, tq, L, stream);
-        case 64: return launch_one<D, BF16, 64>(tk, tv, tq, L, stream);
-        case 80: return launch_one<D, BF16, 80>(tk, tv, tq, L, stream);
-        case 96: return launch_one<D, BF16, 96>(tk, tv, tq, L, stream);
-        case 112: return launch_one<D, BF16, 112>(tk, tv, tq, L, stream);
-        case 128: return launch_one<D, BF16, 128>(tk, tv, tq, L, stream);
-        case 144: return launch_one<D, BF16, 144>(tk, tv, tq, L, stream);
+        case 16: return launch_one<D, BF16, 16, VQ>(tk, tv, tq, tve, L, stream);
+        case 32: return launch_one<D, BF16, 32, VQ>(tk, tv, tq, tve, L, stream);
+        case 48: return launch_one<D, BF16, 48, VQ>(tk, tv, tq, tve, L, stream);
+        case 64: return launch_one<D, BF16, 64, VQ>(tk, tv, tq, tve, L, stream);
+        case 80: return launch_one<D, BF16, 80, VQ>(tk, tv, tq, tve, L, stream);
+        case 96: return launch_one<D, BF16, 96, VQ>(tk, tv, tq, tve, L, stream);
+        case 112: return launch_one<D, BF16, 112, VQ>(tk, tv, tq, tve, L, stream);
+        case 128: return launch_one<D, BF16, 128, VQ>(tk, tv, tq, tve, L, stream);
+        case 144: return launch_one<D, BF16, 144, VQ>(tk, tv, tq, tve, L, stream);
     }
     return cudaErrorInvalidValue;
 }
 
 }  // namespace prefix_tc
 
-cudaError_t launch_prefix_tc_bf16_256(int rgp, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                      const AttnLaunch&, cudaStream_t);
+// tve: the exponent map of quantised V; vq: 0 = 16-bit V, 1 = int8 codes, 2 = int4 codes (head dim 256)
+cudaError_t launch_prefix_tc_bf16_256(int rgp, int vq, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                      const CUtensorMap&, const AttnLaunch&, cudaStream_t);
 cudaError_t launch_prefix_tc_bf16_128(int rgp, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                       const AttnLaunch&, cudaStream_t);
-cudaError_t launch_prefix_tc_f16_256(int rgp, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                     const AttnLaunch&, cudaStream_t);
+cudaError_t launch_prefix_tc_f16_256(int rgp, int vq, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                     const CUtensorMap&, const AttnLaunch&, cudaStream_t);
 cudaError_t launch_prefix_tc_f16_128(int rgp, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                      const AttnLaunch&, cudaStream_t);
 

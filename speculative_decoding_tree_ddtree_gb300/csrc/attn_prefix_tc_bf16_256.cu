@@ -1,11 +1,11 @@
-// Instantiations of the tensor-core prefix kernel for bf16 operands, head dim 256.
+// Instantiations of the tensor-core prefix kernel for bf16 operands, head dim 256, 16-bit V.
 #include "attn_prefix_tc.cuh"
 
 namespace lucetree {
 
-cudaError_t launch_prefix_tc_bf16_256(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                                   const AttnLaunch& L, cudaStream_t stream) {
-    return prefix_tc::launch_rgp<256, true>(rgp, tk, tv, tq, L, stream);
+cudaError_t launch_prefix_tc_bf16_256_v16(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                                          const AttnLaunch& L, cudaStream_t stream) {
+    return prefix_tc::launch_rgp<256, true>(rgp, tk, tv, tq, tv, L, stream);
 }
 
 }  // namespace lucetree

@@ -1,0 +1,18 @@
+// Instantiations of the tensor-core prefix kernel for f16 operands, head dim 256, with V held as
+// int8 or int4 codes and per-token power-of-two exponents; dispatch over the V format.
+#include "attn_prefix_tc.cuh"
+
+namespace lucetree {
+
+cudaError_t launch_prefix_tc_f16_256_v16(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                                         const AttnLaunch& L, cudaStream_t stream);
+
+cudaError_t launch_prefix_tc_f16_256(int rgp, int vq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                     const CUtensorMap& tq, const CUtensorMap& tve, const AttnLaunch& L,
+                                     cudaStream_t stream) {
+    if (vq == 1) return prefix_tc::launch_rgp<256, false, 1>(rgp, tk, tv, tq, tve, L, stream);
+    if (vq == 2) return prefix_tc::launch_rgp<256, false, 2>(rgp, tk, tv, tq, tve, L, stream);
+    return launch_prefix_tc_f16_256_v16(rgp, tk, tv, tq, L, stream);
+}
+
+}  // namespace lucetree

@@ -178,7 +178,9 @@ struct AttnLaunch {
     lucetree_attn_args a;
     PlanDims plan;
     float* ws;
-    float scale_log2;  // scale * log2(e)
+    float scale_log2;    // scale * log2(e)
+    int v_format;        // LUCETREE_V_SAME (v_pool in dtype), LUCETREE_V_INT8 or LUCETREE_V_INT4 (v_pool holds codes)
+    const uint8_t* v_exp;  // per-token exponents of quantised V [num_pages][Hkv][64]
 };
 
 int prefix_grid_ctas(int device);  // persistent grid size of the prefix kernel

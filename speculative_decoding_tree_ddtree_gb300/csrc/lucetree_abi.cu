@@ -66,8 +66,24 @@ lucetree_status lucetree_verify_attn_workspace(int B, int N, int Hq, int Hkv, in
     return LUCETREE_OK;
 }
 
+static lucetree_status verify_attn_impl(const lucetree_attn_args* a, int v_format, const uint8_t* v_exp,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
 lucetree_status lucetree_verify_attn(const lucetree_attn_args* a, void* workspace, size_t workspace_bytes,
                                      void* stream) {
+    return verify_attn_impl(a, LUCETREE_V_SAME, nullptr, workspace, workspace_bytes, stream);
+}
+
+lucetree_status lucetree_verify_attn_vq(const lucetree_attn_args* a, int v_format, const uint8_t* v_exp,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (v_format != LUCETREE_V_INT8 && v_format != LUCETREE_V_INT4) return LUCETREE_ERR_UNSUPPORTED;
+    if (!v_exp || !aligned16(v_exp)) return LUCETREE_ERR_INVALID_ARG;
+    if (a && a->D != 256) return LUCETREE_ERR_UNSUPPORTED;
+    return verify_attn_impl(a, v_format, v_exp, workspace, workspace_bytes, stream);
+}
+
+static lucetree_status verify_attn_impl(const lucetree_attn_args* a, int v_format, const uint8_t* v_exp,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
     if (!a) return LUCETREE_ERR_INVALID_ARG;
     if (a->dtype != LUCETREE_F16 && a->dtype != LUCETREE_BF16) return LUCETREE_ERR_UNSUPPORTED;
     if (a->page_size != LUCETREE_PAGE_SIZE) return LUCETREE_ERR_UNSUPPORTED;
@@ -90,6 +106,8 @@ lucetree_status lucetree_verify_attn(const lucetree_attn_args* a, void* workspac
         return LUCETREE_ERR_WORKSPACE;
     L.ws = reinterpret_cast<float*>(workspace);
     L.scale_log2 = a->scale * kLog2e;
+    L.v_format = v_format;
+    L.v_exp = v_exp;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_attn_prefix(L, s) != cudaSuccess) return LUCETREE_ERR_CUDA;
     if (launch_attn_merge(L, s) != cudaSuccess) return LUCETREE_ERR_CUDA;

@@ -45,6 +45,7 @@ EXPORTED = (
     "lucetree_delta_tree",
     "lucetree_delta_commit",
     "lucetree_stage_pages",
+    "lucetree_verify_attn_vq",
 )
 
 
@@ -134,6 +135,7 @@ def load(path: str | None = None):
     lib.lucetree_delta_tree.argtypes = [ctypes.POINTER(DeltaArgs), P]
     lib.lucetree_delta_commit.argtypes = [ctypes.POINTER(DeltaArgs), P]
     lib.lucetree_stage_pages.argtypes = [ctypes.POINTER(StageArgs), P]
+    lib.lucetree_verify_attn_vq.argtypes = [ctypes.POINTER(AttnArgs), I, P, P, SZ, P]
     for name in EXPORTED:
         if name not in ("lucetree_status_string", "lucetree_abi_version"):
             getattr(lib, name).restype = I
@@ -180,12 +182,7 @@ def lucetree_verify_attn_workspace(B: int, N: int, Hq: int, Hkv: int, D: int) ->
     return int(n.value)
 
 
-def lucetree_verify_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status,
-                         workspace, lse=None, scale: float | None = None, stream=None):
-    """q [B][N][Hq][D]; pools [P][Hkv][64][D]; page_table int32 [B][max_pages];
-    ctx_len int32 [B]; tree K/V [B][N][Hkv][D]; anc_mask int64 [B][N];
-    out fp32 [B][N][Hq][D]; status int32 [1]; workspace uint8 (see
-    lucetree_verify_attn_workspace)."""
+def _attn_args(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale):
     B, N, Hq, D = q.shape
     Hkv = k_pool.shape[1]
     a = AttnArgs()
@@ -198,8 +195,31 @@ def lucetree_verify_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree,
     a.page_table, a.max_pages_per_seq = _ptr(page_table), page_table.shape[1]
     a.ctx_len, a.k_tree, a.v_tree, a.anc_mask = _ptr(ctx_len), _ptr(k_tree), _ptr(v_tree), _ptr(anc_mask)
     a.out, a.lse, a.status = _ptr(out), _ptr(lse), _ptr(status)
+    return a
+
+
+def lucetree_verify_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status,
+                         workspace, lse=None, scale: float | None = None, stream=None):
+    """q [B][N][Hq][D]; pools [P][Hkv][64][D]; page_table int32 [B][max_pages];
+    ctx_len int32 [B]; tree K/V [B][N][Hkv][D]; anc_mask int64 [B][N];
+    out fp32 [B][N][Hq][D]; status int32 [1]; workspace uint8 (see
+    lucetree_verify_attn_workspace)."""
+    a = _attn_args(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale)
     _check(load().lucetree_verify_attn(ctypes.byref(a), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                        _stream(stream)))
+
+
+LUCETREE_V_INT8, LUCETREE_V_INT4 = 1, 2
+
+
+def lucetree_verify_attn_vq(q, k_pool, v_codes, v_exp, v_format, page_table, ctx_len, k_tree, v_tree, anc_mask, out,
+                            status, workspace, lse=None, scale: float | None = None, stream=None):
+    """As lucetree_verify_attn with V stored quantised: v_codes uint8 [P][Hkv][64][D]
+    (int8 codes) or [P][Hkv][64][D/2] (int4 codes, low nibble first), v_exp uint8
+    [P][Hkv][64] (value = code * 2^(e - 127))."""
+    a = _attn_args(q, k_pool, v_codes, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale)
+    _check(load().lucetree_verify_attn_vq(ctypes.byref(a), int(v_format), _ptr(v_exp), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def lucetree_build_anc_mask(parent, anc, status, stream=None):

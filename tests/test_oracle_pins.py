@@ -563,3 +563,28 @@ def test_stage_pages_hand_example():
     assert vp.tolist() == [[0, 0], [1104, 1105], [1100, 1101], [0, 0]]
     assert pt.tolist() == [[0, 1, 3], [1, 2, -1]]
     assert pool_k.sum() == 0 and table[0, 1] == -1  # inputs untouched
+
+
+# ---------------------------------------------------------------- quantised V storage
+
+def test_dequant_v_hand_examples():
+    # int8: codes 3, -5, 127 at exponents 127 (x1), 126 (x1/2), 0 (zero)
+    codes = np.array([[3, 0xFB], [127, 1], [7, 7]], np.uint8)[None]     # [1][3 tokens][2 dims]
+    exps = np.array([[127, 126, 0]], np.uint8)
+    got = oracle.dequant_v(codes, exps, oracle.V_INT8, oracle.F16).view(np.float16).astype(float)
+    assert got.tolist() == [[[3.0, -5.0], [63.5, 0.5], [0.0, 0.0]]]
+    # int4: byte 0x9F holds even dim 0xF = -1 and odd dim 0x9 = -7; byte 0x71 holds 1 and 7
+    codes4 = np.array([[[0x9F, 0x71]]], np.uint8)                      # [1][1 token][4 dims]
+    got4 = oracle.dequant_v(codes4, np.array([[129]], np.uint8), oracle.V_INT4, oracle.BF16)
+    vals = (got4.astype(np.uint32) << 16).view(np.float32).astype(float)
+    assert vals.tolist() == [[[-4.0, -28.0, 4.0, 28.0]]]
+
+
+def test_dequant_v_is_exact_over_the_code_and_exponent_range():
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 256, size=(2, 64, 16)).astype(np.uint8)
+    exps = rng.integers(103, 136, size=(2, 64)).astype(np.uint8)
+    for dt in (oracle.F16, oracle.BF16):
+        oracle.dequant_v(codes, exps, oracle.V_INT8, dt)  # raises if any value were rounded
+    with pytest.raises(ValueError):  # 127 * 2^9 = 65024 is still fp16, 127 * 2^10 is not
+        oracle.dequant_v(np.full((1, 1, 2), 127, np.uint8), np.array([[137]], np.uint8), oracle.V_INT8, oracle.F16)

@@ -382,3 +382,29 @@ def generate_delta(cfg: DeltaConfig, seed: int = 0) -> dict:
     parent = np.stack([random_parents(rng, cfg.N, cfg.tree, cfg.branch_cap) for _ in range(cfg.B)]).astype(np.int32)
     state = (0.1 * rng.standard_normal((cfg.B, cfg.Hv, cfg.dk, cfg.dv), dtype=np.float32)).astype(np.float32)
     return dict(q=q, k=k, v=v, alpha=alpha, beta=beta, parent=parent, state=state)
+
+
+# ----------------------------------------------------------------------------- quantised V storage
+
+V_INT8, V_INT4 = 1, 2
+
+
+def generate_vq(cfg: VerifyConfig, v_format: int, seed: int = 0) -> dict:
+    """Quantised V pool for ``cfg``'s page geometry, drawn directly as storage:
+    v_codes uint8 [num_pages][Hkv][64][D] (int8 codes uniform in [-127, 127]) or
+    [num_pages][Hkv][64][D/2] (int4 codes uniform in [-7, 7], two per byte, low
+    nibble first), v_exp uint8 [num_pages][Hkv][64] uniform in [118, 124]
+    (scales 2^-9 .. 2^-3).  Use with generate(cfg, seed) for the other inputs."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, _name_key(cfg.name), 0x5651]))
+    need = [pages_needed(L, cfg.N) for L in cfg.ctx]
+    num_pages = sum(need) + cfg.spare_pages
+    shape = (num_pages, cfg.Hkv, PAGE, cfg.D)
+    if v_format == V_INT8:
+        codes = rng.integers(-127, 128, size=shape).astype(np.int8).view(np.uint8)
+    elif v_format == V_INT4:
+        q = rng.integers(-7, 8, size=shape).astype(np.int64) & 0x0F
+        codes = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+    else:
+        raise ValueError(v_format)
+    v_exp = rng.integers(118, 125, size=shape[:3]).astype(np.uint8)
+    return dict(v_codes=codes, v_exp=v_exp)
