@@ -414,6 +414,8 @@ def run_ours(args, cfg):
         line["delta_rule"] = measure_delta(args, dev, stream, rank, with_cpu=world == 1 and not args.no_cpu_baseline)
     if not args.no_stage:
         line["stage_pages"] = measure_stage(args, dev, stream, rank)
+    if not args.no_vq and cfg.D == 256:
+        line["quantised_v"] = measure_vq(args, dev, stream, rank, d, step, cfg)
     print(json.dumps(line), flush=True)
     if dist.is_initialized():
         dist.destroy_process_group()
@@ -571,6 +573,48 @@ def measure_delta(args, dev, stream, rank, with_cpu=True):
     return res
 
 
+def measure_vq(args, dev, stream, rank, d, step, cfg):
+    """The headline attention call with V stored quantised (int8 and int4 codes,
+    one power-of-two exponent per token and head; K stays bf16), timed with
+    CUDA events on the stream over the same resident inputs as the step."""
+    import torch
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    res = {}
+    L = sum(cfg.ctx)
+    peak, peak_kind = peak_hbm()
+    for name, fmt, vbytes in (("int8", W.V_INT8, 1.0), ("int4", W.V_INT4, 0.5)):
+        vq = W.generate_vq(cfg, fmt, seed=rank)
+        codes = torch.from_numpy(vq["v_codes"]).to(dev)
+        vexp = torch.from_numpy(vq["v_exp"]).to(dev)
+
+        def call():
+            LT.lucetree_verify_attn_vq(d["q"], d["k_pool"], codes, vexp, fmt, d["page_table"], d["ctx_len"],
+                                       d["k_tree"], d["v_tree"], step.anc, step.out, step.status, step.ws_attn,
+                                       stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                call()
+            n = max(20, min(200, args.steps // 10))
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            torch.cuda.synchronize(dev)
+            for e0, e1 in evs:
+                e0.record(stream)
+                call()
+                e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+        nbytes = int(L * cfg.Hkv * cfg.D * (2 + vbytes) + L * cfg.Hkv
+                     + cfg.B * cfg.N * cfg.Hq * cfg.D * 2 + cfg.B * cfg.N * cfg.Hq * cfg.D * 4 + 4 * L // 64)
+        res[name] = {"ms_per_call": ms, "device_status": int(step.status.item()),
+                     "algorithmic_bytes_per_launch": nbytes, "achieved_GBps": nbytes / (ms * 1e-3) / 1e9,
+                     "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
+                     "kv_bytes_per_token": cfg.Hkv * cfg.D * (2 + vbytes) + cfg.Hkv}
+    res["workload"] = f"{cfg.name} attention call, K bf16, V as int8 / int4 codes with per-token exponents"
+    res["peak"], res["peak_kind"] = peak, peak_kind
+    return res
+
+
 def measure_stage(args, dev, stream, rank):
     """Host-resident cold pages: a quarter of the 128K-token sequence's pages
     (512 pages of [4 heads][64][256] bf16, K and V: 128 MiB) staged from
@@ -673,6 +717,7 @@ def main(argv=None):
     ap.add_argument("--no-delta", action="store_true", help="skip the recurrent-state (delta rule) measurement")
     ap.add_argument("--delta-only", action="store_true", help="time only the recurrent-state tree pass and commit")
     ap.add_argument("--no-stage", action="store_true", help="skip the host-resident page staging measurement")
+    ap.add_argument("--no-vq", action="store_true", help="skip the quantised-V attention measurement")
     ap.add_argument("--stage-only", action="store_true", help="time only the host-resident page staging")
     args = ap.parse_args(argv)
     if args.lmhead_only:
