@@ -282,17 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int R_seg = (min(p.N, i0 + p.rg.NPG) - i0) * p.G;
     const int RG = p.rg.RG;
 
-    // inputs may come from the previous kernel on the stream (programmatic
-    // dependent launch): wait for it, then let the merge kernel start its
-    // blocks as SMs free up (it waits for this grid before reading partials)
-    pdl_wait();
-    if (threadIdx.x == 0) pdl_trigger();
-    const long long nT = total_tiles(p, a.ctx_len);
-    const int t0 = nT ? (int)cta_begin(cta, nT, p.Cg) : 0, t1 = nT ? (int)cta_begin(cta + 1, nT, p.Cg) : 0;
-    if (t0 >= t1) return;  // uniform across the CTA
-    const uint32_t n_tiles = (uint32_t)(t1 - t0);
-
     // ---------------------------------------------------------------- set-up
+    // (no global memory is read here, so it overlaps the previous kernel's
+    // tail under programmatic dependent launch)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNS; ++i) {
             mbar_init(&ms->full[i], 1);
@@ -335,6 +327,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
+
+    // inputs may come from the previous kernel on the stream: wait for it, then
+    // let the merge kernel start its blocks as SMs free up (it waits for this
+    // grid before reading partials)
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
+    const long long nT = total_tiles(p, a.ctx_len);
+    const int t0 = nT ? (int)cta_begin(cta, nT, p.Cg) : 0, t1 = nT ? (int)cta_begin(cta + 1, nT, p.Cg) : 0;
+    if (t0 >= t1) {  // uniform across the CTA: nothing to do but give TMEM back
+        if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
+    const uint32_t n_tiles = (uint32_t)(t1 - t0);
 
     if (warp < 4) {
     regs_dec<kRegsIssue>();
