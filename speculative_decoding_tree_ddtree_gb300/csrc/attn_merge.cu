@@ -7,11 +7,12 @@
 // lse = ln(sum) + max.  Maxima are kept in the log2 domain
 // (scores pre-multiplied by log2 e), so every rescale is one exp2.
 //
-// The partials are independent.  Warp w folds partials w, w + 8, ... into its
-// own running (max, sum, output slice), kB at a time: all kB rows (and their
-// maxima and sums) are loaded before any is used, so a block of about 40
-// partials costs one memory round trip per warp rather than one per row.  The
-// eight warps' states are combined through shared memory at the end.
+// The partials are independent: their maxima are reduced first (one thread
+// per partial), then warp w adds the weighted partial rows w, w + 8, ... with
+// several 16-byte loads in flight per lane, and the eight warp sums are added
+// through shared memory.  A block reads about 40 partial rows of D floats, so
+// spreading them over eight warps keeps enough loads in flight to stream the
+// partials at memory speed instead of one dependent row at a time.
 #include "internal.cuh"
 
 namespace lucetree {
@@ -31,7 +32,7 @@ __device__ inline float warp_max(float v) {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kB = 6;  // partial rows per warp batch (kB x D/32 floats per lane in flight)
+constexpr int kUnroll = 2;  // partial rows per warp iteration (2 x D/32 floats per lane in flight)
 
 template <typename T, int D>
 __device__ inline void load_slice(const T* p, float (&out)[D / 32]) {
@@ -126,53 +127,50 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(AttnLaunch L) {
         return k < count && cta_begin(c_lo + k, nT, p.Cg) != cta_begin(c_lo + k + 1, nT, p.Cg);
     };
 
-    // the warp's partials, kB at a time, into its running state (m_t, l_t, o)
-    for (int k0 = warp; k0 < count; k0 += kWarps * kB) {
-        float mk[kB], lk[kB];
-        float part[kB][DPL];
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-            const int k = k0 + u * kWarps;
-            mk[u] = -INFINITY;
-            lk[u] = 0.f;
-#pragma unroll
-            for (int x = 0; x < DPL; ++x) part[u][x] = 0.f;
-            if (has_partial(k)) {
-                const float* slot = ws + (size_t)k * sf;
-                mk[u] = slot[(size_t)p.rg.RG * D + rl];
-                lk[u] = slot[(size_t)p.rg.RG * D + p.rg.RG + rl];
-                load_partial<DPL>(slot + (size_t)rl * D + lane * DPL, part[u]);
-            }
-        }
-        float mb = m_t;
-#pragma unroll
-        for (int u = 0; u < kB; ++u) mb = fmaxf(mb, mk[u]);
-        if (mb == -INFINITY) continue;  // nothing in this batch or before it
-        const float sc = m_t > -INFINITY ? exp2f(m_t - mb) : 0.f;
-        l_t *= sc;
-#pragma unroll
-        for (int x = 0; x < DPL; ++x) o[x] *= sc;
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-            const float w = mk[u] > -INFINITY ? exp2f(mk[u] - mb) : 0.f;
-            l_t = fmaf(w, lk[u], l_t);
-#pragma unroll
-            for (int x = 0; x < DPL; ++x) o[x] = fmaf(part[u][x], w, o[x]);
-        }
-        m_t = mb;
-    }
-    // the common shift over the warps, then every warp's sums moved onto it
-    if (lane == 0) s_red[warp] = m_t;
+    // pass 1: the common shift (maximum over the tree parts and every partial)
+    float mk_local = m_t;
+    for (int k = threadIdx.x; k < count; k += kThreads)
+        if (has_partial(k)) mk_local = fmaxf(mk_local, ws[k * sf + (size_t)p.rg.RG * D + rl]);
+    mk_local = warp_max(mk_local);
+    if (lane == 0) s_red[warp] = mk_local;
     __syncthreads();
     float mmax = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, s_red[w]);
-    const float a_w = m_t > -INFINITY ? exp2f(m_t - mmax) : 0.f;
-    const float lsum = l_t * a_w;
+    const float a_tree = m_t > -INFINITY ? exp2f(m_t - mmax) : 0.f;
 #pragma unroll
-    for (int x = 0; x < DPL; ++x) s_o[warp][lane * DPL + x] = o[x] * a_w;
+    for (int x = 0; x < DPL; ++x) o[x] *= a_tree;
+
+    // pass 2: weighted partial rows, warp w takes partials w, w + kWarps, ...
+    float lsum = l_t * a_tree;  // this warp's sums (the same in every lane)
+    for (int k0 = warp * kUnroll; k0 < count; k0 += kWarps * kUnroll) {
+        float w[kUnroll];
+        float part[kUnroll][DPL];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int k = k0 + u;
+            w[u] = 0.f;
+            if (has_partial(k)) {
+                const float* slot = ws + (size_t)k * sf;
+                const float mk = slot[(size_t)p.rg.RG * D + rl];
+                const float lk = slot[(size_t)p.rg.RG * D + p.rg.RG + rl];
+                w[u] = mk > -INFINITY ? exp2f(mk - mmax) : 0.f;
+                lsum += w[u] * lk;
+                load_partial<DPL>(slot + (size_t)rl * D + lane * DPL, part[u]);
+            } else {
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) part[u][x] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int x = 0; x < DPL; ++x) o[x] = fmaf(part[u][x], w[u], o[x]);
+    }
+#pragma unroll
+    for (int x = 0; x < DPL; ++x) s_o[warp][lane * DPL + x] = o[x];
     __syncthreads();
-    if (lane == 0) s_red[warp] = lsum;
+    if (lane == 0) s_red[warp] = lsum;  // every lane of a warp holds the same lsum
     __syncthreads();
 
     // ---- combine the warps' sums and write the row
