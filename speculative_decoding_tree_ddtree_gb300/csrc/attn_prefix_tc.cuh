@@ -750,13 +750,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < kChunks; ++c) {
                         const uint32_t vn = j * kChunks + c;
                         const bool landed = wait_all(&ms->vfull[vn % kMaxSlots], (vn / kMaxSlots) & 1);
-                        if (!VQ && !landed) {
+                        if (VQ != 2 && !landed) {  // (int4 reports a timeout through its barrier)
                             bad = true;
                             break;
                         }
                         uint4* base = reinterpret_cast<uint4*>(sSlots + ((vbase + c) % kNS) * kChunkBytes);
                         const int nv = nvalid - 64 * (c & 1);  // valid keys of this chunk's page
-                        if constexpr (VQ != 0) {
+                        if constexpr (VQ == 1) {
+                            // int8: the fp16 output of key row r covers bytes [128 r, 128 r + 128) of
+                            // each 8 KB box; the second box's lands exactly on row r's own 128 code
+                            // bytes and nowhere else.  So one half-warp expands one row (lane l of
+                            // 16: box l / 8, swizzled unit l % 8), all 16 lanes reading before any
+                            // writes: a __syncwarp suffices, no CTA barrier.  Both halves of a warp
+                            // always get the same number of rows (rows hw, hw + 24, hw + 48).
+                            const uint8_t* codes = reinterpret_cast<const uint8_t*>(base) + VCodes<1>::kOff;
+                            const uint8_t* ex = ms->vexp[vn % kMaxSlots];
+                            const int hw = 2 * (warp - 4) + (lane >> 4), l = lane & 15;
+#pragma unroll
+                            for (int it = 0; it < 3; ++it) {
+                                const int r = hw + 24 * it;
+                                const int u = (l >> 3) * 512 + r * 8 + (l & 7);
+                                const int d0 = 64 * (l >> 3) + 8 * ((l & 7) ^ (r & 7));
+                                uint2 cw = make_uint2(0, 0);
+                                float sc = 0.f;
+                                if (r < 64 && r < nv) {
+                                    cw = *reinterpret_cast<const uint2*>(codes + r * 128 + d0);
+                                    sc = __uint_as_float((uint32_t)ex[r] << 23);  // 2^(e - 127)
+                                }
+                                __syncwarp();
+                                if (r < 64) {
+                                    float f[8];
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        f[e] = (float)(int)(int8_t)(((e < 4 ? cw.x : cw.y) >> (8 * (e & 3))) & 0xFFu) * sc;
+                                    base[u] = make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]),
+                                                         pack_half2(f[4], f[5]), pack_half2(f[6], f[7]));
+                                }
+                            }
+                        } else if constexpr (VQ == 2) {
                             // output unit u: box u / 512 (dims 64 * box ..), key row r, 16-byte unit
                             // p of the swizzled row = logical 8-dim group p ^ (r % 8); its codes
                             // are read for every unit first, since the fp16 output overwrites them
