@@ -55,16 +55,17 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const float* __restric
     unsigned long long best = 0ull;
     long long k = k0;
     if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
-        // 16-byte loads, 4 in flight per thread
+        // 16-byte loads, kU in flight per thread (a chunk is about one round of them)
+        constexpr int kU = 8;
         const float4* x4 = reinterpret_cast<const float4*>(x);
         const long long q0 = k0 / 4, q1 = k1 / 4;  // full float4 groups in [k0, k1)
         long long q = q0 + threadIdx.x;
-        for (; q + 3 * kThreads < q1; q += 4 * kThreads) {
-            float4 v[4];
+        for (; q + (kU - 1) * kThreads < q1; q += kU * kThreads) {
+            float4 v[kU];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = __ldg(x4 + q + u * kThreads);
+            for (int u = 0; u < kU; ++u) v[u] = __ldg(x4 + q + u * kThreads);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kU; ++u) {
                 const unsigned base = (unsigned)(4 * (q + u * kThreads));
                 best = umax64(best, pack_key(v[u].x, base));
                 best = umax64(best, pack_key(v[u].y, base + 1));
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const float* __restric
 
 int argmax_chunks(int rows, int vocab, int device) {
     const int sms = device_sm_count(device);
-    int chunks = (2 * sms + rows - 1) / rows;
+    int chunks = (4 * sms + rows - 1) / rows;
     const int max_by_size = (vocab + 4 * kThreads - 1) / (4 * kThreads);
     if (chunks > max_by_size) chunks = max_by_size;
     if (chunks < 1) chunks = 1;
