@@ -68,6 +68,13 @@ def test_host_side_queries_without_gpu(lib):
     a = LT.LmHeadArgs(dtype=LT.LUCETREE_BF16, rows=8, d_model=256, vocab=1000,
                       hidden=fake, weight=fake, out_idx=fake, out_logit=None, status=fake)
     assert lt.lucetree_lmhead_argmax(ctypes.byref(a), None, 0, None) == 3  # no workspace
+    # quantised-V attention: format and head dim are checked on the host
+    aa = LT.AttnArgs()
+    aa.dtype, aa.B, aa.N, aa.Hq, aa.Hkv, aa.D, aa.page_size = LT.LUCETREE_BF16, 1, 4, 4, 1, 256, 64
+    assert lt.lucetree_verify_attn_vq(ctypes.byref(aa), 3, fake, None, 0, None) == 2   # unknown format
+    assert lt.lucetree_verify_attn_vq(ctypes.byref(aa), 1, None, None, 0, None) == 1   # no exponents
+    aa.D = 128
+    assert lt.lucetree_verify_attn_vq(ctypes.byref(aa), 1, fake, None, 0, None) == 2   # head dim 256 only
     # delta-rule step: shape limits and required pointers, checked on the host
     assert lt.lucetree_delta_tree(None, None) == 1 and lt.lucetree_delta_commit(None, None) == 1
     for (dk, dv, N, want) in ((64, 128, 8, 2), (128, 12, 8, 2), (128, 128, 65, 2), (128, 128, 0, 1)):
