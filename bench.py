@@ -701,6 +701,29 @@ def measure_stage(args, dev, stream, rank):
     }
 
 
+def run_vq_only(args):
+    """Only the quantised-V attention calls on the headline workload (for
+    profiler captures): inputs, ancestor masks, then measure_vq."""
+    import torch
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    from speculative_decoding_tree_ddtree_gb300.build import build
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    cfg = W.CONFIGS[args.config]
+    inp = W.generate(cfg, seed=0, with_logits=False)
+    tdt = torch.bfloat16 if cfg.dtype == W.BF16 else torch.float16
+    h16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(tdt).to(dev)
+    d = dict(q=h16(inp["q"]), k_pool=h16(inp["k_pool"]), k_tree=h16(inp["k_tree"]), v_tree=h16(inp["v_tree"]),
+             page_table=torch.from_numpy(inp["page_table"]).to(dev), ctx_len=torch.from_numpy(inp["ctx_len"]).to(dev),
+             parent=torch.from_numpy(inp["parent"]).to(dev))
+    step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, device=dev)
+    LT.lucetree_build_anc_mask(d["parent"], step.anc, step.status, stream)
+    print(json.dumps({"quantised_v": measure_vq(args, dev, stream, 0, d, step, cfg)}), flush=True)
+    return 0
+
+
 def run_stage_only(args):
     import torch
     from speculative_decoding_tree_ddtree_gb300.build import build
@@ -750,6 +773,7 @@ def main(argv=None):
     ap.add_argument("--delta-only", action="store_true", help="time only the recurrent-state tree pass and commit")
     ap.add_argument("--no-stage", action="store_true", help="skip the host-resident page staging measurement")
     ap.add_argument("--no-vq", action="store_true", help="skip the quantised-V attention measurement")
+    ap.add_argument("--vq-only", action="store_true", help="time only the quantised-V attention calls")
     ap.add_argument("--stage-only", action="store_true", help="time only the host-resident page staging")
     args = ap.parse_args(argv)
     if args.lmhead_only:
@@ -758,6 +782,8 @@ def main(argv=None):
         return run_delta_only(args)
     if args.stage_only:
         return run_stage_only(args)
+    if args.vq_only:
+        return run_vq_only(args)
     cfg = W.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)
