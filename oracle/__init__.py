@@ -281,3 +281,41 @@ def dequant_v(codes, v_exp, v_format: int, dtype: int) -> np.ndarray:
     if not np.array_equal(h.astype(np.float64), val):
         raise ValueError("value not exact in fp16")
     return h.view(np.uint16)
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    """FP8 E4M3 (the OCP 8-bit floating-point format: 1 sign bit, 4 exponent
+    bits with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN) to
+    float64, from the format's definition: exponent field 0 gives subnormals
+    (m / 8) * 2^-6, otherwise (1 + m / 8) * 2^(E - 7)."""
+    c = np.asarray(codes, np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    mag = np.where((e == 0xF) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def dequant_k_e4m3(codes, k_exp, dtype: int) -> np.ndarray:
+    """Quantised K storage (a reading for the asymmetric K/V quantisation the
+    pages list; the library's own format): value = e4m3(code) * 2^(e - 127)
+    with one exponent byte e per token and head (e = 0: zero).  codes: uint8
+    [..][64][D]; k_exp: uint8 [..][64].  Returns 16-bit storage bits of dtype;
+    exact (4 significant bits) where the value is in the dtype's range, which
+    is checked."""
+    val = decode_e4m3(codes)
+    e = np.asarray(k_exp, np.int64)
+    scale = np.where(e == 0, 0.0, np.ldexp(1.0, e - 127))
+    val = val * scale[..., None]
+    if np.isnan(val).any():
+        raise ValueError("NaN code in quantised K")
+    if dtype == BF16:
+        bits32 = val.astype(np.float32).view(np.uint32)
+        if np.any(bits32 & 0xFFFF) or not np.array_equal(bits32.view(np.float32).astype(np.float64), val):
+            raise ValueError("value not exact in bf16")
+        return (bits32 >> 16).astype(np.uint16)
+    h = val.astype(np.float16)
+    if not np.array_equal(h.astype(np.float64), val):
+        raise ValueError("value not exact in fp16")
+    return h.view(np.uint16)

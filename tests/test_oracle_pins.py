@@ -588,3 +588,27 @@ def test_dequant_v_is_exact_over_the_code_and_exponent_range():
         oracle.dequant_v(codes, exps, oracle.V_INT8, dt)  # raises if any value were rounded
     with pytest.raises(ValueError):  # 127 * 2^9 = 65024 is still fp16, 127 * 2^10 is not
         oracle.dequant_v(np.full((1, 1, 2), 127, np.uint8), np.array([[137]], np.uint8), oracle.V_INT8, oracle.F16)
+
+
+# ---------------------------------------------------------------- quantised K storage (FP8 E4M3 codes)
+
+def test_decode_e4m3_matches_torch_on_every_code():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.decode_e4m3(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_decode_e4m3_hand_values_and_dequant():
+    got = oracle.decode_e4m3([0x38, 0x7E, 0x01, 0xB8, 0x00, 0x80, 0x3C])
+    assert got.tolist() == [1.0, 448.0, 2.0 ** -9, -1.0, 0.0, -0.0, 1.5]
+    # code 1.5 at exponent 126 (x 1/2) -> 0.75; exponent 0 -> 0
+    bits = oracle.dequant_k_e4m3(np.array([[[0x3C, 0xB8]]], np.uint8), np.array([[126]], np.uint8), oracle.F16)
+    assert bits.view(np.float16).astype(float).tolist() == [[[0.75, -0.5]]]
+    zero = oracle.dequant_k_e4m3(np.array([[[0x3C]]], np.uint8), np.array([[0]], np.uint8), oracle.BF16)
+    assert zero.tolist() == [[[0]]]
+    with pytest.raises(ValueError):
+        oracle.dequant_k_e4m3(np.array([[[0x7F]]], np.uint8), np.array([[127]], np.uint8), oracle.F16)

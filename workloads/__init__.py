@@ -408,3 +408,18 @@ def generate_vq(cfg: VerifyConfig, v_format: int, seed: int = 0) -> dict:
         raise ValueError(v_format)
     v_exp = rng.integers(118, 125, size=shape[:3]).astype(np.uint8)
     return dict(v_codes=codes, v_exp=v_exp)
+
+
+def generate_kq(cfg: VerifyConfig, seed: int = 0) -> dict:
+    """Quantised K pool for ``cfg``'s page geometry, drawn as storage: k_codes
+    uint8 [num_pages][Hkv][64][D], FP8 E4M3 codes uniform over the finite ones
+    (NaN codes 0x7F / 0xFF excluded), k_exp uint8 [num_pages][Hkv][64] uniform in
+    [120, 124]."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, _name_key(cfg.name), 0x4B51]))
+    need = [pages_needed(L, cfg.N) for L in cfg.ctx]
+    num_pages = sum(need) + cfg.spare_pages
+    shape = (num_pages, cfg.Hkv, PAGE, cfg.D)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    codes = finite[rng.integers(0, len(finite), size=shape)]
+    k_exp = rng.integers(120, 125, size=shape[:3]).astype(np.uint8)
+    return dict(k_codes=codes, k_exp=k_exp)
