@@ -126,9 +126,12 @@ LUCETREE_API lucetree_status lucetree_verify_attn_workspace(int B, int N, int Hq
  * table) and every tree node j with bit j of anc_mask[b][i] set.  Split-K over
  * the committed prefix on the tensor cores, then one merge launch that adds
  * the tree block and combines the splits by log-sum-exp.
+ * Scores and sums are fp32; the P.V product runs on fp16 operands on chip
+ * (P rounded to fp16, bf16 V converted exactly while |v| < 65536).
  * Device checks: ctx_len outside [0, max_pages_per_seq*64] -> BAD_CTX (the
  * sequence is treated as empty); page id out of range -> BAD_PAGE (those keys
- * are skipped); a mask without its own bit -> BAD_NODE.
+ * are skipped); a mask without its own bit -> BAD_NODE; an output row that is
+ * not finite -> NONFINITE.
  */
 LUCETREE_API lucetree_status lucetree_verify_attn(const lucetree_attn_args* args, void* workspace, size_t workspace_bytes,
                                      void* stream);
