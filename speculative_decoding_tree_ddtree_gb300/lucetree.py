@@ -16,6 +16,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblucetree.so")
 
 LUCETREE_OK = 0
+LUCETREE_V_INT8, LUCETREE_V_INT4 = 1, 2
 LUCETREE_F16 = 0
 LUCETREE_BF16 = 1
 PAGE_SIZE = 64
@@ -166,6 +167,49 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+# Element types the kernels read and write: 16-bit activations, int32 indices
+# and lengths, fp32 outputs, 32-bit status words, 64-bit ancestor masks.
+_H16 = (torch.float16, torch.bfloat16)
+_I32 = (torch.int32,)
+_F32 = (torch.float32,)
+_W32 = tuple(t for t in (torch.int32, getattr(torch, "uint32", None)) if t is not None)
+_W64 = tuple(t for t in (torch.int64, getattr(torch, "uint64", None)) if t is not None)
+_U8 = (torch.uint8, torch.int8)
+
+
+def _dims(t, name: str, ndim: int):
+    """The shape of a required tensor of rank ndim."""
+    if t is None:
+        raise LucetreeError(f"{name} is required")
+    if t.dim() != ndim:
+        raise LucetreeError(f"{name}: expected {ndim} dimensions, got shape {tuple(t.shape)}")
+    return t.shape
+
+
+def _expect(t, name: str, shape: tuple, dtypes: tuple):
+    """Refuse a tensor whose shape or element type differs from what the
+    kernel will index: a mismatch would read or write past its end."""
+    if t is None:
+        raise LucetreeError(f"{name} is required")
+    if t.dtype in dtypes and t.shape == shape:
+        return
+    raise LucetreeError(f"{name}: expected shape {tuple(shape)} of {'/'.join(str(d) for d in dtypes)}, "
+                        f"got {tuple(t.shape)} of {t.dtype}")
+
+
+def _expect_status(t):
+    if t is None or t.dtype not in _W32 or t.numel() < 1:
+        raise LucetreeError("status: expected a device int32 word")
+
+
+def _expect_16bit(t, name: str, shape: tuple):
+    """Raw 16-bit data of any 16-bit element type (byte copies)."""
+    if t is None:
+        raise LucetreeError(f"{name} is required")
+    if t.element_size() != 2 or t.shape != shape:
+        raise LucetreeError(f"{name}: expected shape {tuple(shape)} of a 16-bit type, got {tuple(t.shape)} of {t.dtype}")
+
+
 def dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return LUCETREE_BF16
@@ -182,7 +226,34 @@ def lucetree_verify_attn_workspace(B: int, N: int, Hq: int, Hkv: int, D: int) ->
     return int(n.value)
 
 
-def _attn_args(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale):
+def _check_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse,
+                v_format=None, v_exp=None):
+    """Shapes and element types of one tree-verify attention call (layouts as
+    lucetree_verify_attn documents them); v_format selects the quantised V pool."""
+    B, N, Hq, D = _dims(q, "q", 4)
+    if q.dtype not in _H16:
+        raise LucetreeError(f"q: unsupported dtype {q.dtype}")
+    P, Hkv, page, _ = _dims(k_pool, "k_pool", 4)
+    _expect(k_pool, "k_pool", (P, Hkv, page, D), (q.dtype,))
+    if v_format is None:
+        _expect(v_pool, "v_pool", (P, Hkv, page, D), (q.dtype,))
+    else:
+        _expect(v_pool, "v_codes", (P, Hkv, page, D // 2 if v_format == LUCETREE_V_INT4 else D), _U8)
+        _expect(v_exp, "v_exp", (P, Hkv, page), _U8)
+    _expect(k_tree, "k_tree", (B, N, Hkv, D), (q.dtype,))
+    _expect(v_tree, "v_tree", (B, N, Hkv, D), (q.dtype,))
+    _expect(page_table, "page_table", (B, _dims(page_table, "page_table", 2)[1]), _I32)
+    _expect(ctx_len, "ctx_len", (B,), _I32)
+    _expect(anc_mask, "anc_mask", (B, N), _W64)
+    _expect(out, "out", (B, N, Hq, D), _F32)
+    if lse is not None:
+        _expect(lse, "lse", (B, N, Hq), _F32)
+    _expect_status(status)
+
+
+def _attn_args(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale,
+               v_format=None, v_exp=None):
+    _check_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, v_format, v_exp)
     B, N, Hq, D = q.shape
     Hkv = k_pool.shape[1]
     a = AttnArgs()
@@ -209,21 +280,25 @@ def lucetree_verify_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree,
                                        _stream(stream)))
 
 
-LUCETREE_V_INT8, LUCETREE_V_INT4 = 1, 2
-
 
 def lucetree_verify_attn_vq(q, k_pool, v_codes, v_exp, v_format, page_table, ctx_len, k_tree, v_tree, anc_mask, out,
                             status, workspace, lse=None, scale: float | None = None, stream=None):
     """As lucetree_verify_attn with V stored quantised: v_codes uint8 [P][Hkv][64][D]
     (int8 codes) or [P][Hkv][64][D/2] (int4 codes, low nibble first), v_exp uint8
     [P][Hkv][64] (value = code * 2^(e - 127))."""
-    a = _attn_args(q, k_pool, v_codes, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale)
+    if v_format not in (LUCETREE_V_INT8, LUCETREE_V_INT4):
+        raise LucetreeError(f"unsupported V format {v_format}")
+    a = _attn_args(q, k_pool, v_codes, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale,
+                   v_format=v_format, v_exp=v_exp)
     _check(load().lucetree_verify_attn_vq(ctypes.byref(a), int(v_format), _ptr(v_exp), _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def lucetree_build_anc_mask(parent, anc, status, stream=None):
-    B, N = parent.shape
+    B, N = _dims(parent, "parent", 2)
+    _expect(parent, "parent", (B, N), _I32)
+    _expect(anc, "anc", (B, N), _W64)
+    _expect_status(status)
     _check(load().lucetree_build_anc_mask(_ptr(parent), B, N, _ptr(anc), _ptr(status), _stream(stream)))
 
 
@@ -235,21 +310,44 @@ def lucetree_argmax_workspace(rows: int, vocab: int) -> int:
 
 def lucetree_argmax(logits, out_idx, workspace, stream=None):
     """logits fp32 [..., V] (rows = all leading dims) -> out_idx int32 [...]."""
+    if logits is None or logits.dim() < 1 or logits.dtype != torch.float32:
+        raise LucetreeError("logits: expected a float32 tensor [..., V]")
     V = logits.shape[-1]
-    rows = logits.numel() // V
+    rows = logits.numel() // V if V > 0 else 0
+    if out_idx is None or out_idx.dtype != torch.int32 or out_idx.numel() != rows:
+        raise LucetreeError(f"out_idx: expected {rows} int32 entries")
     _check(load().lucetree_argmax(_ptr(logits), rows, V, V, _ptr(out_idx), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def lucetree_accept(parent, draft, argmax_idx, vocab: int, acc_nodes, acc_len, bonus, status, stream=None):
-    B, N = parent.shape
+    B, N = _dims(parent, "parent", 2)
+    _expect(parent, "parent", (B, N), _I32)
+    _expect(draft, "draft", (B, N), _I32)
+    _expect(argmax_idx, "argmax", (B, N + 1), _I32)
+    _expect(acc_nodes, "acc_nodes", (B, N), _I32)
+    _expect(acc_len, "acc_len", (B,), _I32)
+    _expect(bonus, "bonus", (B,), _I32)
+    _expect_status(status)
     _check(load().lucetree_accept(_ptr(parent), _ptr(draft), _ptr(argmax_idx), B, N, vocab, _ptr(acc_nodes),
                                   _ptr(acc_len), _ptr(bonus), _ptr(status), _stream(stream)))
 
 
 def lucetree_commit(k_tree, v_tree, acc_nodes, acc_len, page_table, ctx_len_in, ctx_len_out, k_pool, v_pool,
                     status, stream=None):
-    B, N, Hkv, D = k_tree.shape
+    B, N, Hkv, D = _dims(k_tree, "k_tree", 4)
+    if k_tree.dtype not in _H16:
+        raise LucetreeError(f"k_tree: unsupported dtype {k_tree.dtype}")
+    _expect(v_tree, "v_tree", (B, N, Hkv, D), (k_tree.dtype,))
+    _expect(acc_nodes, "acc_nodes", (B, N), _I32)
+    _expect(acc_len, "acc_len", (B,), _I32)
+    _expect(page_table, "page_table", (B, _dims(page_table, "page_table", 2)[1]), _I32)
+    _expect(ctx_len_in, "ctx_len_in", (B,), _I32)
+    _expect(ctx_len_out, "ctx_len_out", (B,), _I32)
+    P, _, page, _ = _dims(k_pool, "k_pool", 4)
+    _expect(k_pool, "k_pool", (P, Hkv, page, D), (k_tree.dtype,))
+    _expect(v_pool, "v_pool", (P, Hkv, page, D), (k_tree.dtype,))
+    _expect_status(status)
     c = CommitArgs()
     c.dtype = dtype_code(k_tree)
     c.B, c.N, c.Hkv, c.D = B, N, Hkv, D
@@ -315,16 +413,7 @@ def lucetree_verify_attn_noalloc(q, k_pool, v_pool, page_table, ctx_len, k_tree,
     if need > NOALLOC_SCRATCH_BYTES:
         raise LucetreeError(f"lucetree_verify_attn_noalloc: these sizes need {need} bytes of scratch, "
                             f"more than the fixed {NOALLOC_SCRATCH_BYTES}")
-    a = AttnArgs()
-    a.dtype = dtype_code(q)
-    a.B, a.N, a.Hq, a.Hkv, a.D = B, N, Hq, Hkv, D
-    a.page_size = k_pool.shape[2]
-    a.scale = float(scale) if scale is not None else float(D) ** -0.5
-    a.q, a.k_pool, a.v_pool = _ptr(q), _ptr(k_pool), _ptr(v_pool)
-    a.num_pages = k_pool.shape[0]
-    a.page_table, a.max_pages_per_seq = _ptr(page_table), page_table.shape[1]
-    a.ctx_len, a.k_tree, a.v_tree, a.anc_mask = _ptr(ctx_len), _ptr(k_tree), _ptr(v_tree), _ptr(anc_mask)
-    a.out, a.lse, a.status = _ptr(out), _ptr(lse), _ptr(status)
+    a = _attn_args(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale)
     _check(load().lucetree_verify_attn_noalloc(ctypes.byref(a), _stream(stream)))
 
 
@@ -340,11 +429,14 @@ def lucetree_lmhead_argmax(hidden, weight, out_idx, status, workspace, out_logit
     """hidden [rows][d_model] and weight [vocab][d_model] (both fp16 or both
     bf16) -> out_idx int32 [rows]: the lowest vocabulary index of each row's
     largest logit; optionally out_logit fp32 [rows] (that logit)."""
-    rows, d_model = hidden.shape
+    rows, d_model = _dims(hidden, "hidden", 2)
     a = LmHeadArgs()
     a.dtype = dtype_code(hidden)
-    if dtype_code(weight) != a.dtype:
-        raise LucetreeError("hidden and weight must share a dtype")
+    _expect(weight, "weight", (_dims(weight, "weight", 2)[0], d_model), (hidden.dtype,))
+    _expect(out_idx, "out_idx", (rows,), _I32)
+    if out_logit is not None:
+        _expect(out_logit, "out_logit", (rows,), _F32)
+    _expect_status(status)
     a.rows, a.d_model, a.vocab = rows, d_model, weight.shape[0]
     a.hidden, a.weight = _ptr(hidden), _ptr(weight)
     a.out_idx, a.out_logit, a.status = _ptr(out_idx), _ptr(out_logit), _ptr(status)
@@ -354,13 +446,24 @@ def lucetree_lmhead_argmax(hidden, weight, out_idx, status, workspace, out_logit
 
 # ---------------------------------------------------------------- recurrent-state (delta rule) step
 
-def _delta_args(q, k, v, alpha, beta, state, status, parent=None, out=None, acc_nodes=None, acc_len=None):
-    B, N, Hk, dk = k.shape
-    Hv, dv = v.shape[2], v.shape[3]
+def _delta_args(q, k, v, alpha, beta, state, status, parent=None, out=None, acc_nodes=None, acc_len=None,
+                tree=True):
+    B, N, Hk, dk = _dims(k, "k", 4)
+    Hv, dv = _dims(v, "v", 4)[2:]
     a = DeltaArgs()
     a.dtype = dtype_code(k)
-    if dtype_code(v) != a.dtype or (q is not None and dtype_code(q) != a.dtype):
-        raise LucetreeError("q, k and v must share a dtype")
+    _expect(v, "v", (B, N, Hv, dv), (k.dtype,))
+    _expect(alpha, "alpha", (B, N, Hv), _F32)
+    _expect(beta, "beta", (B, N, Hv), _F32)
+    _expect(state, "state", (B, Hv, dk, dv), _F32)
+    _expect_status(status)
+    if tree:
+        _expect(q, "q", (B, N, Hk, dk), (k.dtype,))
+        _expect(parent, "parent", (B, N), _I32)
+        _expect(out, "out", (B, N, Hv, dv), _F32)
+    else:
+        _expect(acc_nodes, "acc_nodes", (B, N), _I32)
+        _expect(acc_len, "acc_len", (B,), _I32)
     a.B, a.N, a.Hk, a.Hv, a.dk, a.dv = B, N, Hk, Hv, dk, dv
     a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
     a.alpha, a.beta, a.parent = _ptr(alpha), _ptr(beta), _ptr(parent)
@@ -378,7 +481,7 @@ def lucetree_delta_tree(q, k, v, alpha, beta, parent, state, out, status, stream
 
 def lucetree_delta_commit(k, v, alpha, beta, acc_nodes, acc_len, state, status, stream=None):
     """state[b][h] <- the recurrence along acc_nodes[b][:acc_len[b]] (in place)."""
-    a = _delta_args(None, k, v, alpha, beta, state, status, acc_nodes=acc_nodes, acc_len=acc_len)
+    a = _delta_args(None, k, v, alpha, beta, state, status, acc_nodes=acc_nodes, acc_len=acc_len, tree=False)
     _check(load().lucetree_delta_commit(ctypes.byref(a), _stream(stream)))
 
 
@@ -396,6 +499,20 @@ def lucetree_stage_pages(host_k, host_v, src, dst, k_pool, v_pool, status, table
                          stream=None):
     """Copy host pages src[i] (page-locked host pools [host_pages][Hkv][64][D])
     into device pool pages dst[i]; with table_idx, page_table.view(-1)[table_idx[i]] = dst[i]."""
+    P, Hkv, page, D = _dims(k_pool, "k_pool", 4)
+    _expect_16bit(k_pool, "k_pool", (P, Hkv, page, D))
+    _expect_16bit(v_pool, "v_pool", (P, Hkv, page, D))
+    host_pages = _dims(host_k, "host_k", 4)[0]
+    _expect_16bit(host_k, "host_k", (host_pages, Hkv, page, D))
+    _expect_16bit(host_v, "host_v", (host_pages, Hkv, page, D))
+    n = _dims(src, "src", 1)[0]
+    _expect(src, "src", (n,), _I32)
+    _expect(dst, "dst", (n,), _I32)
+    if table_idx is not None:
+        _expect(table_idx, "table_idx", (n,), _I32)
+        if page_table is None or page_table.dtype != torch.int32:
+            raise LucetreeError("page_table: an int32 table is required with table_idx")
+    _expect_status(status)
     a = StageArgs()
     a.Hkv, a.D = k_pool.shape[1], k_pool.shape[3]
     a.n = src.numel()
