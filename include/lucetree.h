@@ -360,6 +360,17 @@ typedef struct lucetree_stage_args {
  */
 LUCETREE_API lucetree_status lucetree_stage_pages(const lucetree_stage_args* args, void* stream);
 
+/*
+ * Self-test of the failure path shared by every kernel wait: one block waits
+ * on a barrier that nothing arrives on, gives up after ~limit_cycles SM
+ * cycles (1 .. 4e9; the step kernels use 4e9, about two seconds), sets
+ * LUCETREE_DEV_TIMEOUT in *status and returns.  waited_cycles (device
+ * int64, or NULL) receives the cycles the wait took.  Host errors:
+ * INVALID_ARG (null status, limit out of range), CUDA.
+ */
+LUCETREE_API lucetree_status lucetree_selftest_wait_timeout(uint32_t* status, long long limit_cycles,
+                                                            long long* waited_cycles, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 LUCETREE_API const char* lucetree_status_string(lucetree_status status);
 

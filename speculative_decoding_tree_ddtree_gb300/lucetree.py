@@ -47,6 +47,7 @@ EXPORTED = (
     "lucetree_delta_commit",
     "lucetree_stage_pages",
     "lucetree_verify_attn_vq",
+    "lucetree_selftest_wait_timeout",
 )
 
 
@@ -137,6 +138,7 @@ def load(path: str | None = None):
     lib.lucetree_delta_commit.argtypes = [ctypes.POINTER(DeltaArgs), P]
     lib.lucetree_stage_pages.argtypes = [ctypes.POINTER(StageArgs), P]
     lib.lucetree_verify_attn_vq.argtypes = [ctypes.POINTER(AttnArgs), I, P, P, SZ, P]
+    lib.lucetree_selftest_wait_timeout.argtypes = [P, ctypes.c_longlong, P, P]
     for name in EXPORTED:
         if name not in ("lucetree_status_string", "lucetree_abi_version"):
             getattr(lib, name).restype = I
@@ -523,3 +525,15 @@ def lucetree_stage_pages(host_k, host_v, src, dst, k_pool, v_pool, status, table
     a.k_pool, a.v_pool, a.num_pages = _ptr(k_pool), _ptr(v_pool), k_pool.shape[0]
     a.status = _ptr(status)
     _check(load().lucetree_stage_pages(ctypes.byref(a), _stream(stream)))
+
+
+# ---------------------------------------------------------------- failure path self-test
+
+def lucetree_selftest_wait_timeout(status, limit_cycles: int, waited_cycles=None, stream=None):
+    """One block waits on a barrier nothing arrives on; after ~limit_cycles SM
+    cycles it sets DEV_TIMEOUT in status and returns (waited_cycles: int64 [1])."""
+    _expect_status(status)
+    if waited_cycles is not None:
+        _expect(waited_cycles, "waited_cycles", (1,), (torch.int64,))
+    _check(load().lucetree_selftest_wait_timeout(_ptr(status), int(limit_cycles), _ptr(waited_cycles),
+                                                 _stream(stream)))
