@@ -1,0 +1,35 @@
+"""bench.py's reference arm (the fp64 oracle timed on the host cores) runs
+without a GPU: one JSON line with the contract's keys, on the same metric
+and unit as the GPU arm, with its CPU baseline and a copy-free e2e."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "1",
+                        "--config", "tiny-1k-b8"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 1 and d["scaling"] == "weak"
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["vs_baseline"] is None
+    assert d["data"] == "synthetic" and d["config"]["workload"].startswith("tiny-1k-b8")
+    assert "smaller than L2" in d["config"]["l2"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_headline_workload_is_larger_than_l2():
+    import workloads as W
+    note = bench.config_dict(W.HEADLINE_128K_B22)["l2"]
+    assert note.startswith("inputs larger than L2: committed K/V 512 MiB")
