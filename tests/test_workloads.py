@@ -77,3 +77,61 @@ def test_sweep_has_27_points():
     pts = W.sweep_points()
     assert len(pts) == 27
     assert len({p.name for p in pts}) == 27
+
+
+def _f64(bits, dtype):
+    bits = np.asarray(bits, np.uint16)
+    if dtype == W.BF16:
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return bits.view(np.float16).astype(np.float64)
+
+
+def test_delta_inputs_follow_their_recipe():
+    cfg = W.DeltaConfig("gen-delta", B=3, N=22, Hk=2, Hv=4, dk=128, dv=64, dtype=W.BF16, tree="random", branch_cap=4)
+    a = W.generate_delta(cfg, seed=1)
+    assert a["q"].shape == a["k"].shape == (3, 22, 2, 128) and a["q"].dtype == np.uint16
+    assert a["v"].shape == (3, 22, 4, 64) and a["state"].shape == (3, 4, 128, 64)
+    assert a["alpha"].dtype == a["beta"].dtype == a["state"].dtype == np.float32
+    for key in ("q", "k"):  # unit vectors up to the dtype's rounding
+        n = np.linalg.norm(_f64(a[key], cfg.dtype), axis=-1)
+        assert np.abs(n - 1.0).max() < 2 ** -7
+    # alpha = exp(-0.1 softplus(z)) lies in (0, 1); beta = sigmoid(z) in (0, 1)
+    assert (a["alpha"] > 0).all() and (a["alpha"] < 1).all() and (a["beta"] > 0).all() and (a["beta"] < 1).all()
+    assert np.exp(-0.1 * np.log1p(np.exp(5.0))) < a["alpha"].min() and abs(float(a["beta"].mean()) - 0.5) < 0.05
+    assert abs(float(a["state"].std()) - 0.1) < 0.005
+    for b in range(3):
+        par = a["parent"][b]
+        assert par[0] == -1 and all(-1 <= par[i] < i for i in range(22))
+        assert np.bincount(par[par >= 0], minlength=22).max() <= 4
+    b = W.generate_delta(cfg, seed=1)
+    c = W.generate_delta(cfg, seed=2)
+    assert all(np.array_equal(a[k], b[k]) for k in a) and not np.array_equal(a["v"], c["v"])
+
+
+def test_quantised_storage_inputs_follow_their_recipe():
+    cfg = W.VerifyConfig("gen-vq", ctx=(700, 64), Hq=6, Hkv=3, D=256, dtype=W.BF16, N=5, paged="permuted",
+                         spare_pages=2)
+    pools = W.generate(cfg, seed=0)["k_pool"].shape
+    v8 = W.generate_vq(cfg, W.V_INT8, seed=0)
+    assert v8["v_codes"].shape == pools and v8["v_codes"].dtype == np.uint8
+    c8 = v8["v_codes"].view(np.int8)
+    assert c8.min() >= -127 and c8.max() <= 127 and c8.min() < -100 and c8.max() > 100
+    assert v8["v_exp"].shape == pools[:3] and v8["v_exp"].min() >= 118 and v8["v_exp"].max() <= 124
+    v4 = W.generate_vq(cfg, W.V_INT4, seed=0)
+    assert v4["v_codes"].shape == pools[:3] + (cfg.D // 2,)
+    nib = np.stack([v4["v_codes"] & 0xF, v4["v_codes"] >> 4]).astype(np.int64)
+    signed = np.where(nib >= 8, nib - 16, nib)
+    assert signed.min() == -7 and signed.max() == 7  # the code -8 is never drawn
+    kq = W.generate_kq(cfg, seed=0)
+    assert kq["k_codes"].shape == pools and not ((kq["k_codes"] & 0x7F) == 0x7F).any()  # no NaN codes
+    assert kq["k_exp"].min() >= 120 and kq["k_exp"].max() <= 124
+    assert len(np.unique(kq["k_codes"])) == 254
+
+
+def test_lmhead_inputs_follow_their_recipe():
+    cfg = W.LmHeadConfig("gen-lm", rows=9, d_model=256, vocab=5000, dtype=W.F16)
+    a = W.generate_lmhead(cfg, seed=0)
+    assert a["hidden"].shape == (9, 256) and a["weight"].shape == (5000, 256)
+    assert a["hidden"].dtype == a["weight"].dtype == np.uint16
+    assert abs(float(_f64(a["hidden"], cfg.dtype).std()) - 1.0) < 0.05
+    assert abs(float(_f64(a["weight"], cfg.dtype).std()) - cfg.w_std) < 0.001

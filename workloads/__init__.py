@@ -293,7 +293,7 @@ class LmHeadConfig:
     """The projection of the verify rows' hidden states through the target's
     lm_head, reduced to each row's argmax.  rows = B * (N + 1) (the root and
     every tree node); the pages give no hidden size, d_model = 5120 is this
-    build's reading for a 27B-class target."""
+    library's reading for a 27B-class target."""
     name: str
     rows: int
     d_model: int
@@ -333,7 +333,7 @@ class DeltaConfig:
     """The tree-verify step of a gated-delta-rule (DeltaNet-style) layer of a
     hybrid target: one recurrent state [dk][dv] per value head, advanced along
     every tree node's root path.  The pages give no layer shape; 16 query/key
-    heads, 32 value heads and 128-dim heads are this build's reading for a
+    heads, 32 value heads and 128-dim heads are this library's reading for a
     27B-class hybrid target."""
     name: str
     B: int = 1
