@@ -84,6 +84,20 @@ def test_host_side_queries_without_gpu(lib):
     d = LT.DeltaArgs(dtype=LT.LUCETREE_BF16, B=1, N=8, Hk=1, Hv=2, dk=128, dv=128, k=fake, v=fake,
                      alpha=fake, beta=fake, state=fake, status=fake)
     assert lt.lucetree_delta_commit(ctypes.byref(d), None) == 1  # no accepted path given
+    # host-resident page staging: sizes and pointers are checked before any CUDA call
+    assert lt.lucetree_stage_pages(None, None) == 1
+    ok = dict(Hkv=2, D=128, n=3, host_k=fake, host_v=fake, host_pages=4, src=fake, dst=fake, table_idx=None,
+              page_table=None, table_len=0, k_pool=fake, v_pool=fake, num_pages=8, status=fake)
+    for change in (dict(n=-1), dict(D=100), dict(Hkv=0), dict(num_pages=0), dict(host_v=None),
+                   dict(host_k=fake + 8), dict(table_idx=fake), dict(status=None)):
+        st = LT.StageArgs(**{**ok, **change})
+        assert lt.lucetree_stage_pages(ctypes.byref(st), None) == 1, change
+    st = LT.StageArgs(**{**ok, "n": 0, "host_k": None})
+    assert lt.lucetree_stage_pages(ctypes.byref(st), None) == 0  # nothing to stage: no launch, no error
+    # the wait-timeout self-test: status required, limit within (0, 4e9]
+    assert lt.lucetree_selftest_wait_timeout(None, 1000, None, None) == 1
+    assert lt.lucetree_selftest_wait_timeout(fake, 0, None, None) == 1
+    assert lt.lucetree_selftest_wait_timeout(fake, 4000000001, None, None) == 1
 
 
 def test_binding_rejects_host_tensors():
