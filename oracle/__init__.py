@@ -319,3 +319,51 @@ def dequant_k_e4m3(codes, k_exp, dtype: int) -> np.ndarray:
     if not np.array_equal(h.astype(np.float64), val):
         raise ValueError("value not exact in fp16")
     return h.view(np.uint16)
+
+
+def _bits_to_f64(bits, dtype: int) -> np.ndarray:
+    """16-bit storage bits of dtype to float64 (exact)."""
+    b = np.asarray(bits, np.uint16)
+    if dtype == BF16:
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return b.view(np.float16).astype(np.float64)
+
+
+def _round_e4m3(y: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 code to each |y| <= 448, ties to the even code (the codes of
+    two neighbouring values differ by one, so exactly one is even); the sign
+    bit follows y's sign bit."""
+    pos = np.arange(0x7F, dtype=np.uint8)          # 0x00 .. 0x7E: the non-negative finite codes, ascending
+    vals = decode_e4m3(pos)
+    a = np.abs(y)
+    if np.any(a > 448.0):
+        raise ValueError("beyond E4M3's range")
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, len(vals) - 1)
+    lo = np.clip(hi - 1, 0, len(vals) - 1)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick = np.where(d_lo < d_hi, lo, hi)
+    tie = (d_lo == d_hi) & (lo != hi)
+    pick = np.where(tie, np.where(lo % 2 == 0, lo, hi), pick)
+    return (pos[pick] | np.where(np.signbit(y), 0x80, 0x00)).astype(np.uint8)
+
+
+def quantise_k_e4m3(k_bits, dtype: int):
+    """The storing side of the quantised-K format (the library's own reading of
+    the asymmetric K/V quantisation the pages list without a format): for each
+    token and head row k of 16-bit values, p is the largest integer with
+    max|k| * 2^p <= 448 (E4M3's largest finite value), the exponent byte is
+    e = 127 - p, and code d = e4m3(k_d * 2^p) rounded to nearest, ties to the
+    even code.  An all-zero row gets e = 0 and zero codes.  k_bits: uint16
+    [..][D]; returns (codes uint8 [..][D], k_exp uint8 [..]), which
+    dequant_k_e4m3 reads back.  Raises if e would leave [1, 254]."""
+    x = _bits_to_f64(k_bits, dtype)
+    m = np.abs(x).max(axis=-1)
+    mant, ex = np.frexp(m)                          # m = mant * 2^ex, mant in [0.5, 1)
+    p = np.where(mant <= 0.875, 9 - ex, 8 - ex)     # 448 = 0.875 * 2^9
+    zero = m == 0
+    p = np.where(zero, 0, p).astype(np.int64)
+    e = np.where(zero, 0, 127 - p)
+    if np.any(~zero & ((e < 1) | (e > 254))):
+        raise ValueError("row scale outside the exponent byte's range")
+    codes = _round_e4m3(x * np.ldexp(1.0, p)[..., None])
+    return codes, e.astype(np.uint8)

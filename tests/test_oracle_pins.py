@@ -612,3 +612,51 @@ def test_decode_e4m3_hand_values_and_dequant():
     assert zero.tolist() == [[[0]]]
     with pytest.raises(ValueError):
         oracle.dequant_k_e4m3(np.array([[[0x7F]]], np.uint8), np.array([[127]], np.uint8), oracle.F16)
+
+
+def _bf16_bits(vals):
+    return W.f32_to_bf16_bits(np.asarray(vals, np.float32))
+
+
+def test_quantise_k_hand_rows():
+    # max 1 -> p = 8 (256 <= 448 < 512), e = 119; codes of 256, -128, 0 and 0.75
+    codes, e = oracle.quantise_k_e4m3(_bf16_bits([[1.0, -0.5, 0.0, 3.0 * 2.0 ** -10]]), oracle.BF16)
+    assert e.tolist() == [119] and codes.tolist() == [[0x78, 0xF0, 0x00, 0x34]]
+    # max 448 -> p = 0; 272 and 304 lie halfway between neighbours and go to the even code
+    codes, e = oracle.quantise_k_e4m3(_bf16_bits([[448.0, 272.0, 304.0, -272.0]]), oracle.BF16)
+    assert e.tolist() == [127] and codes.tolist() == [[0x7E, 0x78, 0x7A, 0xF8]]
+    # an all-zero row
+    codes, e = oracle.quantise_k_e4m3(np.zeros((1, 4), np.uint16), oracle.F16)
+    assert e.tolist() == [0] and codes.tolist() == [[0, 0, 0, 0]]
+
+
+def test_quantise_k_matches_torch_rounding_and_scale_rule():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(8)
+    k = W.f32_to_bf16_bits(rng.standard_normal((300, 256)).astype(np.float32) * np.float32(3.0))
+    codes, e = oracle.quantise_k_e4m3(k, oracle.BF16)
+    x = oracle._bits_to_f64(k, oracle.BF16)
+    p = 127 - e.astype(np.int64)
+    y = x * np.ldexp(1.0, p)[:, None]                       # exact in float32 (bf16 times a power of two)
+    m = np.abs(y).max(axis=1)
+    assert (m > 224).all() and (m <= 448).all()             # the row maximum lands in (224, 448]
+    ref = torch.from_numpy(y.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+
+
+def test_quantise_then_dequantise_error_and_fixed_points():
+    rng = np.random.default_rng(9)
+    k = W.f32_to_bf16_bits(rng.standard_normal((200, 128)).astype(np.float32))
+    codes, e = oracle.quantise_k_e4m3(k, oracle.BF16)
+    back = oracle._bits_to_f64(oracle.dequant_k_e4m3(codes[:, None, :], e[:, None], oracle.BF16)[:, 0, :],
+                               oracle.BF16)
+    x = oracle._bits_to_f64(k, oracle.BF16)
+    step = np.ldexp(1.0, 127 - e.astype(np.int64) - 9)[:, None]   # E4M3's subnormal step at the row's scale
+    assert (np.abs(back - x) <= np.maximum(np.abs(x) * 2.0 ** -4, step / 2)).all()
+    # values already of the form e4m3(code) * 2^(e - 127) come back unchanged
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    c0 = finite[rng.integers(0, len(finite), size=(50, 64))]
+    e0 = rng.integers(118, 126, size=50).astype(np.uint8)
+    v = oracle.dequant_k_e4m3(c0[:, None, :], e0[:, None], oracle.BF16)[:, 0, :]
+    c1, e1 = oracle.quantise_k_e4m3(v, oracle.BF16)
+    assert np.array_equal(oracle.dequant_k_e4m3(c1[:, None, :], e1[:, None], oracle.BF16)[:, 0, :], v)
