@@ -760,7 +760,7 @@ def run_lmhead_only(args):
     return 0
 
 
-def main(argv=None):
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -778,7 +778,11 @@ def main(argv=None):
     ap.add_argument("--no-vq", action="store_true", help="skip the quantised-V attention measurement")
     ap.add_argument("--vq-only", action="store_true", help="time only the quantised-V attention calls")
     ap.add_argument("--stage-only", action="store_true", help="time only the host-resident page staging")
-    args = ap.parse_args(argv)
+    return ap
+
+
+def main(argv=None):
+    args = build_parser().parse_args(argv)
     if args.lmhead_only:
         return run_lmhead_only(args)
     if args.delta_only:
