@@ -40,6 +40,9 @@
  *     depended on the bad input are unspecified.  Clear the word before a
  *     step and read it whenever convenient.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - One GPU per process: the kernels that need more than 48 KB of shared
+ *     memory get that limit raised once per process, on the device that is
+ *     current at the first call.  Drive each GPU from its own process.
  */
 #ifndef LUCETREE_H
 #define LUCETREE_H

@@ -1,5 +1,6 @@
 // lucetree_abi.cu -- the extern "C" entry points: argument checks, workspace
 // sizing and kernel launches on the caller's stream.
+#include <atomic>
 #include <cstring>
 
 #include "internal.cuh"
@@ -10,14 +11,16 @@
 namespace lucetree {
 
 int device_sm_count(int device) {
-    static int cache[128] = {0};
+    // calls may come from several host threads: the per-device cache is atomic
+    // (two threads that both miss store the same value)
+    static std::atomic<int> cache[128];
     if (device < 0 || device >= 128) return 1;
-    if (cache[device] == 0) {
-        int n = 0;
+    int n = cache[device].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) n = 1;
-        cache[device] = n;
+        cache[device].store(n, std::memory_order_relaxed);
     }
-    return cache[device];
+    return n;
 }
 
 static int current_device() {
