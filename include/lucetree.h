@@ -90,8 +90,8 @@ typedef enum lucetree_dtype {
 
 /*
  * Arguments of lucetree_verify_attn.  Sizes: B sequences, N tree nodes
- * (1..64), Hq query heads, Hkv KV heads (Hq % Hkv == 0; query head h reads KV
- * head h / (Hq / Hkv)), D head dim (128 or 256).
+ * (1..64), Hq query heads, Hkv KV heads (Hq % Hkv == 0 and Hq / Hkv <= 144;
+ * query head h reads KV head h / (Hq / Hkv)), D head dim (128 or 256).
  */
 typedef struct lucetree_attn_args {
     int dtype;             /* lucetree_dtype of q, pools and tree K/V */
