@@ -261,6 +261,149 @@ def config_dict(cfg):
                    f"between steps): an L2-resident timing, not a contract figure")}
 
 
+# ----------------------------------------------------------------------------- timing helpers
+
+def ms_stats(ms) -> dict:
+    """Mean, median and 90th percentile of per-iteration device times (ms)."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"mean": float(a.mean()), "p50": float(np.percentile(a, 50)), "p90": float(np.percentile(a, 90)),
+            "n": int(a.size)}
+
+
+def issue_step(LT, step, dd, cfg, stream, ev=None):
+    """One verify step through the C-ABI on `stream`: ancestor masks, tree
+    attention, argmax, acceptance, commit.  ev = (before attention, after
+    attention) events, or None."""
+    LT.lucetree_build_anc_mask(dd["parent"], step.anc, step.status, stream)
+    if ev is not None:
+        ev[0].record(stream)
+    LT.lucetree_verify_attn(dd["q"], dd["k_pool"], dd["v_pool"], dd["page_table"], dd["ctx_len"], dd["k_tree"],
+                            dd["v_tree"], step.anc, step.out, step.status, step.ws_attn, lse=step.lse, stream=stream)
+    if ev is not None:
+        ev[1].record(stream)
+    LT.lucetree_argmax(dd["logits"], step.argmax, step.ws_argmax, stream)
+    LT.lucetree_accept(dd["parent"], dd["draft"], step.argmax, cfg.vocab, step.acc_nodes, step.acc_len, step.bonus,
+                       step.status, stream)
+    LT.lucetree_commit(dd["k_tree"], dd["v_tree"], step.acc_nodes, step.acc_len, dd["page_table"], dd["ctx_len"],
+                       step.ctx_out, dd["k_pool"], dd["v_pool"], step.status, stream)
+
+
+def attn_flops(cfg: W.VerifyConfig) -> int:
+    """Algorithmic flops of one attention call: Q.K^T and P.V over the
+    committed prefix, 4 * N * Hq * L * D per sequence."""
+    return sum(4 * cfg.N * cfg.Hq * L * cfg.D for L in cfg.ctx)
+
+
+def peak_tensor_sustained():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured (sustained)"
+    except Exception:
+        return 1700.0, "fallback (sustained)"
+
+
+def device_inputs(cfg: W.VerifyConfig, dev, seed: int, pool_cfg: W.VerifyConfig | None = None, pools: bool = True):
+    """A verify workload on the device: the tree, draft tokens and planted
+    logits from the seeded generator, the committed K/V pools and queries as
+    seeded N(0, 1) draws made on the device (the same distribution the
+    generator uses; the attention time does not depend on the values).
+    pool_cfg: the configuration whose page geometry the pools follow (a
+    larger budget reserves more pages), by default cfg itself."""
+    import torch
+    pc = pool_cfg or cfg
+    meta = W.generate(cfg, seed=seed, with_pools=False)
+    geo = W.generate(pc, seed=seed, with_pools=False, with_logits=False) if pool_cfg is not None else meta
+    tdt = torch.bfloat16 if cfg.dtype == W.BF16 else torch.float16
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + seed)
+    num_pages = sum(W.pages_needed(L, pc.N) for L in pc.ctx) + pc.spare_pages
+
+    def normal(shape):
+        t = torch.empty(shape, dtype=tdt, device=dev)
+        flat = t.view(-1)
+        step = 1 << 26
+        for i in range(0, flat.numel(), step):
+            j = min(flat.numel(), i + step)
+            flat[i:j] = torch.randn(j - i, device=dev, generator=g).to(tdt)
+        return t
+
+    d = dict(q=normal((cfg.B, cfg.N, cfg.Hq, cfg.D)), k_tree=normal((cfg.B, cfg.N, cfg.Hkv, cfg.D)),
+             v_tree=normal((cfg.B, cfg.N, cfg.Hkv, cfg.D)),
+             page_table=torch.from_numpy(geo["page_table"]).to(dev),
+             ctx_len=torch.from_numpy(meta["ctx_len"]).to(dev), parent=torch.from_numpy(meta["parent"]).to(dev),
+             draft=torch.from_numpy(meta["draft"]).to(dev), logits=torch.from_numpy(meta["logits"]).to(dev))
+    if pools:
+        d["k_pool"] = normal((num_pages, cfg.Hkv, W.PAGE, cfg.D))
+        d["v_pool"] = normal((num_pages, cfg.Hkv, W.PAGE, cfg.D))
+    return d
+
+
+def measure_configs(args, dev, stream, rank):
+    """The other workloads, each timed as whole verify steps through the C-ABI
+    with CUDA events around the step and around its attention call: the
+    27B-class 32K / budget 22 (its 128 MiB of K/V about fills L2, so L2 is
+    flushed between steps here, for every workload), 128K / budget 40,
+    256K on permuted pages / budget 22 with the commit into reserved pages,
+    and the 4-sequence sweep {4K, 32K, 128K, 256K} at budgets 1 / 22 / 40 / 64
+    as chains and random trees (planted match 0.7).  Budget 64 is reported
+    against the sustained bf16 tensor peak as well (384 flop per K/V byte)."""
+    import torch
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    peak, peak_kind = peak_hbm()
+    tpeak, tpeak_kind = peak_tensor_sustained()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MiB > L2
+    n = max(5, min(20, args.steps // 100 or 5))
+    todo = [W.GQA27B_32K, W.LONG_128K, W.PAGED_256K]
+    sweep = [c for c in W.sweep_points() if c.p_plant == 0.7 and c.N in (1, 22, 40, 64)]
+    pool64 = [c for c in W.sweep_points() if c.N == 64 and c.tree == "random" and c.p_plant == 0.7][0]
+    out = {}
+    shared = None
+    for cfg in todo + sweep:
+        is_sweep = cfg in sweep
+        if is_sweep:
+            if shared is None:
+                shared = device_inputs(pool64, dev, seed=rank, pool_cfg=pool64)
+            meta = device_inputs(cfg, dev, seed=rank, pool_cfg=pool64, pools=False) if cfg is not pool64 else shared
+            d = dict(meta, k_pool=shared["k_pool"], v_pool=shared["v_pool"])
+            del meta
+        else:
+            d = device_inputs(cfg, dev, seed=rank)
+        step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, device=dev)
+        ctx0 = d["ctx_len"].clone()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                issue_step(LT, step, d, cfg, stream)
+            stream.synchronize()
+            ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(n)]
+            for e in ev:
+                flush.fill_(1)
+                e[0].record(stream)
+                issue_step(LT, step, d, cfg, stream, ev=(e[1], e[2]))
+                e[3].record(stream)
+        torch.cuda.synchronize(dev)
+        assert torch.equal(d["ctx_len"], ctx0)  # the step writes ctx_out, the committed length stays
+        attn = ms_stats([a.elapsed_time(b) for _, a, b, _ in ev])
+        stp = ms_stats([a.elapsed_time(b) for a, _, _, b in ev])
+        ab = attn_bytes(cfg)
+        rec = {"workload": config_dict(cfg)["workload"], "attn_ms": attn, "step_ms": stp,
+               "kv_bytes": cfg.kv_bytes(), "attn_bytes": ab,
+               "attn_GBps": ab / (attn["p50"] * 1e-3) / 1e9,
+               "frac_of_hbm_peak": ab / (attn["p50"] * 1e-3) / 1e9 / peak,
+               "verify_steps_per_s": 1e3 / stp["p50"], "accepted": int(step.acc_len.sum().item()),
+               "device_status": int(step.status.item()),
+               "l2": "a 256 MiB buffer is written between timed steps (L2 flushed)"}
+        if cfg.N == 64:
+            fl = attn_flops(cfg)
+            rec["tensor"] = {"flops": fl, "achieved_tflops": fl / (attn["p50"] * 1e-3) / 1e12, "peak": tpeak,
+                             "peak_kind": tpeak_kind, "frac": fl / (attn["p50"] * 1e-3) / 1e12 / tpeak}
+        out[cfg.name] = rec
+        del d, step
+        torch.cuda.empty_cache()
+    out["peak"], out["peak_kind"] = peak, peak_kind
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_ours(args, cfg):
@@ -291,20 +434,7 @@ def run_ours(args, cfg):
     step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, device=dev)
 
     def one(ev=None, dd=None):
-        dd = d if dd is None else dd
-        LT.lucetree_build_anc_mask(dd["parent"], step.anc, step.status, stream)
-        if ev is not None:
-            ev[0].record(stream)
-        LT.lucetree_verify_attn(dd["q"], dd["k_pool"], dd["v_pool"], dd["page_table"], dd["ctx_len"], dd["k_tree"],
-                                dd["v_tree"], step.anc, step.out, step.status, step.ws_attn, lse=step.lse,
-                                stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        LT.lucetree_argmax(dd["logits"], step.argmax, step.ws_argmax, stream)
-        LT.lucetree_accept(dd["parent"], dd["draft"], step.argmax, cfg.vocab, step.acc_nodes, step.acc_len,
-                           step.bonus, step.status, stream)
-        LT.lucetree_commit(dd["k_tree"], dd["v_tree"], step.acc_nodes, step.acc_len, dd["page_table"],
-                           dd["ctx_len"], step.ctx_out, dd["k_pool"], dd["v_pool"], step.status, stream)
+        issue_step(LT, step, d if dd is None else dd, cfg, stream, ev)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -319,6 +449,7 @@ def run_ours(args, cfg):
     except Exception:
         pass
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    bounds = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(uuid) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
@@ -326,13 +457,17 @@ def run_ours(args, cfg):
     torch.cuda.synchronize(dev)
     t_start.record(stream)
     for k in range(args.steps):
+        bounds[k].record(stream)
         one(evs[k])
+    bounds[args.steps].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clocks = sampler.stop() if sampler else None
     elapsed_ms = t_start.elapsed_time(t_end)
-    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    attn_st = ms_stats([a.elapsed_time(b) for a, b in evs])
+    step_st = ms_stats([bounds[k].elapsed_time(bounds[k + 1]) for k in range(args.steps)])
+    attn_ms = attn_st["mean"]
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
     ms_per_step = elapsed_ms / args.steps
 
@@ -425,7 +560,7 @@ def run_ours(args, cfg):
         "verify_steps_per_s": world * 1e3 / ms_per_step,
         "verify_steps_per_s_graph": (world * 1e3 / graph_ms) if graph_ms else None,
         "hbm_pct_of_peak": 100.0 * (sb / (ms_per_step * 1e-3) / 1e9) / peak,
-        "attn_ms_per_call": attn_ms,
+        "attn_ms_per_call": attn_ms, "attn_ms_stats": attn_st, "step_ms_stats": step_st,
         "accepted_per_step": acc_total, "device_status": status,
         "clocks": clocks,
         "e2e": {"value": world * sb / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -451,6 +586,11 @@ def run_ours(args, cfg):
         line["stage_pages"] = measure_stage(args, dev, stream, rank)
     if not args.no_vq and cfg.D == 256:
         line["quantised_v"] = measure_vq(args, dev, stream, rank, d, step, cfg)
+    if not args.no_configs:
+        for held in (d, host, bufs[1]):
+            held.clear()  # the other workloads need the device memory
+        torch.cuda.empty_cache()
+        line["configs"] = measure_configs(args, dev, stream, rank)
     print(json.dumps(line), flush=True)
     if dist.is_initialized():
         dist.destroy_process_group()
@@ -488,13 +628,14 @@ def measure_lmhead(args, dev, stream, rank, with_cpu=True):
         LT.lucetree_lmhead_argmax(hidden, weight, out, st, ws, stream=stream)
         evs[k][1].record(stream)
     torch.cuda.synchronize(dev)
-    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    st_ms = ms_stats([a.elapsed_time(b) for a, b in evs])
+    ms = st_ms["mean"]
     nbytes = lc.weight_bytes() + lc.rows * lc.d_model * 2 + lc.rows * 4
     peak, peak_kind = peak_hbm()
     achieved = nbytes / (ms * 1e-3) / 1e9
     res = {
         "workload": f"{lc.name}: rows {lc.rows}, d_model {lc.d_model}, vocab {lc.vocab}, bf16",
-        "ms_per_call": ms, "calls_timed": n, "device_status": int(st.item()),
+        "ms_per_call": ms, "ms_stats": st_ms, "calls_timed": n, "device_status": int(st.item()),
         "tflops": 2.0 * lc.rows * lc.d_model * lc.vocab / (ms * 1e-3) / 1e12,
         "roofline": {"bound": "hbm", "kernel": "lucetree_lmhead_argmax", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
@@ -638,10 +779,11 @@ def measure_vq(args, dev, stream, rank, d, step, cfg):
                 call()
                 e1.record(stream)
         torch.cuda.synchronize(dev)
-        ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+        st_ms = ms_stats([e0.elapsed_time(e1) for e0, e1 in evs])
+        ms = st_ms["mean"]
         nbytes = int(L * cfg.Hkv * cfg.D * (2 + vbytes) + L * cfg.Hkv
                      + cfg.B * cfg.N * cfg.Hq * cfg.D * 2 + cfg.B * cfg.N * cfg.Hq * cfg.D * 4 + 4 * L // 64)
-        res[name] = {"ms_per_call": ms, "device_status": int(step.status.item()),
+        res[name] = {"ms_per_call": ms, "ms_stats": st_ms, "device_status": int(step.status.item()),
                      "algorithmic_bytes_per_launch": nbytes, "achieved_GBps": nbytes / (ms * 1e-3) / 1e9,
                      "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
                      "kv_bytes_per_token": cfg.Hkv * cfg.D * (2 + vbytes) + cfg.Hkv}
@@ -760,6 +902,17 @@ def run_lmhead_only(args):
     return 0
 
 
+def run_configs_only(args):
+    import torch
+    from speculative_decoding_tree_ddtree_gb300.build import build
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    print(json.dumps({"configs": measure_configs(args, dev, stream, 0)}), flush=True)
+    return 0
+
+
 def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -778,6 +931,9 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--no-vq", action="store_true", help="skip the quantised-V attention measurement")
     ap.add_argument("--vq-only", action="store_true", help="time only the quantised-V attention calls")
     ap.add_argument("--stage-only", action="store_true", help="time only the host-resident page staging")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (32K, 128K/b40, 256K paged, the 4-sequence sweep)")
+    ap.add_argument("--configs-only", action="store_true", help="time only the other workloads")
     return ap
 
 
@@ -791,6 +947,8 @@ def main(argv=None):
         return run_stage_only(args)
     if args.vq_only:
         return run_vq_only(args)
+    if args.configs_only:
+        return run_configs_only(args)
     cfg = W.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)

@@ -40,9 +40,10 @@
  *     depended on the bad input are unspecified.  Clear the word before a
  *     step and read it whenever convenient.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
- *   - One GPU per process: the kernels that need more than 48 KB of shared
- *     memory get that limit raised once per process, on the device that is
- *     current at the first call.  Drive each GPU from its own process.
+ *   - Calls act on the device (and context) current in the calling thread.
+ *     One process may drive several GPUs: the kernels that need more than
+ *     48 KB of shared memory get that limit raised once per context, and the
+ *     split plans follow the current device's SM count.
  */
 #ifndef LUCETREE_H
 #define LUCETREE_H
@@ -139,6 +140,9 @@ LUCETREE_API lucetree_status lucetree_verify_attn_workspace(int B, int N, int Hq
 LUCETREE_API lucetree_status lucetree_verify_attn(const lucetree_attn_args* args, void* workspace, size_t workspace_bytes,
                                      void* stream);
 
+/* Size of the device array that backs lucetree_verify_attn_noalloc: 32 MiB. */
+#define LUCETREE_NOALLOC_SCRATCH_BYTES (32u << 20)
+
 /*
  * lucetree_verify_attn without a caller-supplied workspace.  The Lucebox
  * pages have no counterpart to this call; it exists for callers that cannot
@@ -147,14 +151,17 @@ LUCETREE_API lucetree_status lucetree_verify_attn(const lucetree_attn_args* args
  * that only receives raw device pointers and has no allocator of its own.
  * It computes exactly what lucetree_verify_attn computes (same kernels), and
  * allocates nothing: the split-K partials go to a file-scope device array of
- * 32 MiB (33554432 bytes) inside this library, which every GPU that loads the
- * library keeps until the process exits.
+ * 32 MiB (33554432 bytes, LUCETREE_NOALLOC_SCRATCH_BYTES) inside this
+ * library, which every GPU that loads the library keeps until the process
+ * exits.
  *   - Sizes whose workspace (lucetree_verify_attn_workspace) exceeds 32 MiB
  *     are rejected with LUCETREE_ERR_WORKSPACE before anything is launched;
  *     other errors are those of lucetree_verify_attn.
- *   - The first call on a device (made with that device current) looks up the
- *     array's device address once; make that first call before any stream
- *     capture.
+ *   - Every call looks up the array's device address in the calling thread's
+ *     current context, so a device reset or a second context on the device
+ *     is followed correctly.  The first call in a context (made with the
+ *     target device current) may load the library's device code to do so;
+ *     make that first call before any stream capture.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents (the kernels need none of it cleared).  Calls whose
  *     work overlaps on the GPU (different streams, or host threads without

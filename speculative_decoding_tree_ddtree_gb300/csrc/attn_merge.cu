@@ -109,6 +109,14 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(AttnLaunch L) {
     // ---- committed prefix: partials of every CTA that covered this segment
     // (this kernel is launched as a programmatic dependent of the prefix
     // kernel: everything above overlaps its tail, nothing below may)
+    //
+    // The reads above (q, anc_mask, tree K/V) and the status OR come before
+    // this kernel's own wait.  They are safe by transitivity: the prefix
+    // kernel triggers its dependents only after its own pdl_wait() has
+    // returned, i.e. after every kernel before it on the stream (the one that
+    // wrote the masks, the caller's uploads) has completed and flushed.  So
+    // once any block of this kernel runs, those inputs are final.  This holds
+    // only while the prefix kernel keeps pdl_trigger() after pdl_wait().
     pdl_wait();
     const int Lb = seq_len(a.ctx_len, b, p.max_pages, (i == 0 && h == 0 && threadIdx.x == 0) ? a.status : nullptr);
     int count = 0, c_lo = 0;

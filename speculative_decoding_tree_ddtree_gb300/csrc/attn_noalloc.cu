@@ -1,8 +1,6 @@
 // attn_noalloc.cu -- lucetree_verify_attn_noalloc: tree-verify attention whose
 // split-K scratch lives in a fixed device array owned by the library, for
 // callers that cannot allocate device memory themselves.
-#include <atomic>
-
 #include "internal.cuh"
 
 namespace lucetree {
@@ -11,24 +9,23 @@ namespace {
 // Upper bound on the per-call scratch (the partial (O, max, sum) triples of the
 // split-K plan).  One sequence at 24 / 4 heads, D = 256 and a 22-node tree
 // needs about 21 MB on a 152-SM GPU; four sequences at 64 nodes about 27 MB.
-constexpr size_t kNoAllocScratchBytes = 32u << 20;
+constexpr size_t kNoAllocScratchBytes = LUCETREE_NOALLOC_SCRATCH_BYTES;
 
 // File-scope scratch.  Every GPU on which this library's module is loaded
-// holds these 32 MiB until the process exits.  In host code the name is only
+// holds these bytes until the process exits.  In host code the name is only
 // a host-side stand-in: the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 128;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
-
-// Resolves the scratch's device address on the current device (once per device).
-lucetree_status scratch_for_current_device(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LUCETREE_ERR_CUDA;
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LUCETREE_ERR_CUDA;
-        g_scratch_addr[dev].store(p, std::memory_order_release);
+// The scratch's device address in the calling thread's current context.  It
+// is looked up on every call: the address belongs to one context's copy of
+// the module, and a device reset (or another context on the same device)
+// gives the array a new one.  After the first call in a context this is a
+// host-side table lookup; the first one may load the module.
+lucetree_status scratch_for_current_context(void** out) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();  // leave no error behind for the caller's next runtime call
+        return LUCETREE_ERR_CUDA;
     }
     *out = p;
     return LUCETREE_OK;
@@ -44,7 +41,7 @@ extern "C" lucetree_status lucetree_verify_attn_noalloc(const lucetree_attn_args
     if (st != LUCETREE_OK) return st;
     if (need > lucetree::kNoAllocScratchBytes) return LUCETREE_ERR_WORKSPACE;
     void* scratch = nullptr;
-    st = lucetree::scratch_for_current_device(&scratch);
+    st = lucetree::scratch_for_current_context(&scratch);
     if (st != LUCETREE_OK) return st;
     // The attention kernels need no zeroed scratch: every partial they read is
     // written earlier in the same call.

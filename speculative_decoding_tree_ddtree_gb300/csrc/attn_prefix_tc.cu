@@ -7,27 +7,6 @@
 
 namespace lucetree {
 
-namespace {
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-}  // namespace
-
 int prefix_grid_ctas(int device) { return device_sm_count(device); }
 
 bool prefix_shape_supported(const lucetree_attn_args& a) {
@@ -41,7 +20,7 @@ bool prefix_shape_supported(const lucetree_attn_args& a) {
 cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream) {
     const lucetree_attn_args& a = L.a;
     const PlanDims& p = L.plan;
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     const CUtensorMapDataType dt =
         a.dtype == LUCETREE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;

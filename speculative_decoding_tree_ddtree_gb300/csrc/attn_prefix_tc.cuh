@@ -330,7 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // inputs may come from the previous kernel on the stream: wait for it, then
     // let the merge kernel start its blocks as SMs free up (it waits for this
-    // grid before reading partials)
+    // grid before reading partials).  The trigger must stay after the wait: the
+    // merge kernel reads the ancestor masks, queries and tree K/V before its own
+    // wait, relying on this kernel having waited for their producers first.
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
     const long long nT = total_tiles(p, a.ctx_len);
@@ -925,12 +927,9 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const CUten
                        const AttnLaunch& L, cudaStream_t stream) {
     using Lay = Layout<D, RGP>;
     auto kern = prefix_tc_kernel<D, BF16, RGP, VQ>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static SmemLimitSeen seen;
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), Lay::kBytes, seen);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid_ctas(L.plan)), dim3(kThreads), Lay::kBytes, stream, tk, tv, tq, tve, L);
 }
 

@@ -370,28 +370,24 @@ __global__ void __launch_bounds__(kThreads) delta_commit_kernel(lucetree_delta_a
                 make_float4(S[m][j4], S[m][j4 + 1], S[m][j4 + 2], S[m][j4 + 3]);
 }
 
-template <typename K>
-cudaError_t set_smem(K kern, size_t smem, size_t& configured) {
-    if (smem <= configured) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) configured = smem;
-    return e;
-}
-
 template <bool BF16>
 cudaError_t launch_tree_t(const lucetree_delta_args& a, cudaStream_t stream) {
-    static size_t configured = 0;
+    // the limit is raised to the largest tree the kernel takes (64 nodes), so
+    // launches of different sizes from several threads never lower it
+    static SmemLimitSeen seen;
     const size_t smem = delta_tree_smem_bytes(a.N);
-    cudaError_t e = set_smem(delta_tree_kernel<BF16>, smem, configured);
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(delta_tree_kernel<BF16>),
+                                     (int)delta_tree_smem_bytes(64), seen);
     if (e != cudaSuccess) return e;
     return launch_pdl(delta_tree_kernel<BF16>, dim3(a.dv / kC, a.Hv, a.B), dim3(kThreads), smem, stream, a);
 }
 
 template <bool BF16>
 cudaError_t launch_commit_t(const lucetree_delta_args& a, cudaStream_t stream) {
-    static size_t configured = 0;
+    static SmemLimitSeen seen;
     const size_t smem = stage_bytes(a.N, false, kWarps * kC);
-    cudaError_t e = set_smem(delta_commit_kernel<BF16>, smem, configured);
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(delta_commit_kernel<BF16>),
+                                     (int)stage_bytes(64, false, kWarps * kC), seen);
     if (e != cudaSuccess) return e;
     const int per_cta = kWarps * kC;
     return launch_pdl(delta_commit_kernel<BF16>, dim3((a.dv + per_cta - 1) / per_cta, a.Hv, a.B), dim3(kThreads),

@@ -1,10 +1,13 @@
 // internal.cuh -- shared definitions of the lucetree CUDA library (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <atomic>
 
 #include "lucetree.h"
 
@@ -198,6 +201,31 @@ cudaError_t launch_argmax(const float* logits, int rows, int vocab, long long ro
                           void* ws, int device, cudaStream_t stream);
 
 int device_sm_count(int device);
+
+// ---------------------------------------------------------------------------
+// Host helpers shared by the launchers.  Calls may come from several host
+// threads, so every lazily filled cache is atomic or a thread-safe static.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 128;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled, resolved from the driver once per process (null
+// when the driver does not provide it).
+EncodeTiledFn tensor_map_encoder();
+
+// Per-device record of the CUDA context in which a kernel's dynamic
+// shared-memory limit was last raised (0 = never).
+typedef std::atomic<unsigned long long> SmemLimitSeen[kMaxDevices];
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` in the current
+// context.  The attribute belongs to the context's copy of the module, so it
+// is set again whenever the calling thread's context differs from the one
+// recorded for this device (another device, or a context made after a device
+// reset).  `bytes` must be the largest amount any launch of the kernel uses.
+cudaError_t raise_smem_limit(const void* kernel, int bytes, SmemLimitSeen& seen);
 
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every library kernel is launched so that it

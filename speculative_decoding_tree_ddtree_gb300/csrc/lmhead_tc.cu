@@ -7,27 +7,6 @@
 
 namespace lucetree {
 
-namespace {
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-}  // namespace
-
 // padded row count: the smallest instantiated multiple of 16 >= rows
 int lmhead_padded_rows(int rows) {
     static const int kRP[] = {16, 32, 48, 64, 96, 128, 192, 256};
@@ -39,7 +18,7 @@ int lmhead_padded_rows(int rows) {
 size_t lmhead_workspace_bytes(int rows) { return ((size_t)rows * 8 + 255) / 256 * 256 + 256; }
 
 cudaError_t launch_lmhead(const lucetree_lmhead_args& a, void* ws, cudaStream_t stream) {
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     const CUtensorMapDataType dt =
         a.dtype == LUCETREE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;

@@ -10,12 +10,9 @@ cudaError_t launch_rp(const CUtensorMap& tw, const CUtensorMap& th, const lmhead
                       cudaStream_t stream) {
     using Lay = lmhead::Layout<RP>;
     auto kern = lmhead::lmhead_kernel<true, RP>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static SmemLimitSeen seen;
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), Lay::kBytes, seen);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(ctas), dim3(lmhead::kThreads), Lay::kBytes, stream, tw, th, a);
 }
 

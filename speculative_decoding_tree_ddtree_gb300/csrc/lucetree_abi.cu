@@ -23,6 +23,69 @@ int device_sm_count(int device) {
     return n;
 }
 
+EncodeTiledFn tensor_map_encoder() {
+    // a function-local static is initialised exactly once even when several threads arrive together
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return nullptr;
+    }();
+    return fn;
+}
+
+namespace {
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Process-unique id of the calling thread's current context, 0 if unknown.
+unsigned long long current_context_id() {
+    struct Fns {
+        CtxGetCurrentFn get_current = nullptr;
+        CtxGetIdFn get_id = nullptr;
+    };
+    static const Fns fns = []() {
+        Fns f;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_id = reinterpret_cast<CtxGetIdFn>(p);
+        return f;
+    }();
+    if (!fns.get_current || !fns.get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (fns.get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (fns.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+}  // namespace
+
+cudaError_t raise_smem_limit(const void* kernel, int bytes, SmemLimitSeen& seen) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    // the first runtime call may be the one that makes the primary context current
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && dev >= 0 && dev < kMaxDevices && seen[dev].load(std::memory_order_acquire) == ctx)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    const unsigned long long now = current_context_id();
+    if (now != 0 && dev >= 0 && dev < kMaxDevices) seen[dev].store(now, std::memory_order_release);
+    return cudaSuccess;
+}
+
 static int current_device() {
     int d = 0;
     if (cudaGetDevice(&d) != cudaSuccess) return 0;

@@ -399,7 +399,7 @@ class VerifyStep:
 
 # ---------------------------------------------------------------- allocation-free variant
 
-NOALLOC_SCRATCH_BYTES = 32 << 20
+NOALLOC_SCRATCH_BYTES = 32 << 20  # LUCETREE_NOALLOC_SCRATCH_BYTES of include/lucetree.h
 
 
 def lucetree_verify_attn_noalloc(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status,
@@ -407,8 +407,9 @@ def lucetree_verify_attn_noalloc(q, k_pool, v_pool, page_table, ctx_len, k_tree,
     """lucetree_verify_attn for callers that cannot allocate device memory: the
     split-K scratch is a fixed 32 MiB device array inside the library (shared
     by every call on a device; calls that overlap on the GPU race on it).  The
-    first call on a device looks up that array's address, so make it before
-    any stream capture.  Shapes whose workspace would exceed 32 MiB raise."""
+    first call in a context may load the library's device code to find that
+    array, so make it before any stream capture.  Shapes whose workspace
+    would exceed 32 MiB raise."""
     B, N, Hq, D = q.shape
     Hkv = k_pool.shape[1]
     need = lucetree_verify_attn_workspace(B, N, Hq, Hkv, D)

@@ -105,3 +105,13 @@ def test_binding_rejects_host_tensors():
     from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
     with pytest.raises(LT.LucetreeError):
         LT._ptr(torch.zeros(4))
+
+
+def test_noalloc_scratch_size_matches_header():
+    """The binding refuses oversized shapes before calling the library; its
+    limit must be the header's LUCETREE_NOALLOC_SCRATCH_BYTES."""
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    src = open(os.path.join(ROOT, "include", "lucetree.h")).read()
+    m = re.search(r"#define\s+LUCETREE_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "LUCETREE_NOALLOC_SCRATCH_BYTES not found"
+    assert LT.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

@@ -2,7 +2,8 @@
 
 Bar: for every compared row, max_d |gpu - oracle| / max_d |oracle| <= 2e-3
 (bf16 / fp16 inputs, fp32 accumulation; the tolerance the workload states).
-Full sizes are compared on seeded row samples the oracle computes one by one.
+Every output row is compared, at every size, including the five workloads'
+full sizes and every (budget, tree shape) pair of the concurrent sweep.
 """
 import numpy as np
 import pytest
@@ -54,7 +55,7 @@ def test_several_key_segments_per_cta(cuda_dev, dtype, D):
     cfg = W.VerifyConfig("multiseg", ctx=(4000, 3000, 2000, 4100, 130, 5000, 64, 3333), Hq=16, Hkv=4, D=D,
                          dtype=dtype, N=9, tree="random", branch_cap=3, vocab=512, paged="permuted", spare_pages=4)
     inp = W.generate(cfg, seed=31)
-    _check(cfg, inp, rows=W.sample_rows(cfg, 160))
+    _check(cfg, inp)
 
 
 def test_bf16_v_beyond_fp16_range_is_flagged_nonfinite(cuda_dev):
@@ -79,36 +80,42 @@ def test_budgets_cover_row_groups(cuda_dev, N, shape):
     _check(cfg, W.generate(cfg, seed=N))
 
 
-def test_gqa27b_32k_sampled(cuda_dev):
+def test_gqa27b_32k_all_rows(cuda_dev):
     cfg = W.GQA27B_32K
-    _check(cfg, cached_inputs(cfg), rows=W.sample_rows(cfg, 96))
+    _check(cfg, cached_inputs(cfg))
 
 
 @pytest.mark.slow
-def test_long_128k_b40_sampled(cuda_dev):
+def test_long_128k_b40_all_rows(cuda_dev):
     cfg = W.LONG_128K
-    _check(cfg, cached_inputs(cfg), rows=W.sample_rows(cfg, 48))
+    _check(cfg, cached_inputs(cfg))
 
 
 @pytest.mark.slow
-def test_headline_128k_b22_sampled(cuda_dev):
+def test_headline_128k_b22_all_rows(cuda_dev):
     # the workload bench.py times: one sequence, 131072 committed tokens on
     # permuted pages, budget 22 (one row group of 132 rows per KV head)
     cfg = W.HEADLINE_128K_B22
-    _check(cfg, cached_inputs(cfg), rows=W.sample_rows(cfg, 48))
+    _check(cfg, cached_inputs(cfg))
 
 
 @pytest.mark.slow
-def test_paged_256k_sampled(cuda_dev):
+def test_paged_256k_all_rows(cuda_dev):
     cfg = W.PAGED_256K
-    _check(cfg, cached_inputs(cfg), rows=W.sample_rows(cfg, 32))
+    _check(cfg, cached_inputs(cfg))
+
+
+SWEEP_SHAPES = [(1, "chain"), (8, "chain"), (8, "random"), (22, "chain"), (22, "random"), (40, "chain"),
+                (40, "random"), (64, "chain"), (64, "random")]
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("N,shape", [(1, "chain"), (22, "random"), (64, "chain")])
-def test_concurrent_sweep_points_sampled(cuda_dev, N, shape):
+@pytest.mark.parametrize("N,shape", SWEEP_SHAPES)
+def test_concurrent_sweep_point_all_rows(cuda_dev, N, shape):
+    # four ragged sequences {4K, 32K, 128K, 256K} in one permuted pool; the
+    # attention rows do not depend on the planting probability (logits only)
     cfg = [c for c in W.sweep_points() if c.N == N and c.tree == shape and c.p_plant == 0.7][0]
-    _check(cfg, W.generate(cfg, seed=3), rows=W.sample_rows(cfg, 24), lse=False)
+    _check(cfg, W.generate(cfg, seed=3, with_logits=False), lse=N in (1, 64))
 
 
 def test_non_ancestor_tree_kv_is_invisible(cuda_dev):

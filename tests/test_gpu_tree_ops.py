@@ -245,3 +245,51 @@ def test_full_step_matches_oracle(cuda_dev):
     assert np.array_equal(step.acc_len.cpu().numpy(), alen)
     assert np.array_equal(step.bonus.cpu().numpy(), bonus)
     assert step.ctx_out.cpu().numpy()[0] == inp["ctx_len"][0] + alen[0]
+
+
+@pytest.mark.slow
+def test_argmax_and_accept_every_sweep_point_on_gpu(cuda_dev):
+    """The sweep's 27 points: argmax on the GPU bit-exact against the oracle's
+    linear scan, then acceptance from the GPU's own argmax."""
+    import torch
+    LT = _lt()
+    for cfg in W.sweep_points():
+        inp = W.generate(cfg, seed=5, with_pools=False)
+        rows = cfg.B * (cfg.N + 1)
+        xt = torch.from_numpy(inp["logits"]).cuda()
+        out = torch.full((cfg.B, cfg.N + 1), -7, dtype=torch.int32, device="cuda")
+        ws = torch.empty(LT.lucetree_argmax_workspace(rows, cfg.vocab), dtype=torch.uint8, device="cuda")
+        LT.lucetree_argmax(xt, out, ws)
+        am = oracle.argmax(inp["logits"])
+        assert np.array_equal(out.cpu().numpy(), am), cfg.name
+        acc, alen, bonus, st = _gpu_accept(inp["parent"], inp["draft"], out.cpu().numpy(), cfg.vocab)
+        racc, ralen, rbonus = oracle.accept(inp["parent"], inp["draft"], am)
+        assert st == 0
+        assert np.array_equal(acc, racc) and np.array_equal(alen, ralen) and np.array_equal(bonus, rbonus), cfg.name
+
+
+@pytest.mark.slow
+def test_full_step_sweep_point_full_pool_compare(cuda_dev):
+    """One whole step on the 4-sequence sweep pool (budget 40, random tree,
+    planted match 0.95): argmax, acceptance and the commit are bit-exact, and
+    every byte of both 1.6 GiB pools equals the oracle's commit."""
+    import torch
+    LT = _lt()
+    cfg = [c for c in W.sweep_points() if c.N == 40 and c.tree == "random" and c.p_plant == 0.95][0]
+    inp = W.generate(cfg, seed=11)
+    d = to_device(inp, cfg)
+    step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab)
+    step.run(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"],
+             d["parent"], d["draft"], d["logits"])
+    torch.cuda.synchronize()
+    am = oracle.argmax(inp["logits"])
+    acc, alen, bonus = oracle.accept(inp["parent"], inp["draft"], am)
+    assert alen.sum() > cfg.B  # the planting makes multi-node paths
+    assert step.status.item() == 0
+    assert np.array_equal(step.argmax.cpu().numpy(), am)
+    assert np.array_equal(step.acc_nodes.cpu().numpy(), acc)
+    assert np.array_equal(step.acc_len.cpu().numpy(), alen) and np.array_equal(step.bonus.cpu().numpy(), bonus)
+    kp, vp, ctx = oracle.commit(inp, acc, alen, inplace=True)
+    assert np.array_equal(step.ctx_out.cpu().numpy(), ctx)
+    assert np.array_equal(bits16(d["k_pool"]), kp)
+    assert np.array_equal(bits16(d["v_pool"]), vp)
