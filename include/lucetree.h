@@ -19,7 +19,8 @@
  *   lucetree_accept       longest matching root path, greedy
  *   lucetree_commit       copy accepted K/V into the pool, advance lengths
  * plus lucetree_build_anc_mask, which turns a parent array into the ancestor
- * bitmasks verify_attn consumes, and lucetree_lmhead_argmax, which replaces
+ * bitmasks verify_attn consumes; lucetree_verify_step runs all of them as one
+ * call in two launches.  lucetree_lmhead_argmax replaces
  * the logits + lucetree_argmax pair by the lm_head projection with a fused
  * argmax.  For targets with recurrent (gated delta rule) layers,
  * lucetree_delta_tree advances a layer's state along the tree and
@@ -234,6 +235,50 @@ typedef struct lucetree_commit_args {
  * [0, N)), BAD_PAGE, BAD_CTX; copying stops at the first bad entry.
  */
 LUCETREE_API lucetree_status lucetree_commit(const lucetree_commit_args* args, void* stream);
+
+/* Arguments of lucetree_verify_step (sizes as in lucetree_attn_args). */
+typedef struct lucetree_step_args {
+    lucetree_attn_args attn; /* as for lucetree_verify_attn, except: attn.anc_mask is not read (the step
+                                derives each node's ancestors from `parent`; NULL is fine), and the pools
+                                are also written (the commit) */
+    const int32_t* parent;   /* [B][N], parent[b][i] in [-1, i) (-1 = the root) */
+    const int32_t* draft;    /* [B][N] draft token of each node */
+    const float* logits;     /* [B][N + 1][vocab] fp32; row 0 = the root, row j + 1 = node j */
+    int vocab;
+    int32_t* argmax;         /* [B][N + 1] out, as lucetree_argmax */
+    int32_t* acc_nodes;      /* [B][N] out, as lucetree_accept */
+    int32_t* acc_len;        /* [B] out */
+    int32_t* bonus;          /* [B] out */
+    int32_t* ctx_len_out;    /* [B] out: attn.ctx_len + accepted count; must not alias attn.ctx_len */
+} lucetree_step_args;
+
+/*
+ * Workspace bytes lucetree_verify_step needs for these sizes on the CURRENT
+ * device.  Its first bytes past the attention partials hold counters that
+ * must be ZERO before the first call on a workspace (allocate it zeroed);
+ * every call leaves them zero again.  256-byte aligned.
+ */
+LUCETREE_API lucetree_status lucetree_verify_step_workspace(int B, int N, int Hq, int Hkv, int D, int vocab,
+                                                            size_t* bytes);
+
+/*
+ * The whole verify step in one call: what lucetree_build_anc_mask,
+ * lucetree_verify_attn, lucetree_argmax, lucetree_accept and lucetree_commit
+ * compute in sequence, with the same results, in two launches.  The first is
+ * the attention's split-K prefix kernel; the second runs the argmax chunks
+ * (while the prefix kernel's last CTAs still stream K/V), the acceptance and
+ * commit of each sequence (by the CTA that completes its last argmax row,
+ * after the prefix kernel has completed) and the attention merge, with each
+ * node's ancestors walked from `parent`.  The pages describe these steps
+ * (greedy verification of the whole tree, then KV rollback of the rejected
+ * nodes: "Lucebox Hub", section "Speculative decoding 계층"; forum post,
+ * section "Lucebox 설치 및 실행"); fusing them is this library's.
+ * Errors: those of the five calls; INVALID_ARG also when ctx_len_out aliases
+ * attn.ctx_len; UNSUPPORTED when B * (N + 1) > 65535.  Device checks as the
+ * five calls (BAD_PARENT is raised once per bad node).
+ */
+LUCETREE_API lucetree_status lucetree_verify_step(const lucetree_step_args* args, void* workspace,
+                                                  size_t workspace_bytes, void* stream);
 
 /* V storage formats of lucetree_verify_attn_vq (K stays in the args' dtype). */
 #define LUCETREE_V_SAME 0 /* V in the args' 16-bit dtype (lucetree_verify_attn) */

@@ -1,0 +1,206 @@
+// attn_merge.cuh -- tree block + log-sum-exp merge of tree-verify attention,
+// as a CTA device routine shared by the merge kernel and the fused step.
+//
+// One block per output row (b, node i, head h).  The warps share the softmax
+// over the tree keys j with bit j of anc_mask[b][i] set (the node's ancestors
+// and itself) and the prefix partials (O, max, sum) that the split-K prefix
+// kernel left for this row's key segment; the block writes out = O / sum and
+// lse = ln(sum) + max.  Maxima are kept in the log2 domain
+// (scores pre-multiplied by log2 e), so every rescale is one exp2.
+//
+// The partials are independent: their maxima are reduced first (one thread
+// per partial), then warp w adds the weighted partial rows w, w + 8, ... with
+// several 16-byte loads in flight per lane, and the eight warp sums are added
+// through shared memory.  A block reads about 40 partial rows of D floats, so
+// spreading them over eight warps keeps enough loads in flight to stream the
+// partials at memory speed instead of one dependent row at a time.
+#pragma once
+
+#include "internal.cuh"
+
+namespace lucetree {
+
+namespace merge {
+
+__device__ inline float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ inline float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kUnroll = 2;  // partial rows per warp iteration (2 x D/32 floats per lane in flight)
+
+template <typename T, int D>
+__device__ inline void load_slice(const T* p, float (&out)[D / 32]) {
+    if constexpr (D / 32 == 8) load8_f32<T>(p, out);
+    else load4_f32<T>(p, out);
+}
+
+template <int DPL>
+__device__ inline void load_partial(const float* op, float (&v)[DPL]) {
+    const float4 a = *reinterpret_cast<const float4*>(op);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    if constexpr (DPL == 8) {
+        const float4 b = *reinterpret_cast<const float4*>(op + 4);
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+
+// One output row (b, node i, head h) by the whole CTA (kThreads threads).
+// anc: the node's ancestor-or-self mask.  s_o: kWarps x D floats and s_red:
+// kWarps floats of shared memory.  Runs the tree block, then pdl_wait(), then
+// the log-sum-exp merge of the prefix partials.
+template <typename T, int D>
+__device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, uint64_t anc, float (*s_o)[D],
+                                          float* s_red) {
+    constexpr int DPL = D / 32;
+    const lucetree_attn_args& a = L.a;
+    const PlanDims& p = L.plan;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = (int)(row % p.Hq);
+    const int i = (int)((row / p.Hq) % p.N);
+    const int b = (int)(row / ((long long)p.Hq * p.N));
+    const int g = h / p.G;
+    const int rg = i / p.rg.NPG;
+    const int rl = (i - rg * p.rg.NPG) * p.G + (h % p.G);
+    const int s = b * p.Hkv + g;
+
+    // ---- tree block: keys of the node's ancestors and itself, the k-th such
+    // key (in node order) handled by warp k % kWarps with its own running
+    // max, sum and output slice
+    float o[DPL];
+#pragma unroll
+    for (int x = 0; x < DPL; ++x) o[x] = 0.f;
+    float m_t = -INFINITY, l_t = 0.f;
+    {
+        float qf[DPL];
+        load_slice<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)row * D + lane * DPL, qf);
+        if (p.N < 64) anc &= (1ull << p.N) - 1ull;
+        if (!((anc >> i) & 1ull) && threadIdx.x == 0) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
+        const T* kt = reinterpret_cast<const T*>(a.k_tree);
+        const T* vt = reinterpret_cast<const T*>(a.v_tree);
+        int rank = 0;
+        while (anc) {
+            const int j = __ffsll((long long)anc) - 1;
+            anc &= anc - 1ull;
+            if ((rank++ % kWarps) != warp) continue;
+            const size_t base = (((size_t)b * p.N + j) * p.Hkv + g) * D + lane * DPL;
+            float kf[DPL], vf[DPL];
+            load_slice<T, D>(kt + base, kf);
+            load_slice<T, D>(vt + base, vf);
+            float dot = 0.f;
+#pragma unroll
+            for (int x = 0; x < DPL; ++x) dot = fmaf(qf[x], kf[x], dot);
+            const float sc = warp_sum(dot) * L.scale_log2;
+            const float mn = fmaxf(m_t, sc);
+            const float alpha = exp2f(m_t - mn), pj = exp2f(sc - mn);
+            l_t = l_t * alpha + pj;
+#pragma unroll
+            for (int x = 0; x < DPL; ++x) o[x] = fmaf(o[x], alpha, pj * vf[x]);
+            m_t = mn;
+        }
+    }
+
+    // ---- committed prefix: partials of every CTA that covered this segment
+    // (this kernel is launched as a programmatic dependent of the prefix
+    // kernel: everything above overlaps its tail, nothing below may)
+    //
+    // The reads above (q, anc_mask, tree K/V) and the status OR come before
+    // this kernel's own wait.  They are safe by transitivity: the prefix
+    // kernel triggers its dependents only after its own pdl_wait() has
+    // returned, i.e. after every kernel before it on the stream (the one that
+    // wrote the masks, the caller's uploads) has completed and flushed.  So
+    // once any block of this kernel runs, those inputs are final.  This holds
+    // only while the prefix kernel keeps pdl_trigger() after pdl_wait().
+    pdl_wait();
+    const int Lb = seq_len(a.ctx_len, b, p.max_pages, (i == 0 && h == 0 && threadIdx.x == 0) ? a.status : nullptr);
+    int count = 0, c_lo = 0;
+    long long nT = 0;
+    if (Lb > 0) {
+        nT = total_tiles(p, a.ctx_len);
+        const long long first = segment_offset(p, a.ctx_len, s);
+        const long long last = first + tiles_of(Lb) - 1;
+        c_lo = cta_of_tile(first, nT, p.Cg);
+        count = cta_of_tile(last, nT, p.Cg) - c_lo + 1;
+    }
+    const size_t sf = slot_floats(p);
+    const float* ws = L.ws + slot_index(p, rg, c_lo, s) * sf;
+    // with fewer tiles than CTAs some CTAs own no tile and write no partial
+    auto has_partial = [&](int k) {
+        return k < count && cta_begin(c_lo + k, nT, p.Cg) != cta_begin(c_lo + k + 1, nT, p.Cg);
+    };
+
+    // pass 1: the common shift (maximum over the tree parts and every partial)
+    float mk_local = m_t;
+    for (int k = threadIdx.x; k < count; k += kThreads)
+        if (has_partial(k)) mk_local = fmaxf(mk_local, ws[k * sf + (size_t)p.rg.RG * D + rl]);
+    mk_local = warp_max(mk_local);
+    if (lane == 0) s_red[warp] = mk_local;
+    __syncthreads();
+    float mmax = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, s_red[w]);
+    const float a_tree = m_t > -INFINITY ? exp2f(m_t - mmax) : 0.f;
+#pragma unroll
+    for (int x = 0; x < DPL; ++x) o[x] *= a_tree;
+
+    // pass 2: weighted partial rows, warp w takes partials w, w + kWarps, ...
+    float lsum = l_t * a_tree;  // this warp's sums (the same in every lane)
+    for (int k0 = warp * kUnroll; k0 < count; k0 += kWarps * kUnroll) {
+        float w[kUnroll];
+        float part[kUnroll][DPL];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int k = k0 + u;
+            w[u] = 0.f;
+            if (has_partial(k)) {
+                const float* slot = ws + (size_t)k * sf;
+                const float mk = slot[(size_t)p.rg.RG * D + rl];
+                const float lk = slot[(size_t)p.rg.RG * D + p.rg.RG + rl];
+                w[u] = mk > -INFINITY ? exp2f(mk - mmax) : 0.f;
+                lsum += w[u] * lk;
+                load_partial<DPL>(slot + (size_t)rl * D + lane * DPL, part[u]);
+            } else {
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) part[u][x] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int x = 0; x < DPL; ++x) o[x] = fmaf(part[u][x], w[u], o[x]);
+    }
+#pragma unroll
+    for (int x = 0; x < DPL; ++x) s_o[warp][lane * DPL + x] = o[x];
+    __syncthreads();
+    if (lane == 0) s_red[warp] = lsum;  // every lane of a warp holds the same lsum
+    __syncthreads();
+
+    // ---- combine the warps' sums and write the row
+    float l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) l += s_red[w];
+    const float inv = 1.f / l;
+    float* orow = a.out + (size_t)row * D;
+    for (int d = threadIdx.x; d < D; d += kThreads) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += s_o[w][d];
+        v *= inv;
+        orow[d] = v;
+        if (!isfinite(v)) atomicOr(a.status, LUCETREE_DEV_NONFINITE);
+    }
+    if (a.lse && threadIdx.x == 0) a.lse[row] = (mmax + log2f(l)) * kLn2;
+}
+
+}  // namespace merge
+
+}  // namespace lucetree

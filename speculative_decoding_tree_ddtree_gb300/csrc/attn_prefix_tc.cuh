@@ -572,12 +572,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // One streaming pass over my chunks of S^T: P = 2^(s*scale*log2e - m)
         // with the current shifts; lpart += P (sign +1) or -= P (sign -1, the
-        // exact undo of a pass made with the same shifts); optionally stores
-        // P^T (fp16) and tracks the largest exponent.  Invalid
-        // keys and padding columns give P = 0.  (A separate unmasked copy of
-        // this pass for interior tiles measured slower: the extra code costs
-        // more in instruction fetch than the selects it saves.)
-        auto exp_pass = [&](float (&lpart)[kNa * 16], bool valid, float sign, bool write_p, float& ex) {
+        // exact undo of a pass made with the same shifts); optionally keeps
+        // P (fp16 pairs) in registers `ph` and tracks the largest exponent.
+        // Invalid keys and padding columns give P = 0.  (A separate unmasked
+        // copy of this pass for interior tiles measured slower: the extra code
+        // costs more in instruction fetch than the selects it saves.)
+        // P stays in registers so that the pass can run while PV of the
+        // previous tile still reads the shared P^T buffer; store_p writes it
+        // once that PV has completed.
+        auto exp_pass = [&](float (&lpart)[kNa * 16], bool valid, float sign, bool keep_p, float& ex,
+                            uint32_t (&ph)[kNa * 8]) {
             // 8-column blocks b = 2*cc + hb; the TMEM load of block b+1 is in
             // flight while block b is computed
             constexpr int kBlocks = 2 * kNa;
@@ -608,13 +612,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float& acc = lpart[cc * 16 + 8 * hb + k];
                     acc = fmaf(sign, pv[k], acc);
                 }
-                if (write_p) {
-                    const int nb = 2 * c + hb;
-                    uint32_t w[4];
+                if (keep_p) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) w[k] = pack_half2(pv[2 * k], pv[2 * k + 1]);
-                    *reinterpret_cast<uint4*>(sP + nb * 2048 + kl * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int k = 0; k < 4; ++k) ph[4 * bi + k] = pack_half2(pv[2 * k], pv[2 * k + 1]);
                 }
+            }
+        };
+        // P^T [8-column block][128 keys][8 columns] fp16: block 2c + hb of my chunks
+        auto store_p = [&](const uint32_t (&ph)[kNa * 8]) {
+#pragma unroll
+            for (int bi = 0; bi < 2 * kNa; ++bi) {
+                if (bi >= 2 * nch) continue;
+                const int nb = 2 * cb + bi;
+                *reinterpret_cast<uint4*>(sP + nb * 2048 + kl * 16) =
+                    make_uint4(ph[4 * bi], ph[4 * bi + 1], ph[4 * bi + 2], ph[4 * bi + 3]);
             }
         };
 
@@ -651,20 +662,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = kl < nvalid && page_ok;
                 const bool first = cur.first();
 
-                // S^T(j) ready; P^T and O^T free once PV(j-1) has completed
+                // S^T(j) ready (P^T and O^T are waited for later: PV(j-1) may still
+                // be reading P^T while this tile's exponents are computed)
                 if (!bad && !wait_all(&ms->s_full, j & 1)) bad = true;
-                if (!bad && j > 0 && !wait_all(&ms->pv_done, (j - 1) & 1)) bad = true;
                 if (!bad) tc_fence_after();
+                bool pv_prev_done = j == 0;  // PV(j-1) known complete
 
-                // pass 0: exponents with the current shifts (P^T written, sums added,
-                //         largest exponent voted across the CTA)
+                // pass 0: exponents with the current shifts (P kept in registers,
+                //         sums added, largest exponent voted across the CTA)
                 // pass 1: if an exponent exceeded kTau, the same pass with the sums
                 //         subtracted (exact undo)
-                // pass 2: exact column maxima move the shifts, then P^T and sums again
+                // pass 2: exact column maxima move the shifts, then P and sums again
                 // The first tile of a range has no shifts yet and starts at pass 2.
                 float ex = -INFINITY;
+                uint32_t ph[kNa * 8];
                 if (!bad && !first) {
-                    exp_pass(lpart, valid, 1.f, true, ex);
+                    exp_pass(lpart, valid, 1.f, true, ex, ph);
                 }
                 // one barrier decides the path; a second one only when it says
                 // "slow", to tell a timeout (somewhere) from a shift update
@@ -675,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 if (slow) {
-                    if (!first) exp_pass(lpart, valid, -1.f, false, ex);  // pass 1
+                    if (!first) exp_pass(lpart, valid, -1.f, false, ex, ph);  // pass 1
                     // pass 2: exact column maxima of this tile, then move the shifts
 #pragma unroll 1
                     for (int cc = 0; cc < nch; ++cc) {
@@ -708,9 +721,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < 16; ++k) lpart[cc * 16 + k] *= ms->alpha[16 * (cb + cc) + k];
                     }
                     if (!first) {
-                        // O^T columns accumulated so far move with their shift
+                        // O^T columns accumulated so far move with their shift, once
+                        // PV(j-1) has finished adding to them (a warp that timed out
+                        // here skips its TMEM accesses but keeps to the barriers)
+                        if (!bad && j > 0 && !wait_all(&ms->pv_done, (j - 1) & 1)) bad = true;
+                        pv_prev_done = true;
+                        if (!bad) tc_fence_after();
 #pragma unroll 1
-                        for (int cc = 0; cc < nch; ++cc) {
+                        for (int cc = 0; cc < nch && !bad; ++cc) {
                             const int c = cb + cc;
                             bool any = false;
 #pragma unroll
@@ -728,17 +746,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tmem_st16(addr, r);
                             }
                         }
-                        tmem_wait_st();
+                        if (!bad) tmem_wait_st();
                     }
-                    exp_pass(lpart, valid, 1.f, true, ex);
+                    if (!bad) exp_pass(lpart, valid, 1.f, true, ex, ph);
                 }
                 // S^T is no longer read: the next tile's QK may overwrite it
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ms->s_free);
 
+                // P^T is free once PV(j-1) has completed; then this tile's P goes in
+                if (!bad && !pv_prev_done && !wait_all(&ms->pv_done, (j - 1) & 1)) bad = true;
+                if (!bad) {
+                    tc_fence_after();
+                    store_p(ph);
+                }
                 tc_fence_before();
                 fence_proxy_async_smem();  // P^T stores -> tensor-core reads
+                __syncwarp();              // every lane's stores and fence come before lane 0's arrive
                 if (!bad && lane == 0) mbar_arrive(&ms->p_full);
 
                 // V(j), chunk by chunk as it lands: bf16 -> fp16 in place, rows of

@@ -148,14 +148,20 @@ lucetree_status lucetree_verify_attn_vq(const lucetree_attn_args* a, int v_forma
     return verify_attn_impl(a, v_format, v_exp, workspace, workspace_bytes, stream);
 }
 
-static lucetree_status verify_attn_impl(const lucetree_attn_args* a, int v_format, const uint8_t* v_exp,
-                                        void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace lucetree {
+
+// Host checks of one attention call and its launch description (everything
+// but the workspace).  need_mask: whether anc_mask is read (the fused step
+// derives the masks from the parent array instead).
+lucetree_status verify_attn_check(const lucetree_attn_args* a, bool need_mask, int v_format, AttnLaunch* L) {
     if (!a) return LUCETREE_ERR_INVALID_ARG;
     if (a->dtype != LUCETREE_F16 && a->dtype != LUCETREE_BF16) return LUCETREE_ERR_UNSUPPORTED;
     if (a->page_size != LUCETREE_PAGE_SIZE) return LUCETREE_ERR_UNSUPPORTED;
     if (!attn_shape_ok(a->B, a->N, a->Hq, a->Hkv, a->D)) return LUCETREE_ERR_UNSUPPORTED;
     if (!a->q || !a->k_pool || !a->v_pool || !a->page_table || !a->ctx_len || !a->k_tree || !a->v_tree ||
-        !a->anc_mask || !a->out || !a->status)
+        (need_mask && !a->anc_mask) || !a->out || !a->status)
         return LUCETREE_ERR_INVALID_ARG;
     if (a->num_pages <= 0 || a->max_pages_per_seq <= 0) return LUCETREE_ERR_INVALID_ARG;
     if (!aligned16(a->q) || !aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->k_tree) ||
@@ -164,15 +170,28 @@ static lucetree_status verify_attn_impl(const lucetree_attn_args* a, int v_forma
     if (!isfinite(a->scale)) return LUCETREE_ERR_INVALID_ARG;
     if (!prefix_shape_supported(*a)) return LUCETREE_ERR_UNSUPPORTED;
     const int dev = current_device();
+    L->a = *a;
+    L->plan = make_plan(a->B, a->N, a->Hq, a->Hkv, a->D, prefix_grid_ctas(dev), a->max_pages_per_seq);
+    L->ws = nullptr;
+    L->scale_log2 = a->scale * kLog2e;
+    L->v_format = v_format;
+    L->v_exp = nullptr;
+    return LUCETREE_OK;
+}
+
+}  // namespace lucetree
+
+extern "C" {
+
+static lucetree_status verify_attn_impl(const lucetree_attn_args* a, int v_format, const uint8_t* v_exp,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
     AttnLaunch L;
-    L.a = *a;
-    L.plan = make_plan(a->B, a->N, a->Hq, a->Hkv, a->D, prefix_grid_ctas(dev), a->max_pages_per_seq);
+    const lucetree_status st = verify_attn_check(a, true, v_format, &L);
+    if (st != LUCETREE_OK) return st;
     if (!workspace || workspace_bytes < attn_workspace_bytes(L.plan) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return LUCETREE_ERR_WORKSPACE;
     L.ws = reinterpret_cast<float*>(workspace);
-    L.scale_log2 = a->scale * kLog2e;
-    L.v_format = v_format;
     L.v_exp = v_exp;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_attn_prefix(L, s) != cudaSuccess) return LUCETREE_ERR_CUDA;

@@ -48,6 +48,8 @@ EXPORTED = (
     "lucetree_stage_pages",
     "lucetree_verify_attn_vq",
     "lucetree_selftest_wait_timeout",
+    "lucetree_verify_step_workspace",
+    "lucetree_verify_step",
 )
 
 
@@ -64,6 +66,14 @@ class AttnArgs(ctypes.Structure):
         ("ctx_len", ctypes.c_void_p), ("k_tree", ctypes.c_void_p), ("v_tree", ctypes.c_void_p),
         ("anc_mask", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("status", ctypes.c_void_p),
+    ]
+
+
+class StepArgs(ctypes.Structure):
+    _fields_ = [
+        ("attn", AttnArgs), ("parent", ctypes.c_void_p), ("draft", ctypes.c_void_p), ("logits", ctypes.c_void_p),
+        ("vocab", ctypes.c_int), ("argmax", ctypes.c_void_p), ("acc_nodes", ctypes.c_void_p),
+        ("acc_len", ctypes.c_void_p), ("bonus", ctypes.c_void_p), ("ctx_len_out", ctypes.c_void_p),
     ]
 
 
@@ -139,6 +149,8 @@ def load(path: str | None = None):
     lib.lucetree_stage_pages.argtypes = [ctypes.POINTER(StageArgs), P]
     lib.lucetree_verify_attn_vq.argtypes = [ctypes.POINTER(AttnArgs), I, P, P, SZ, P]
     lib.lucetree_selftest_wait_timeout.argtypes = [P, ctypes.c_longlong, P, P]
+    lib.lucetree_verify_step_workspace.argtypes = [I, I, I, I, I, I, ctypes.POINTER(SZ)]
+    lib.lucetree_verify_step.argtypes = [ctypes.POINTER(StepArgs), P, SZ, P]
     for name in EXPORTED:
         if name not in ("lucetree_status_string", "lucetree_abi_version"):
             getattr(lib, name).restype = I
@@ -365,15 +377,63 @@ def lucetree_commit(k_tree, v_tree, acc_nodes, acc_len, page_table, ctx_len_in, 
 
 # ---------------------------------------------------------------- one whole step
 
+def lucetree_verify_step_workspace(B: int, N: int, Hq: int, Hkv: int, D: int, vocab: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().lucetree_verify_step_workspace(B, N, Hq, Hkv, D, vocab, ctypes.byref(n)))
+    return int(n.value)
+
+
+def _step_args(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, parent, draft, logits, out, lse, argmax_idx,
+               acc_nodes, acc_len, bonus, ctx_len_out, status, scale=None):
+    """Checks every tensor of one fused step against the documented layouts and
+    packs the C argument struct."""
+    B, N, Hq, D = _dims(q, "q", 4)
+    _expect(parent, "parent", (B, N), _I32)
+    _expect(draft, "draft", (B, N), _I32)
+    V = _dims(logits, "logits", 3)[2]
+    _expect(logits, "logits", (B, N + 1, V), _F32)
+    _expect(argmax_idx, "argmax", (B, N + 1), _I32)
+    _expect(acc_nodes, "acc_nodes", (B, N), _I32)
+    _expect(acc_len, "acc_len", (B,), _I32)
+    _expect(bonus, "bonus", (B,), _I32)
+    _expect(ctx_len_out, "ctx_len_out", (B,), _I32)
+    if ctx_len_out.data_ptr() == ctx_len.data_ptr():
+        raise LucetreeError("ctx_len_out must not alias ctx_len in the fused step")
+    anc_dummy = torch.empty((B, N), dtype=torch.int64, device="meta")
+    _check_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_dummy, out, status, lse)
+    s = StepArgs()
+    a = s.attn
+    a.dtype = dtype_code(q)
+    a.B, a.N, a.Hq, a.Hkv, a.D = B, N, Hq, k_pool.shape[1], D
+    a.page_size = k_pool.shape[2]
+    a.scale = float(scale) if scale is not None else float(D) ** -0.5
+    a.q, a.k_pool, a.v_pool = _ptr(q), _ptr(k_pool), _ptr(v_pool)
+    a.num_pages = k_pool.shape[0]
+    a.page_table, a.max_pages_per_seq = _ptr(page_table), page_table.shape[1]
+    a.ctx_len, a.k_tree, a.v_tree, a.anc_mask = _ptr(ctx_len), _ptr(k_tree), _ptr(v_tree), None
+    a.out, a.lse, a.status = _ptr(out), _ptr(lse), _ptr(status)
+    s.parent, s.draft, s.logits, s.vocab = _ptr(parent), _ptr(draft), _ptr(logits), V
+    s.argmax, s.acc_nodes, s.acc_len, s.bonus = _ptr(argmax_idx), _ptr(acc_nodes), _ptr(acc_len), _ptr(bonus)
+    s.ctx_len_out = _ptr(ctx_len_out)
+    return s
+
+
 class VerifyStep:
     """Device buffers and workspaces for repeated verify steps of one shape.
 
-    ``run`` issues the whole step on one stream: ancestor masks, tree-verify
-    attention, argmax, acceptance and commit (all library kernels)."""
+    ``run`` issues the whole step (ancestor masks, tree-verify attention,
+    argmax, acceptance and commit, all library kernels) as ONE C call,
+    lucetree_verify_step.  The tensors of a call are checked against the
+    documented layouts the first time that set of buffers is seen; later
+    calls with the same buffers reuse the packed arguments, so a step costs
+    one ctypes call on the host."""
 
     def __init__(self, B, N, Hq, Hkv, D, vocab, device="cuda"):
         self.B, self.N, self.Hq, self.Hkv, self.D, self.vocab = B, N, Hq, Hkv, D, vocab
         dev = torch.device(device)
+        # zeroed once: the step's counters must start at zero and every call leaves them so
+        self.ws_step = torch.zeros(lucetree_verify_step_workspace(B, N, Hq, Hkv, D, vocab), dtype=torch.uint8,
+                                   device=dev)
         self.ws_attn = torch.empty(lucetree_verify_attn_workspace(B, N, Hq, Hkv, D), dtype=torch.uint8, device=dev)
         self.ws_argmax = torch.empty(lucetree_argmax_workspace(B * (N + 1), vocab), dtype=torch.uint8, device=dev)
         self.anc = torch.empty(B, N, dtype=torch.int64, device=dev)
@@ -385,8 +445,24 @@ class VerifyStep:
         self.bonus = torch.empty(B, dtype=torch.int32, device=dev)
         self.ctx_out = torch.empty(B, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._packed = {}
 
     def run(self, q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, parent, draft, logits, stream=None):
+        ts = (q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, parent, draft, logits)
+        key = tuple((t.data_ptr(), tuple(t.shape), t.dtype, t.is_contiguous()) for t in ts)
+        s = self._packed.get(key)
+        if s is None:
+            s = _step_args(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, parent, draft, logits, self.out,
+                           self.lse, self.argmax, self.acc_nodes, self.acc_len, self.bonus, self.ctx_out, self.status)
+            if len(self._packed) > 64:
+                self._packed.clear()
+            self._packed[key] = s
+        _check(load().lucetree_verify_step(ctypes.byref(s), _ptr(self.ws_step), self.ws_step.numel(),
+                                           _stream(stream)))
+
+    def run_calls(self, q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, parent, draft, logits, stream=None):
+        """The same step as the five separate C calls (masks, attention,
+        argmax, acceptance, commit)."""
         lucetree_build_anc_mask(parent, self.anc, self.status, stream)
         lucetree_verify_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, self.anc, self.out,
                              self.status, self.ws_attn, lse=self.lse, stream=stream)

@@ -165,10 +165,29 @@ def test_tree_ops_accept_generated_inputs_and_refuse_mismatches(stub, attn):
 def test_verify_step_buffers_pass_the_checks(stub, attn):
     _, d, _ = attn
     step = LT.VerifyStep(CFG.B, CFG.N, CFG.Hq, CFG.Hkv, CFG.D, CFG.vocab, device="cpu")
-    step.run(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"],
-             d["parent"], d["draft"], d["logits"])
+    args = (d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"], d["parent"],
+            d["draft"], d["logits"])
+    step.run(*args)
+    step.run(*args)
+    assert stub.calls[-2:] == ["lucetree_verify_step"] * 2
+    assert len(step._packed) == 1  # the second call reused the checked arguments
+    step.run_calls(*args)
     assert stub.calls[-5:] == ["lucetree_build_anc_mask", "lucetree_verify_attn", "lucetree_argmax",
                                "lucetree_accept", "lucetree_commit"]
+
+
+def test_verify_step_refuses_mismatched_buffers(stub, attn):
+    _, d, _ = attn
+    step = LT.VerifyStep(CFG.B, CFG.N, CFG.Hq, CFG.Hkv, CFG.D, CFG.vocab, device="cpu")
+    good = dict(q=d["q"], k_pool=d["k_pool"], v_pool=d["v_pool"], page_table=d["page_table"], ctx_len=d["ctx_len"],
+                k_tree=d["k_tree"], v_tree=d["v_tree"], parent=d["parent"], draft=d["draft"], logits=d["logits"])
+    for k, bad in (("logits", d["logits"][:, :-1].contiguous()),      # one row short per sequence
+                   ("draft", d["draft"].to(torch.int64)),              # wrong element type
+                   ("parent", d["parent"][:-1].contiguous()),          # one sequence short
+                   ("k_tree", d["k_tree"].view(torch.float16))):       # dtype differs from q
+        with pytest.raises(LT.LucetreeError):
+            step.run(**dict(good, **{k: bad}))
+    assert "lucetree_verify_step" not in stub.calls
 
 
 def test_lmhead_shapes(stub):

@@ -293,3 +293,98 @@ def test_full_step_sweep_point_full_pool_compare(cuda_dev):
     assert np.array_equal(step.ctx_out.cpu().numpy(), ctx)
     assert np.array_equal(bits16(d["k_pool"]), kp)
     assert np.array_equal(bits16(d["v_pool"]), vp)
+
+
+# ---------------------------------------------------------------- the fused step (one C call)
+
+def _inputs_step(cfg, seed):
+    inp = W.generate(cfg, seed=seed)
+    return inp, to_device(inp, cfg)
+
+
+@pytest.mark.parametrize("name", ["ragged-f16-d128", "multi-bf16-d256"])
+def test_fused_step_equals_the_five_calls(cuda_dev, name):
+    """lucetree_verify_step gives bit for bit what the five separate calls
+    give: attention output and lse, argmax, acceptance, and the pools and
+    lengths after the commit."""
+    import torch
+    LT = _lt()
+    if name == "ragged-f16-d128":
+        cfg = W.VerifyConfig(name, ctx=(0, 63, 65, 1000, 2049), Hq=12, Hkv=3, D=128, dtype=W.F16, N=9,
+                             tree="random", branch_cap=3, vocab=3000, p_plant=0.9, paged="permuted", spare_pages=5)
+    else:
+        cfg = W.VerifyConfig(name, ctx=(4000, 130, 9000), Hq=24, Hkv=4, D=256, dtype=W.BF16, N=22,
+                             tree="random", branch_cap=4, vocab=5000, p_plant=0.9, paged="permuted", spare_pages=6)
+    inp, d1 = _inputs_step(cfg, 41)
+    d2 = to_device(inp, cfg)
+    s1 = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab)
+    s2 = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab)
+    args = lambda d: (d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"],
+                      d["parent"], d["draft"], d["logits"])
+    s1.run(*args(d1))
+    s2.run_calls(*args(d2))
+    torch.cuda.synchronize()
+    assert s1.status.item() == 0 and s2.status.item() == 0
+    for name_ in ("out", "lse", "argmax", "acc_nodes", "acc_len", "bonus", "ctx_out"):
+        a, b = getattr(s1, name_), getattr(s2, name_)
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name_
+    assert torch.equal(d1["k_pool"].view(torch.int16), d2["k_pool"].view(torch.int16))
+    assert torch.equal(d1["v_pool"].view(torch.int16), d2["v_pool"].view(torch.int16))
+    assert s1.acc_len.sum().item() > 0
+
+
+def test_fused_step_repeated_calls_are_identical(cuda_dev):
+    """Twenty fused steps on the same inputs (the commit rewrites the same
+    rows each time) give bitwise identical results and a clean status: a
+    race between the kernels' roles would show up as a difference."""
+    import torch
+    LT = _lt()
+    cfg = W.VerifyConfig("repeat", ctx=(20000, 3000), Hq=24, Hkv=4, D=256, dtype=W.BF16, N=22, tree="random",
+                         branch_cap=4, vocab=20000, p_plant=0.9, paged="permuted", spare_pages=4)
+    inp, d = _inputs_step(cfg, 43)
+    step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab)
+    args = (d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"], d["parent"],
+            d["draft"], d["logits"])
+    step.run(*args)
+    torch.cuda.synchronize()
+    first = {k: getattr(step, k).clone() for k in ("out", "lse", "argmax", "acc_nodes", "acc_len", "bonus", "ctx_out")}
+    for _ in range(19):
+        step.run(*args)
+    torch.cuda.synchronize()
+    assert step.status.item() == 0
+    for k, v in first.items():
+        assert torch.equal(getattr(step, k).view(torch.int32), v.view(torch.int32)), k
+    ref, _ = oracle.verify_attn(inp, oracle.BF16)
+    from tests.helpers import ATTN_TOL, row_error
+    assert row_error(step.out.cpu().numpy().reshape(-1, cfg.D), ref).max() <= ATTN_TOL
+
+
+def test_fused_step_host_and_device_checks(cuda_dev):
+    import torch
+    LT = _lt()
+    cfg = W.VerifyConfig("step-bad", ctx=(300, 100), Hq=4, Hkv=2, D=128, dtype=W.F16, N=5, vocab=50,
+                         paged="permuted", spare_pages=2)
+    inp, d = _inputs_step(cfg, 44)
+    step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab)
+    # the new lengths may not overwrite the old ones: merge CTAs still read them
+    with pytest.raises(LT.LucetreeError):
+        LT._step_args(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"],
+                      d["parent"], d["draft"], d["logits"], step.out, step.lse, step.argmax, step.acc_nodes,
+                      step.acc_len, step.bonus, d["ctx_len"], step.status)
+    s = LT._step_args(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"],
+                      d["parent"], d["draft"], d["logits"], step.out, step.lse, step.argmax, step.acc_nodes,
+                      step.acc_len, step.bonus, step.ctx_out, step.status)
+    lib = LT.load()
+    import ctypes
+    s.ctx_len_out = s.attn.ctx_len
+    assert lib.lucetree_verify_step(ctypes.byref(s), LT._ptr(step.ws_step), step.ws_step.numel(), None) == 1
+    s.ctx_len_out = LT._ptr(step.ctx_out)
+    assert lib.lucetree_verify_step(ctypes.byref(s), LT._ptr(step.ws_step), 16, None) == 3  # workspace too small
+    # a parent that is not an earlier node is flagged on the device, the call completes
+    bad = d["parent"].clone()
+    bad[1, 3] = 4
+    step.run(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"], bad,
+             d["draft"], d["logits"])
+    torch.cuda.synchronize()
+    assert step.status.item() & LT.DEV_BAD_PARENT
+    assert step.acc_len[1].item() == 0
