@@ -381,6 +381,9 @@ def measure_configs(args, dev, stream, rank):
             d = device_inputs(cfg, dev, seed=rank)
         step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, device=dev)
         ctx0 = d["ctx_len"].clone()
+        # the inputs were drawn (and the step's counters zeroed) on the current
+        # stream: the side stream must not start before they are complete
+        stream.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(stream):
             for _ in range(3):
                 issue_step(step, d, stream)
@@ -442,6 +445,7 @@ def run_ours(args, cfg):
              draft=torch.from_numpy(inp["draft"]).to(dev), logits=torch.from_numpy(inp["logits"]).to(dev))
     stream = torch.cuda.Stream(device=dev)
     step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # inputs and the zeroed counters are ready first
 
     def one(dd=None):
         issue_step(step, d if dd is None else dd, stream)
@@ -635,6 +639,7 @@ def measure_lmhead(args, dev, stream, rank, with_cpu=True):
     out = torch.empty(lc.rows, dtype=torch.int32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = torch.empty(LT.lucetree_lmhead_argmax_workspace(lc.rows), dtype=torch.uint8, device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # the weights are drawn on the current stream
     for _ in range(3):
         LT.lucetree_lmhead_argmax(hidden, weight, out, st, ws, stream=stream)
     n = max(10, min(100, args.steps // 20))
@@ -703,6 +708,7 @@ def measure_delta(args, dev, stream, rank, with_cpu=True):
     acc_d = torch.from_numpy(acc).to(dev)
     len_d = torch.tensor([len(path)], dtype=torch.int32, device=dev)
     state_work = d["state"].clone()
+    stream.wait_stream(torch.cuda.current_stream(dev))  # the copies above run on the current stream
 
     def tree():
         LT.lucetree_delta_tree(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["state"], out, st,
@@ -779,6 +785,7 @@ def measure_vq(args, dev, stream, rank, d, step, cfg):
         vq = W.generate_vq(cfg, fmt, seed=rank)
         codes = torch.from_numpy(vq["v_codes"]).to(dev)
         vexp = torch.from_numpy(vq["v_exp"]).to(dev)
+        stream.wait_stream(torch.cuda.current_stream(dev))
 
         def call():
             LT.lucetree_verify_attn_vq(d["q"], d["k_pool"], codes, vexp, fmt, d["page_table"], d["ctx_len"],
@@ -830,6 +837,7 @@ def measure_stage(args, dev, stream, rank):
     dst = torch.randperm(n + 64, generator=g)[:n].to(torch.int32).to(dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     nbytes = 2 * host_k.numel() * 2
+    stream.wait_stream(torch.cuda.current_stream(dev))
 
     def stage():
         LT.lucetree_stage_pages(host_k, host_v, src, dst, pool_k, pool_v, st, stream=stream)

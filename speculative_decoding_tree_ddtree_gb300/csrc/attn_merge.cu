@@ -7,7 +7,7 @@ namespace lucetree {
 namespace {
 
 template <typename T, int D>
-__global__ void __launch_bounds__(merge::kThreads) merge_kernel(AttnLaunch L) {
+__global__ void __launch_bounds__(merge::kThreads, 3) merge_kernel(AttnLaunch L) {
     __shared__ float s_o[merge::kWarps][D];
     __shared__ float s_red[merge::kWarps];
     if (threadIdx.x == 0) pdl_trigger();

@@ -8,12 +8,13 @@
 // lse = ln(sum) + max.  Maxima are kept in the log2 domain
 // (scores pre-multiplied by log2 e), so every rescale is one exp2.
 //
-// The partials are independent: their maxima are reduced first (one thread
-// per partial), then warp w adds the weighted partial rows w, w + 8, ... with
-// several 16-byte loads in flight per lane, and the eight warp sums are added
-// through shared memory.  A block reads about 40 partial rows of D floats, so
-// spreading them over eight warps keeps enough loads in flight to stream the
-// partials at memory speed instead of one dependent row at a time.
+// The partials are independent: warp w folds partials w, w + 8, ... into a
+// running (max, sum, output slice) of its own, issuing all of a round's
+// loads before using any, and the eight warps' parts are combined through
+// shared memory on their common maximum.  A block reads about 40 partial
+// rows of D floats, so spreading them over eight warps, five rows each, gets
+// the whole row in about one L2 round trip instead of one dependent row at a
+// time.
 #pragma once
 
 #include "internal.cuh"
@@ -35,7 +36,7 @@ __device__ inline float warp_max(float v) {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kUnroll = 2;  // partial rows per warp iteration (2 x D/32 floats per lane in flight)
+constexpr int kRound = 5;  // partial rows per warp per round, all loads in flight together
 
 template <typename T, int D>
 __device__ inline void load_slice(const T* p, float (&out)[D / 32]) {
@@ -138,50 +139,61 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
         return k < count && cta_begin(c_lo + k, nT, p.Cg) != cta_begin(c_lo + k + 1, nT, p.Cg);
     };
 
-    // pass 1: the common shift (maximum over the tree parts and every partial)
-    float mk_local = m_t;
-    for (int k = threadIdx.x; k < count; k += kThreads)
-        if (has_partial(k)) mk_local = fmaxf(mk_local, ws[k * sf + (size_t)p.rg.RG * D + rl]);
-    mk_local = warp_max(mk_local);
-    if (lane == 0) s_red[warp] = mk_local;
-    __syncthreads();
-    float mmax = -INFINITY;
+    // Each warp folds partials w, w + kWarps, w + 2 kWarps, ... into its own
+    // running (max, sum, output slice), which starts from its share of the
+    // tree block.  All of a round's loads (up to kRound partials per warp:
+    // maxima, sums and the row slices) are issued before any is used, so a
+    // round costs one trip to L2; the headline shapes need one round.
+    float m_w = m_t, l_w = l_t;
+    for (int k0 = warp; k0 < count; k0 += kWarps * kRound) {
+        float mk[kRound], lk[kRound];
+        float part[kRound][DPL];
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, s_red[w]);
-    const float a_tree = m_t > -INFINITY ? exp2f(m_t - mmax) : 0.f;
-#pragma unroll
-    for (int x = 0; x < DPL; ++x) o[x] *= a_tree;
-
-    // pass 2: weighted partial rows, warp w takes partials w, w + kWarps, ...
-    float lsum = l_t * a_tree;  // this warp's sums (the same in every lane)
-    for (int k0 = warp * kUnroll; k0 < count; k0 += kWarps * kUnroll) {
-        float w[kUnroll];
-        float part[kUnroll][DPL];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int k = k0 + u;
-            w[u] = 0.f;
+        for (int u = 0; u < kRound; ++u) {
+            const int k = k0 + u * kWarps;
+            mk[u] = -INFINITY;
+            lk[u] = 0.f;
             if (has_partial(k)) {
                 const float* slot = ws + (size_t)k * sf;
-                const float mk = slot[(size_t)p.rg.RG * D + rl];
-                const float lk = slot[(size_t)p.rg.RG * D + p.rg.RG + rl];
-                w[u] = mk > -INFINITY ? exp2f(mk - mmax) : 0.f;
-                lsum += w[u] * lk;
+                mk[u] = slot[(size_t)p.rg.RG * D + rl];
+                lk[u] = slot[(size_t)p.rg.RG * D + p.rg.RG + rl];
                 load_partial<DPL>(slot + (size_t)rl * D + lane * DPL, part[u]);
             } else {
 #pragma unroll
                 for (int x = 0; x < DPL; ++x) part[u][x] = 0.f;
             }
         }
+        float mr = m_w;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
+        for (int u = 0; u < kRound; ++u) mr = fmaxf(mr, mk[u]);
+        if (mr > -INFINITY) {
+            const float a0 = m_w > -INFINITY ? exp2f(m_w - mr) : 0.f;
+            l_w *= a0;
 #pragma unroll
-            for (int x = 0; x < DPL; ++x) o[x] = fmaf(part[u][x], w[u], o[x]);
+            for (int x = 0; x < DPL; ++x) o[x] *= a0;
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+                const float w = mk[u] > -INFINITY ? exp2f(mk[u] - mr) : 0.f;
+                l_w = fmaf(w, lk[u], l_w);
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) o[x] = fmaf(part[u][x], w, o[x]);
+            }
+            m_w = mr;
+        }
     }
-#pragma unroll
-    for (int x = 0; x < DPL; ++x) s_o[warp][lane * DPL + x] = o[x];
+
+    // ---- the warps' parts on the common shift
+    if (lane == 0) s_red[warp] = m_w;
     __syncthreads();
-    if (lane == 0) s_red[warp] = lsum;  // every lane of a warp holds the same lsum
+    float mmax = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, s_red[w]);
+    const float aw = m_w > -INFINITY ? exp2f(m_w - mmax) : 0.f;
+#pragma unroll
+    for (int x = 0; x < DPL; ++x) s_o[warp][lane * DPL + x] = o[x] * aw;
+    const float lsum = l_w * aw;  // the same in every lane of the warp
+    __syncthreads();              // every warp has read the maxima in s_red
+    if (lane == 0) s_red[warp] = lsum;
     __syncthreads();
 
     // ---- combine the warps' sums and write the row
