@@ -367,3 +367,31 @@ def quantise_k_e4m3(k_bits, dtype: int):
         raise ValueError("row scale outside the exponent byte's range")
     codes = _round_e4m3(x * np.ldexp(1.0, p)[..., None])
     return codes, e.astype(np.uint8)
+
+
+def commit_kq(inp: dict, k_codes, k_exp, acc_nodes, acc_len, inplace: bool = False):
+    """Commit / rollback into a K pool held in the quantised-K format (V stays
+    16-bit and goes through ``commit``): the k-th accepted node's K row of
+    every KV head is stored at logical position L_b + k (pool page
+    page_table[b][(L_b+k)/64], slot (L_b+k) % 64) as quantise_k_e4m3 of that
+    16-bit row; every other code and exponent byte is unchanged.  k_codes
+    uint8 [P][Hkv][64][D], k_exp uint8 [P][Hkv][64].  Returns (k_codes, k_exp),
+    on copies unless ``inplace``."""
+    dtype = inp.get("dtype_id", BF16)
+    codes = k_codes if inplace else np.array(k_codes, dtype=np.uint8, copy=True)
+    expo = k_exp if inplace else np.array(k_exp, dtype=np.uint8, copy=True)
+    kt = np.asarray(inp["k_tree"], np.uint16)
+    pt = np.asarray(inp["page_table"], np.int32)
+    ctx = np.asarray(inp["ctx_len"], np.int32)
+    acc = np.asarray(acc_nodes, np.int32)
+    alen = np.asarray(acc_len, np.int32)
+    B = kt.shape[0]
+    for b in range(B):
+        for k in range(int(alen[b])):
+            node = int(acc[b, k])
+            pos = int(ctx[b]) + k
+            page = int(pt[b, pos // 64])
+            c, e = quantise_k_e4m3(kt[b, node], dtype)   # one row per KV head
+            codes[page, :, pos % 64, :] = c
+            expo[page, :, pos % 64] = e
+    return codes, expo

@@ -660,3 +660,50 @@ def test_quantise_then_dequantise_error_and_fixed_points():
     v = oracle.dequant_k_e4m3(c0[:, None, :], e0[:, None], oracle.BF16)[:, 0, :]
     c1, e1 = oracle.quantise_k_e4m3(v, oracle.BF16)
     assert np.array_equal(oracle.dequant_k_e4m3(c1[:, None, :], e1[:, None], oracle.BF16)[:, 0, :], v)
+
+
+def test_commit_kq_hand_example():
+    """L = 64, accepted path [0, 2] of a 3-node tree, one KV head, D = 4: node
+    0's K row lands in page_table[0][1] slot 0 and node 2's in slot 1, each as
+    the quantised row worked by hand (see test_quantise_k_hand_rows); every
+    other byte keeps its value."""
+    kt = np.zeros((1, 3, 1, 4), np.uint16)
+    kt[0, 0, 0] = _bf16_bits([1.0, -0.5, 0.0, 3.0 * 2.0 ** -10])    # e 119, codes 78 F0 00 34
+    kt[0, 1, 0] = _bf16_bits([5.0, 5.0, 5.0, 5.0])                   # rejected: never written
+    kt[0, 2, 0] = _bf16_bits([448.0, 272.0, 304.0, -272.0])          # e 127, codes 7E 78 7A F8
+    inp = dict(k_tree=kt, page_table=np.array([[3, 1, 0, 2]], np.int32), ctx_len=np.array([64], np.int32),
+               dtype_id=oracle.BF16)
+    codes = np.full((4, 1, 64, 4), 0x11, np.uint8)
+    expo = np.full((4, 1, 64), 0x22, np.uint8)
+    c, e = oracle.commit_kq(inp, codes, expo, np.array([[0, 2, -1]], np.int32), np.array([2], np.int32))
+    assert c[1, 0, 0].tolist() == [0x78, 0xF0, 0x00, 0x34] and e[1, 0, 0] == 119
+    assert c[1, 0, 1].tolist() == [0x7E, 0x78, 0x7A, 0xF8] and e[1, 0, 1] == 127
+    untouched = np.ones(codes.shape[:3], bool)
+    untouched[1, 0, :2] = False
+    assert (c[untouched] == 0x11).all() and (e[untouched] == 0x22).all()
+    assert (codes == 0x11).all() and (expo == 0x22).all()  # not in place: the inputs are left alone
+
+
+def test_commit_kq_touches_the_rows_the_16bit_commit_touches():
+    """On a ragged 3-sequence batch, the rows commit_kq writes are exactly the
+    rows the 16-bit commit writes, and each reads back (dequant_k_e4m3) as the
+    quantised form of the accepted node's K row."""
+    cfg = W.VerifyConfig("commit-kq", ctx=(64, 130, 1000), Hq=4, Hkv=2, D=128, dtype=W.BF16, N=10,
+                         tree="random", vocab=8, p_plant=0.95, paged="permuted", spare_pages=3)
+    inp = W.generate(cfg, seed=2)
+    am = oracle.argmax(inp["logits"])
+    acc, alen, _ = oracle.accept(inp["parent"], inp["draft"], am)
+    assert alen.sum() >= 3
+    kq = W.generate_kq(cfg, seed=2)
+    c, e = oracle.commit_kq(dict(inp, dtype_id=oracle.BF16), kq["k_codes"], kq["k_exp"], acc, alen)
+    kp, _, _ = oracle.commit(inp, acc, alen)
+    changed16 = (kp != inp["k_pool"]).any(axis=-1) | np.zeros(kp.shape[:3], bool)
+    # rows of the 16-bit pool may be unchanged by chance only if the tree row equals the old row: never here
+    changed_kq = (c != kq["k_codes"]).any(axis=-1) | (e != kq["k_exp"])
+    assert np.array_equal(changed_kq, changed16)
+    for b in range(cfg.B):
+        for k in range(int(alen[b])):
+            pos = int(inp["ctx_len"][b]) + k
+            page = int(inp["page_table"][b, pos // 64])
+            want_c, want_e = oracle.quantise_k_e4m3(inp["k_tree"][b, acc[b, k]], oracle.BF16)
+            assert np.array_equal(c[page, :, pos % 64], want_c) and np.array_equal(e[page, :, pos % 64], want_e)
