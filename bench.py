@@ -607,6 +607,7 @@ def run_ours(args, cfg):
         line["stage_pages"] = measure_stage(args, dev, stream, rank)
     if not args.no_vq and cfg.D == 256:
         line["quantised_v"] = measure_vq(args, dev, stream, rank, d, step, cfg)
+        line["quantised_k"] = measure_kq(args, dev, stream, rank, d, step, cfg)
     if not args.no_configs:
         for held in (d, host, bufs[1]):
             held.clear()  # the other workloads need the device memory
@@ -816,6 +817,59 @@ def measure_vq(args, dev, stream, rank, d, step, cfg):
     return res
 
 
+def measure_kq(args, dev, stream, rank, d, step, cfg):
+    """The headline attention call with K stored as FP8 E4M3 codes (one
+    power-of-two exponent per token and head) and V in bf16 or as int8 codes,
+    timed with CUDA events on the stream over resident inputs.  The codes
+    are drawn on the device as uniform finite E4M3 codes with exponents in
+    [120, 124] (the generator's distribution for this format)."""
+    import torch
+    from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
+    res = {}
+    L = sum(cfg.ctx)
+    P = d["k_pool"].shape[0]
+    peak, peak_kind = peak_hbm()
+    g = torch.Generator(device=dev)
+    g.manual_seed(99 + rank)
+    kc = torch.randint(0, 254, (P, cfg.Hkv, W.PAGE, cfg.D), generator=g, device=dev, dtype=torch.int32)
+    kc = (kc + (kc >= 127).int()).to(torch.uint8)  # skip 0x7F; 0xFF is never drawn
+    ke = torch.randint(120, 125, (P, cfg.Hkv, W.PAGE), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    vq = W.generate_vq(cfg, W.V_INT8, seed=rank)
+    vcodes = torch.from_numpy(vq["v_codes"]).to(dev)
+    vexp = torch.from_numpy(vq["v_exp"]).to(dev)
+    ws = torch.empty(LT.lucetree_verify_attn_kq_workspace(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D), dtype=torch.uint8,
+                     device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    for name, fmt, vbytes in (("e4m3_k_bf16_v", LT.LUCETREE_V_SAME, 2.0), ("e4m3_k_int8_v", LT.LUCETREE_V_INT8, 1.0)):
+        vp, vx = (d["v_pool"], None) if fmt == LT.LUCETREE_V_SAME else (vcodes, vexp)
+
+        def call():
+            LT.lucetree_verify_attn_kq(d["q"], kc, ke, vp, d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"],
+                                       step.anc, step.out, step.status, ws, v_format=fmt, v_exp=vx, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                call()
+            n = max(20, min(200, args.steps // 10))
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            torch.cuda.synchronize(dev)
+            for e0, e1 in evs:
+                e0.record(stream)
+                call()
+                e1.record(stream)
+        torch.cuda.synchronize(dev)
+        st_ms = ms_stats([e0.elapsed_time(e1) for e0, e1 in evs])
+        per_tok = cfg.Hkv * (cfg.D * (1 + vbytes) + 1 + (1 if fmt != LT.LUCETREE_V_SAME else 0))
+        nbytes = int(L * per_tok + cfg.B * cfg.N * cfg.Hq * cfg.D * 2 + cfg.B * cfg.N * cfg.Hq * cfg.D * 4
+                     + 4 * L // 64)
+        res[name] = {"ms_per_call": st_ms["mean"], "ms_stats": st_ms, "device_status": int(step.status.item()),
+                     "algorithmic_bytes_per_launch": nbytes, "achieved_GBps": nbytes / (st_ms["mean"] * 1e-3) / 1e9,
+                     "frac_of_hbm_peak": nbytes / (st_ms["mean"] * 1e-3) / 1e9 / peak, "kv_bytes_per_token": per_tok}
+    res["workload"] = f"{cfg.name} attention call, K as E4M3 codes with per-token exponents, V bf16 or int8 codes"
+    res["peak"], res["peak_kind"] = peak, peak_kind
+    return res
+
+
 def measure_stage(args, dev, stream, rank):
     """Host-resident cold pages: a quarter of the 128K-token sequence's pages
     (512 pages of [4 heads][64][256] bf16, K and V: 128 MiB) staged from
@@ -890,7 +944,9 @@ def run_vq_only(args):
              parent=torch.from_numpy(inp["parent"]).to(dev))
     step = LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, device=dev)
     LT.lucetree_build_anc_mask(d["parent"], step.anc, step.status, stream)
-    print(json.dumps({"quantised_v": measure_vq(args, dev, stream, 0, d, step, cfg)}), flush=True)
+    d["v_pool"] = h16(inp["v_pool"])
+    print(json.dumps({"quantised_v": measure_vq(args, dev, stream, 0, d, step, cfg),
+                      "quantised_k": measure_kq(args, dev, stream, 0, d, step, cfg)}), flush=True)
     return 0
 
 

@@ -280,6 +280,10 @@ LUCETREE_API lucetree_status lucetree_verify_step_workspace(int B, int N, int Hq
 LUCETREE_API lucetree_status lucetree_verify_step(const lucetree_step_args* args, void* workspace,
                                                   size_t workspace_bytes, void* stream);
 
+/* K storage formats (lucetree_verify_attn_kq, lucetree_commit_kq). */
+#define LUCETREE_K_SAME 0 /* K in the args' 16-bit dtype */
+#define LUCETREE_K_E4M3 1 /* FP8 E4M3 codes [num_pages][Hkv][64][D], value = e4m3(code) * 2^(e - 127) */
+
 /* V storage formats of lucetree_verify_attn_vq (K stays in the args' dtype). */
 #define LUCETREE_V_SAME 0 /* V in the args' 16-bit dtype (lucetree_verify_attn) */
 #define LUCETREE_V_INT8 1 /* int8 codes [num_pages][Hkv][64][D], value = code * 2^(e - 127) */
@@ -306,6 +310,54 @@ LUCETREE_API lucetree_status lucetree_verify_step(const lucetree_step_args* args
 LUCETREE_API lucetree_status lucetree_verify_attn_vq(const lucetree_attn_args* args, int v_format,
                                                      const uint8_t* v_exp, void* workspace, size_t workspace_bytes,
                                                      void* stream);
+
+/*
+ * Workspace bytes lucetree_verify_attn_kq needs on the CURRENT device: the
+ * attention partials plus the two E4M3 parts of the scaled queries (B*N*Hq*D
+ * bytes each) and one float per key segment.  Needs no initialisation;
+ * 256-byte aligned.  UNSUPPORTED for shapes without a kernel (D != 256).
+ */
+LUCETREE_API lucetree_status lucetree_verify_attn_kq_workspace(int B, int N, int Hq, int Hkv, int D,
+                                                               size_t* bytes);
+
+/*
+ * lucetree_verify_attn with K held as FP8 E4M3 codes: asymmetric K/V storage
+ * on the K side (the pages list KV quantisation, TQ3_0 and asymmetric K/V
+ * quantisation among the project's components without defining a format:
+ * "Lucebox Hub", section "Speculative decoding 계층"; forum post, section
+ * "Lucebox의 최적화 구성요소"; this format is the library's own):
+ *   - a->k_pool holds the codes [num_pages][Hkv][64][D] (uint8);
+ *   - k_exp [num_pages][Hkv][64] holds one exponent byte e per token and KV
+ *     head (16-byte aligned); the value is e4m3(code) * 2^(e - 127), e = 0
+ *     reads as zero, e = 255 and the NaN codes (0x7F, 0xFF) are outside the
+ *     contract;
+ *   - V as in lucetree_verify_attn (v_format LUCETREE_V_SAME) or as the codes
+ *     of lucetree_verify_attn_vq (LUCETREE_V_INT8 / LUCETREE_V_INT4 with v_exp).
+ * QK runs on the FP8 tensor cores with the queries of each (sequence, KV
+ * head) scaled by one power of two and split into two E4M3 parts, which
+ * reproduce exactly every bf16 query element whose scaled magnitude is at
+ * least 1/4 (the largest lies in (224, 448]; smaller elements are off by at
+ * most 2^-10 of the scaled unit);
+ * the tree's own K/V (k_tree, v_tree) stay bf16.  bf16 queries, D = 256.
+ * Errors as lucetree_verify_attn, plus UNSUPPORTED (dtype, D, v_format) and
+ * INVALID_ARG (k_exp / v_exp null or misaligned).
+ */
+LUCETREE_API lucetree_status lucetree_verify_attn_kq(const lucetree_attn_args* args, const uint8_t* k_exp,
+                                                     int v_format, const uint8_t* v_exp, void* workspace,
+                                                     size_t workspace_bytes, void* stream);
+
+/*
+ * lucetree_commit into a K pool held as E4M3 codes (args->k_pool: codes
+ * [num_pages][Hkv][64][D], k_exp [num_pages][Hkv][64]) with V in bf16: the
+ * k-th accepted node's K row of each KV head is stored at position L_b + k as
+ * its codes and exponent: e = 127 - p with p the largest integer such that
+ * max|k| * 2^p <= 448, code_d = e4m3(k_d * 2^p) rounded to nearest, ties to
+ * the even code.  A row of zeros, or one whose largest magnitude is below
+ * 2^-118 (e would leave [1, 254]), is stored as zero (e = 0).  V rows, the
+ * length update, the rollback and the device checks are those of
+ * lucetree_commit.  bf16, D = 256.
+ */
+LUCETREE_API lucetree_status lucetree_commit_kq(const lucetree_commit_args* args, uint8_t* k_exp, void* stream);
 
 /* Arguments of lucetree_lmhead_argmax. */
 typedef struct lucetree_lmhead_args {

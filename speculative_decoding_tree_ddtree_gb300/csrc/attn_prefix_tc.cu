@@ -27,11 +27,16 @@ cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream) {
     const cuuint32_t estr[3] = {1, 1, 1};
 
     // K, V pools as 2-D [num_pages * Hkv * 64 rows][D]; box = one 64-token page x 64 dims
-    CUtensorMap tk, tv, tq;
+    // (E4M3 K: codes as bytes [rows][D], box = one page x 128 dims)
+    const bool kq = L.k_format == LUCETREE_K_E4M3;
+    CUtensorMap tk, tv, tq, tq2;
     const cuuint64_t kv_dims[2] = {(cuuint64_t)a.D, (cuuint64_t)a.num_pages * a.Hkv * kPage};
     const cuuint64_t kv_strides[1] = {(cuuint64_t)a.D * 2};
     const cuuint32_t kv_box[2] = {64, (cuuint32_t)kPage};
-    if (enc(&tk, dt, 2, const_cast<void*>(a.k_pool), kv_dims, kv_strides, kv_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const cuuint64_t kc_strides[1] = {(cuuint64_t)a.D};
+    const cuuint32_t kc_box[2] = {128, (cuuint32_t)kPage};
+    if (enc(&tk, kq ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : dt, 2, const_cast<void*>(a.k_pool), kv_dims,
+            kq ? kc_strides : kv_strides, kq ? kc_box : kv_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
@@ -43,10 +48,23 @@ cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream) {
     const cuuint64_t q_dims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.N};
     const cuuint64_t q_strides[2] = {(cuuint64_t)a.D * 2, (cuuint64_t)a.Hq * a.D * 2};
     const cuuint32_t q_box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)p.rg.NPG};
-    if (enc(&tq, dt, 3, const_cast<void*>(a.q), q_dims, q_strides, q_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (!kq && enc(&tq, dt, 3, const_cast<void*>(a.q), q_dims, q_strides, q_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    tq2 = tv;
+    if (kq) {
+        // the two E4M3 parts of the scaled queries, bytes with the layout of q; box = 128 dims x G x NPG
+        const cuuint64_t qb_strides[2] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq * a.D};
+        const cuuint32_t qb_box[3] = {128, (cuuint32_t)p.G, (cuuint32_t)p.rg.NPG};
+        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(L.q_hi), q_dims, qb_strides, qb_box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            enc(&tq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(L.q_lo), q_dims, qb_strides, qb_box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
 
     // quantised V: codes as bytes [rows][D or D/2] (one 64-token page x 128 dims per box, no
     // swizzle: the softmax warps expand them), exponents [num_pages * Hkv][64] one page per box
@@ -71,6 +89,7 @@ cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream) {
     }
 
     const int rgp = (p.rg.RG + 15) / 16 * 16;
+    if (kq) return launch_prefix_tc_bf16_256_kq(rgp, vq, tk, tv, tq, tve, tq2, L, stream);
     if (a.dtype == LUCETREE_BF16)
         return a.D == 256 ? launch_prefix_tc_bf16_256(rgp, vq, tk, tv, tq, tve, L, stream)
                           : launch_prefix_tc_bf16_128(rgp, tk, tv, tq, L, stream);

@@ -193,10 +193,6 @@ struct TileCursor {
     }
 };
 
-// Position of tile j's V operand in the ring's operand sequence
-// K(0) K(1) V(0) K(2) V(1) ... K(n-1) V(n-2) V(n-1).
-__device__ __forceinline__ uint32_t v_operand(uint32_t j, uint32_t n) { return j + 1 < n ? 2 * j + 2 : 2 * j + 1; }
-
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -255,13 +251,23 @@ __device__ __forceinline__ void set_abort(Misc* ms, uint32_t* status) {
 }
 __device__ __forceinline__ bool aborted(Misc* ms) { return *(volatile int*)&ms->abort_flag != 0; }
 
-template <int D, bool BF16, int RGP, int VQ>
+// KQ = 1: K held as FP8 E4M3 codes with one power-of-two exponent per token
+// (the codes [128 keys][128 dims] fill a 16 KB chunk, so a 256-dim K tile is
+// two chunks); the queries arrive split in two E4M3 parts (tm_q: high part,
+// tm_q2: low part, both scaled by one power of two per key segment) and QK
+// runs as two kind::f8f6f4 MMAs per 32-dim step into the same accumulator.
+// The softmax multiplies each key's scores by its exponent and the segment's
+// query scale.
+template <int D, bool BF16, int RGP, int VQ, int KQ>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_ve,
-                     const AttnLaunch L) {
+                     const __grid_constant__ CUtensorMap tm_q2, const AttnLaunch L) {
     using Lay = Layout<D, RGP>;
-    constexpr int kChunks = Lay::kChunks;
+    constexpr int kChunks = Lay::kChunks;                  // Q chunks (16-bit: 64 dims; E4M3: 2 parts x 128 dims)
+    constexpr int kChunksK = KQ ? D / 128 : D / 64;        // ring chunks per K operand
+    constexpr int kChunksV = D / 64;                       // ring chunks per V operand
+    static_assert(!KQ || (D == 256 && BF16), "E4M3 K: head dim 256, bf16 queries");
     constexpr int kNch = Lay::kNch;
     constexpr int kNa = (kNch + kSmGroups - 1) / kSmGroups;  // column chunks per softmax warp (at most)
     constexpr int kNS = Lay::kNS;
@@ -322,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_q);
         if (VQ) prefetch_tensormap(&tm_ve);
+        if (KQ) prefetch_tensormap(&tm_q2);
     }
     tc_fence_before();
     __syncthreads();
@@ -352,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t chunk = 0, vchunk = 0;
         int q_loads = 0;
         bool ok = true;
-        // one operand (one tile's K or V): kChunks slots of two boxes each
+        // one operand (one tile's K or V): kChunksK / kChunksV slots of two boxes each
         auto issue = [&](bool is_v, int row0, int row1) -> bool {
-            for (int c = 0; c < kChunks; ++c) {
+            for (int c = 0; c < (is_v ? kChunksV : kChunksK); ++c) {
                 const int slot = chunk % kNS;
                 const bool w = mbar_wait(&ms->empty[slot], ((chunk / kNS) & 1) ^ 1);
                 if (!__all_sync(0xffffffffu, w)) return false;  // lanes agree on a timeout
@@ -380,10 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d_hint(dst, &tm_v, x, row, bar, pol_stream);
                         tma_load_2d_hint(dst + 8192, &tm_v, x + 64, row, bar, pol_stream);
                     } else {
-                        // [128 keys: page 0 then page 1][dims 64 * c .. +63]
+                        // [128 keys: page 0 then page 1][dims 64 * c .. +63] (16-bit K), or
+                        // [128 keys][dims 128 * c .. +127] (E4M3 codes: x counts bytes)
                         mbar_arrive_expect_tx(bar, kChunkBytes);
-                        tma_load_2d_hint(dst, &tm_k, 64 * c, row0, bar, pol_stream);
-                        tma_load_2d_hint(dst + 8192, &tm_k, 64 * c, row1, bar, pol_stream);
+                        tma_load_2d_hint(dst, &tm_k, (KQ ? 128 : 64) * c, row0, bar, pol_stream);
+                        tma_load_2d_hint(dst + 8192, &tm_k, (KQ ? 128 : 64) * c, row1, bar, pol_stream);
                     }
                 }
                 __syncwarp();
@@ -421,8 +429,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&ms->q_full, kChunks * RG * 128);
                     const int b = cur.pc.s / p.Hkv, g = cur.pc.s % p.Hkv;
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d(sQ + c * RGP * 128, &tm_q, 64 * c, g * p.G, b * p.N + i0, &ms->q_full);
+                    if constexpr (KQ) {
+                        // high parts, then low parts: [RGP rows][128 dims] bytes per chunk
+                        for (int c = 0; c < D / 128; ++c) {
+                            tma_load_3d(sQ + c * RGP * 128, &tm_q, 128 * c, g * p.G, b * p.N + i0, &ms->q_full);
+                            tma_load_3d(sQ + (D / 128 + c) * RGP * 128, &tm_q2, 128 * c, g * p.G, b * p.N + i0,
+                                        &ms->q_full);
+                        }
+                    } else {
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_3d(sQ + c * RGP * 128, &tm_q, 64 * c, g * p.G, b * p.N + i0, &ms->q_full);
+                    }
                 }
                 __syncwarp();
                 ++q_loads;
@@ -465,7 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         if (lane == 0) {
-            const uint32_t id_qk = idesc_f16(128, RGP, kAB, 0, 0);
+            // (for E4M3 K the same descriptor bits read as E4M3 x E4M3 under kind::f8f6f4)
+            const uint32_t id_qk = idesc_f16(128, RGP, KQ ? 0u : kAB, 0, 0);
             const uint32_t id_pv = idesc_f16(128, RGP, 0u, 1, 1);  // fp16 V and P
             constexpr uint64_t hi_k = desc_hi(16, 1024, kLayoutSwizzle128);
             constexpr uint64_t hi_v = desc_hi(8192, 1024, kLayoutSwizzle128);  // 2nd 64-dim box at +8 KB
@@ -486,15 +504,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(&ms->q_full, qk.piece_no & 1)) return false;
                     tc_fence_after();
                 }
-                for (int c = 0; c < kChunks; ++c) {
+                for (int c = 0; c < kChunksK; ++c) {
                     const int slot = chunk % kNS;
                     if (!mbar_wait(&ms->full[slot], (chunk / kNS) & 1)) return false;
                     tc_fence_after();
 #pragma unroll
                     for (int sub = 0; sub < 4; ++sub) {
                         const uint64_t ad = make_desc(hi_k, aS + slot * kChunkBytes + sub * 32);
-                        const uint64_t bd = make_desc(hi_k, aQ + c * RGP * 128 + sub * 32);
-                        mma_f16_ss(tmem, ad, bd, id_qk, (c | sub) != 0);
+                        if constexpr (KQ) {
+                            // 32 dims per step: K codes times the high, then the low query part
+                            const uint64_t bh = make_desc(hi_k, aQ + c * RGP * 128 + sub * 32);
+                            const uint64_t bl = make_desc(hi_k, aQ + (kChunksK + c) * RGP * 128 + sub * 32);
+                            mma_f8f6f4_ss(tmem, ad, bh, id_qk, (c | sub) != 0);
+                            mma_f8f6f4_ss(tmem, ad, bl, id_qk, 1u);
+                        } else {
+                            const uint64_t bd = make_desc(hi_k, aQ + c * RGP * 128 + sub * 32);
+                            mma_f16_ss(tmem, ad, bd, id_qk, (c | sub) != 0);
+                        }
                     }
                     mma_commit(&ms->empty[slot]);
                     ++chunk;
@@ -518,12 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool first = pv.first();
                 // output dims 128h..128h+127: chunk 2h holds keys 0..63, chunk
                 // 2h+1 keys 64..127 (four 16-key steps each)
-                for (int h = 0; h < kChunks / 2 && ok; ++h) {
+                for (int h = 0; h < kChunksV / 2 && ok; ++h) {
                     const uint32_t dO = tmem + (h ? Lay::kColO1 : Lay::kColO0);
                     for (int kh = 0; kh < 2 && ok; ++kh) {
                         const int slot = chunk % kNS;
                         // landed and converted by the softmax warps
-                        const uint32_t vn = j * kChunks + 2 * h + kh;
+                        const uint32_t vn = j * kChunksV + 2 * h + kh;
                         if (!(ok = mbar_wait(&ms->vready[vn % kMaxSlots], (vn / kMaxSlots) & 1))) break;
                         tc_fence_after();
 #pragma unroll
@@ -561,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cb = min(hf * kNa, kNch), ce = min(cb + kNa, kNch);
         const int nch = ce - cb;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float sl2 = L.scale_log2;
+        float sl2 = L.scale_log2;  // E4M3 K: set per tile from the key's exponent and the segment's query scale
         const int my_half = kl >> 6;  // which 64-token page of the tile holds my key
         uint32_t j = 0;
         bool bad = false;  // warp-uniform at every tcgen05 load / store below
@@ -642,6 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kNa * 16; ++i) lpart[i] = 0.f;
             uint32_t page_bits = 0;
+            int pid_lane = -1;  // E4M3 K: page id of my key's page for tile (batch start + lane)
 
             while (cur.live && cur.piece_no == piece_no) {
                 const int t = cur.t;
@@ -654,6 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (tt < cur.pc.te && pg < (cur.pc.L + kPage - 1) / kPage) {
                         const int pid = a.page_table[(size_t)(seg / p.Hkv) * p.max_pages + pg];
                         okp = pid >= 0 && pid < a.num_pages;
+                        pid_lane = pid;
                     }
                     page_bits = __ballot_sync(0xffffffffu, okp);
                 }
@@ -661,6 +689,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool page_ok = (page_bits >> tb) & 1u;
                 const bool valid = kl < nvalid && page_ok;
                 const bool first = cur.first();
+                if constexpr (KQ) {
+                    // my key's exponent byte (one load, overlapping the wait for S^T)
+                    const int pid_t = __shfl_sync(0xffffffffu, pid_lane, tb);
+                    uint32_t ek = 0;
+                    if (valid) ek = L.k_exp[((size_t)pid_t * p.Hkv + seg % p.Hkv) * kPage + (kl & (kPage - 1))];
+                    sl2 = L.q_scale[seg] * __uint_as_float(ek << 23);  // x 2^(e - 127); e = 0 reads as zero
+                }
 
                 // S^T(j) ready (P^T and O^T are waited for later: PV(j-1) may still
                 // be reading P^T while this tile's exponents are computed)
@@ -773,9 +808,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // 64 * (c & 1) + (u % 512) / 8 (each 8 KB box is [64 keys][128 B];
                 // the swizzle permutes units only within a key's row).
                 if (!bad) {
-                    const uint32_t vbase = v_operand(j, n_tiles) * kChunks;
-                    for (int c = 0; c < kChunks; ++c) {
-                        const uint32_t vn = j * kChunks + c;
+                    // ring position of V(j)'s first chunk: the K operands before it
+                    // (K(0) .. K(j+1), or .. K(j) for the last tile) and V(0) .. V(j-1)
+                    const uint32_t vbase = (j + 1 < n_tiles ? j + 2 : j + 1) * kChunksK + j * kChunksV;
+                    for (int c = 0; c < kChunksV; ++c) {
+                        const uint32_t vn = j * kChunksV + c;
                         const bool landed = wait_all(&ms->vfull[vn % kMaxSlots], (vn / kMaxSlots) & 1);
                         if (VQ != 2 && !landed) {  // (int4 reports a timeout through its barrier)
                             bad = true;
@@ -947,32 +984,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, bool BF16, int RGP, int VQ>
+template <int D, bool BF16, int RGP, int VQ, int KQ>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq, const CUtensorMap& tve,
-                       const AttnLaunch& L, cudaStream_t stream) {
+                       const CUtensorMap& tq2, const AttnLaunch& L, cudaStream_t stream) {
     using Lay = Layout<D, RGP>;
-    auto kern = prefix_tc_kernel<D, BF16, RGP, VQ>;
+    auto kern = prefix_tc_kernel<D, BF16, RGP, VQ, KQ>;
     static SmemLimitSeen seen;
     cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), Lay::kBytes, seen);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(grid_ctas(L.plan)), dim3(kThreads), Lay::kBytes, stream, tk, tv, tq, tve, L);
+    return launch_pdl(kern, dim3(grid_ctas(L.plan)), dim3(kThreads), Lay::kBytes, stream, tk, tv, tq, tve, tq2, L);
 }
 
-// tve: the per-token exponents of quantised V (VQ != 0); unused otherwise
-template <int D, bool BF16, int VQ = 0>
+// tve: the per-token exponents of quantised V (VQ != 0); tq2: the low query
+// parts of E4M3 K (KQ != 0); unused otherwise
+template <int D, bool BF16, int VQ = 0, int KQ = 0>
 cudaError_t launch_rgp(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                       const CUtensorMap& tve, const AttnLaunch& L, cudaStream_t stream) {
+                       const CUtensorMap& tve, const CUtensorMap& tq2, const AttnLaunch& L, cudaStream_t stream) {
     static_assert(kRowsMax == 144, "one instantiation per padded row count up to kRowsMax");
     switch (rgp) {
-        case 16: return launch_one<D, BF16, 16, VQ>(tk, tv, tq, tve, L, stream);
-        case 32: return launch_one<D, BF16, 32, VQ>(tk, tv, tq, tve, L, stream);
-        case 48: return launch_one<D, BF16, 48, VQ>(tk, tv, tq, tve, L, stream);
-        case 64: return launch_one<D, BF16, 64, VQ>(tk, tv, tq, tve, L, stream);
-        case 80: return launch_one<D, BF16, 80, VQ>(tk, tv, tq, tve, L, stream);
-        case 96: return launch_one<D, BF16, 96, VQ>(tk, tv, tq, tve, L, stream);
-        case 112: return launch_one<D, BF16, 112, VQ>(tk, tv, tq, tve, L, stream);
-        case 128: return launch_one<D, BF16, 128, VQ>(tk, tv, tq, tve, L, stream);
-        case 144: return launch_one<D, BF16, 144, VQ>(tk, tv, tq, tve, L, stream);
+        case 16: return launch_one<D, BF16, 16, VQ, KQ>(tk, tv, tq, tve, tq2, L, stream);
+        case 32: return launch_one<D, BF16, 32, VQ, KQ>(tk, tv, tq, tve, tq2, L, stream);
+        case 48: return launch_one<D, BF16, 48, VQ, KQ>(tk, tv, tq, tve, tq2, L, stream);
+        case 64: return launch_one<D, BF16, 64, VQ, KQ>(tk, tv, tq, tve, tq2, L, stream);
+        case 80: return launch_one<D, BF16, 80, VQ, KQ>(tk, tv, tq, tve, tq2, L, stream);
+        case 96: return launch_one<D, BF16, 96, VQ, KQ>(tk, tv, tq, tve, tq2, L, stream);
+        case 112: return launch_one<D, BF16, 112, VQ, KQ>(tk, tv, tq, tve, tq2, L, stream);
+        case 128: return launch_one<D, BF16, 128, VQ, KQ>(tk, tv, tq, tve, tq2, L, stream);
+        case 144: return launch_one<D, BF16, 144, VQ, KQ>(tk, tv, tq, tve, tq2, L, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -982,6 +1020,10 @@ cudaError_t launch_rgp(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, co
 // tve: the exponent map of quantised V; vq: 0 = 16-bit V, 1 = int8 codes, 2 = int4 codes (head dim 256)
 cudaError_t launch_prefix_tc_bf16_256(int rgp, int vq, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                       const CUtensorMap&, const AttnLaunch&, cudaStream_t);
+// E4M3 K (codes map tk, query parts tq / tq2) with V as vq above; bf16, head dim 256
+cudaError_t launch_prefix_tc_bf16_256_kq(int rgp, int vq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                         const CUtensorMap& tq, const CUtensorMap& tve, const CUtensorMap& tq2,
+                                         const AttnLaunch&, cudaStream_t);
 cudaError_t launch_prefix_tc_bf16_128(int rgp, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                       const AttnLaunch&, cudaStream_t);
 cudaError_t launch_prefix_tc_f16_256(int rgp, int vq, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,

@@ -5,7 +5,7 @@ namespace lucetree {
 
 cudaError_t launch_prefix_tc_bf16_256_v16(int rgp, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                                           const AttnLaunch& L, cudaStream_t stream) {
-    return prefix_tc::launch_rgp<256, true>(rgp, tk, tv, tq, tv, L, stream);
+    return prefix_tc::launch_rgp<256, true>(rgp, tk, tv, tq, tv, tv, L, stream);
 }
 
 }  // namespace lucetree

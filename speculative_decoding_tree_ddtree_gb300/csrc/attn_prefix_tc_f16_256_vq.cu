@@ -10,8 +10,8 @@ cudaError_t launch_prefix_tc_f16_256_v16(int rgp, const CUtensorMap& tk, const C
 cudaError_t launch_prefix_tc_f16_256(int rgp, int vq, const CUtensorMap& tk, const CUtensorMap& tv,
                                      const CUtensorMap& tq, const CUtensorMap& tve, const AttnLaunch& L,
                                      cudaStream_t stream) {
-    if (vq == 1) return prefix_tc::launch_rgp<256, false, 1>(rgp, tk, tv, tq, tve, L, stream);
-    if (vq == 2) return prefix_tc::launch_rgp<256, false, 2>(rgp, tk, tv, tq, tve, L, stream);
+    if (vq == 1) return prefix_tc::launch_rgp<256, false, 1>(rgp, tk, tv, tq, tve, tv, L, stream);
+    if (vq == 2) return prefix_tc::launch_rgp<256, false, 2>(rgp, tk, tv, tq, tve, tv, L, stream);
     return launch_prefix_tc_f16_256_v16(rgp, tk, tv, tq, L, stream);
 }
 

@@ -16,7 +16,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblucetree.so")
 
 LUCETREE_OK = 0
-LUCETREE_V_INT8, LUCETREE_V_INT4 = 1, 2
+LUCETREE_V_SAME, LUCETREE_V_INT8, LUCETREE_V_INT4 = 0, 1, 2
+LUCETREE_K_SAME, LUCETREE_K_E4M3 = 0, 1
 LUCETREE_F16 = 0
 LUCETREE_BF16 = 1
 PAGE_SIZE = 64
@@ -50,6 +51,9 @@ EXPORTED = (
     "lucetree_selftest_wait_timeout",
     "lucetree_verify_step_workspace",
     "lucetree_verify_step",
+    "lucetree_verify_attn_kq_workspace",
+    "lucetree_verify_attn_kq",
+    "lucetree_commit_kq",
 )
 
 
@@ -151,6 +155,9 @@ def load(path: str | None = None):
     lib.lucetree_selftest_wait_timeout.argtypes = [P, ctypes.c_longlong, P, P]
     lib.lucetree_verify_step_workspace.argtypes = [I, I, I, I, I, I, ctypes.POINTER(SZ)]
     lib.lucetree_verify_step.argtypes = [ctypes.POINTER(StepArgs), P, SZ, P]
+    lib.lucetree_verify_attn_kq_workspace.argtypes = [I, I, I, I, I, ctypes.POINTER(SZ)]
+    lib.lucetree_verify_attn_kq.argtypes = [ctypes.POINTER(AttnArgs), P, I, P, P, SZ, P]
+    lib.lucetree_commit_kq.argtypes = [ctypes.POINTER(CommitArgs), P, P]
     for name in EXPORTED:
         if name not in ("lucetree_status_string", "lucetree_abi_version"):
             getattr(lib, name).restype = I
@@ -241,15 +248,20 @@ def lucetree_verify_attn_workspace(B: int, N: int, Hq: int, Hkv: int, D: int) ->
 
 
 def _check_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse,
-                v_format=None, v_exp=None):
+                v_format=None, v_exp=None, k_exp=None):
     """Shapes and element types of one tree-verify attention call (layouts as
-    lucetree_verify_attn documents them); v_format selects the quantised V pool."""
+    lucetree_verify_attn documents them); v_format selects the quantised V
+    pool, k_exp the E4M3 K pool (k_pool then holds the codes)."""
     B, N, Hq, D = _dims(q, "q", 4)
     if q.dtype not in _H16:
         raise LucetreeError(f"q: unsupported dtype {q.dtype}")
     P, Hkv, page, _ = _dims(k_pool, "k_pool", 4)
-    _expect(k_pool, "k_pool", (P, Hkv, page, D), (q.dtype,))
-    if v_format is None:
+    if k_exp is None:
+        _expect(k_pool, "k_pool", (P, Hkv, page, D), (q.dtype,))
+    else:
+        _expect(k_pool, "k_codes", (P, Hkv, page, D), _U8)
+        _expect(k_exp, "k_exp", (P, Hkv, page), _U8)
+    if v_format is None or v_format == LUCETREE_V_SAME:
         _expect(v_pool, "v_pool", (P, Hkv, page, D), (q.dtype,))
     else:
         _expect(v_pool, "v_codes", (P, Hkv, page, D // 2 if v_format == LUCETREE_V_INT4 else D), _U8)
@@ -266,8 +278,9 @@ def _check_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask
 
 
 def _attn_args(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale,
-               v_format=None, v_exp=None):
-    _check_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, v_format, v_exp)
+               v_format=None, v_exp=None, k_exp=None):
+    _check_attn(q, k_pool, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, v_format, v_exp,
+                k_exp)
     B, N, Hq, D = q.shape
     Hkv = k_pool.shape[1]
     a = AttnArgs()
@@ -305,6 +318,27 @@ def lucetree_verify_attn_vq(q, k_pool, v_codes, v_exp, v_format, page_table, ctx
     a = _attn_args(q, k_pool, v_codes, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale,
                    v_format=v_format, v_exp=v_exp)
     _check(load().lucetree_verify_attn_vq(ctypes.byref(a), int(v_format), _ptr(v_exp), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lucetree_verify_attn_kq_workspace(B: int, N: int, Hq: int, Hkv: int, D: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().lucetree_verify_attn_kq_workspace(B, N, Hq, Hkv, D, ctypes.byref(n)))
+    return int(n.value)
+
+
+def lucetree_verify_attn_kq(q, k_codes, k_exp, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status,
+                            workspace, v_format=LUCETREE_V_SAME, v_exp=None, lse=None, scale: float | None = None,
+                            stream=None):
+    """As lucetree_verify_attn with K stored as FP8 E4M3: k_codes uint8
+    [P][Hkv][64][D], k_exp uint8 [P][Hkv][64] (value = e4m3(code) * 2^(e - 127));
+    V in q's dtype (v_format LUCETREE_V_SAME) or as int8 / int4 codes with
+    v_exp.  bf16 queries, D = 256; workspace from lucetree_verify_attn_kq_workspace."""
+    if v_format not in (LUCETREE_V_SAME, LUCETREE_V_INT8, LUCETREE_V_INT4):
+        raise LucetreeError(f"unsupported V format {v_format}")
+    a = _attn_args(q, k_codes, v_pool, page_table, ctx_len, k_tree, v_tree, anc_mask, out, status, lse, scale,
+                   v_format=v_format, v_exp=v_exp, k_exp=k_exp)
+    _check(load().lucetree_verify_attn_kq(ctypes.byref(a), _ptr(k_exp), int(v_format), _ptr(v_exp), _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -373,6 +407,38 @@ def lucetree_commit(k_tree, v_tree, acc_nodes, acc_len, page_table, ctx_len_in, 
     c.ctx_len_in, c.ctx_len_out = _ptr(ctx_len_in), _ptr(ctx_len_out)
     c.k_pool, c.v_pool, c.status = _ptr(k_pool), _ptr(v_pool), _ptr(status)
     _check(load().lucetree_commit(ctypes.byref(c), _stream(stream)))
+
+
+def lucetree_commit_kq(k_tree, v_tree, acc_nodes, acc_len, page_table, ctx_len_in, ctx_len_out, k_codes, k_exp,
+                       v_pool, status, stream=None):
+    """lucetree_commit into a K pool held as E4M3 codes (k_codes uint8
+    [P][Hkv][64][D], k_exp uint8 [P][Hkv][64]): each accepted K row is stored
+    quantised; V rows are copied into the bf16 v_pool."""
+    B, N, Hkv, D = _dims(k_tree, "k_tree", 4)
+    if k_tree.dtype != torch.bfloat16:
+        raise LucetreeError(f"k_tree: expected bfloat16, got {k_tree.dtype}")
+    _expect(v_tree, "v_tree", (B, N, Hkv, D), (k_tree.dtype,))
+    _expect(acc_nodes, "acc_nodes", (B, N), _I32)
+    _expect(acc_len, "acc_len", (B,), _I32)
+    _expect(page_table, "page_table", (B, _dims(page_table, "page_table", 2)[1]), _I32)
+    _expect(ctx_len_in, "ctx_len_in", (B,), _I32)
+    _expect(ctx_len_out, "ctx_len_out", (B,), _I32)
+    P, _, page, _ = _dims(k_codes, "k_codes", 4)
+    _expect(k_codes, "k_codes", (P, Hkv, page, D), _U8)
+    _expect(k_exp, "k_exp", (P, Hkv, page), _U8)
+    _expect(v_pool, "v_pool", (P, Hkv, page, D), (k_tree.dtype,))
+    _expect_status(status)
+    c = CommitArgs()
+    c.dtype = dtype_code(k_tree)
+    c.B, c.N, c.Hkv, c.D = B, N, Hkv, D
+    c.page_size = page
+    c.k_tree, c.v_tree = _ptr(k_tree), _ptr(v_tree)
+    c.acc_nodes, c.acc_len = _ptr(acc_nodes), _ptr(acc_len)
+    c.page_table, c.max_pages_per_seq = _ptr(page_table), page_table.shape[1]
+    c.num_pages = P
+    c.ctx_len_in, c.ctx_len_out = _ptr(ctx_len_in), _ptr(ctx_len_out)
+    c.k_pool, c.v_pool, c.status = _ptr(k_codes), _ptr(v_pool), _ptr(status)
+    _check(load().lucetree_commit_kq(ctypes.byref(c), _ptr(k_exp), _stream(stream)))
 
 
 # ---------------------------------------------------------------- one whole step
