@@ -669,6 +669,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < kNa * 16; ++i) lpart[i] = 0.f;
             uint32_t page_bits = 0;
             int pid_lane = -1;  // E4M3 K: page id of my key's page for tile (batch start + lane)
+            // E4M3 K: my key's exponent byte, loaded one tile ahead; the segment's query scale
+            auto page_of = [&](int tile) -> int {
+                const int pg = 2 * tile + my_half;
+                return pg < (cur.pc.L + kPage - 1) / kPage ? a.page_table[(size_t)(seg / p.Hkv) * p.max_pages + pg] : -1;
+            };
+            auto k_exp_of = [&](int pid) -> uint32_t {
+                return pid >= 0 && pid < a.num_pages
+                           ? (uint32_t)L.k_exp[((size_t)pid * p.Hkv + seg % p.Hkv) * kPage + (kl & (kPage - 1))]
+                           : 0u;
+            };
+            uint32_t ek_next = 0;
+            float qs = 0.f;
+            if constexpr (KQ) {
+                ek_next = k_exp_of(page_of(cur.pc.ta));
+                qs = L.q_scale[seg];
+            }
 
             while (cur.live && cur.piece_no == piece_no) {
                 const int t = cur.t;
@@ -678,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int tt = t + lane;
                     const int pg = 2 * tt + my_half;
                     bool okp = false;
+                    pid_lane = -1;
                     if (tt < cur.pc.te && pg < (cur.pc.L + kPage - 1) / kPage) {
                         const int pid = a.page_table[(size_t)(seg / p.Hkv) * p.max_pages + pg];
                         okp = pid >= 0 && pid < a.num_pages;
@@ -690,11 +707,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = kl < nvalid && page_ok;
                 const bool first = cur.first();
                 if constexpr (KQ) {
-                    // my key's exponent byte (one load, overlapping the wait for S^T)
-                    const int pid_t = __shfl_sync(0xffffffffu, pid_lane, tb);
-                    uint32_t ek = 0;
-                    if (valid) ek = L.k_exp[((size_t)pid_t * p.Hkv + seg % p.Hkv) * kPage + (kl & (kPage - 1))];
-                    sl2 = L.q_scale[seg] * __uint_as_float(ek << 23);  // x 2^(e - 127); e = 0 reads as zero
+                    // this tile's exponent was loaded during the previous tile; load the next one's
+                    const uint32_t ek = valid ? ek_next : 0u;
+                    if (t + 1 < cur.pc.te) {
+                        const int pid1 = tb + 1 < 32 ? __shfl_sync(0xffffffffu, pid_lane, tb + 1) : page_of(t + 1);
+                        ek_next = k_exp_of(pid1);
+                    }
+                    sl2 = qs * __uint_as_float(ek << 23);  // x 2^(e - 127); e = 0 reads as zero
                 }
 
                 // S^T(j) ready (P^T and O^T are waited for later: PV(j-1) may still

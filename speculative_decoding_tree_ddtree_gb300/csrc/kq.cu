@@ -48,9 +48,13 @@ __device__ __forceinline__ int scale_exponent(float m) {
     return mant <= 0.875f ? 9 - ex : 8 - ex;
 }
 
-// One CTA per key segment s = (b, g): the largest |q| over the segment's
-// rows (nodes x heads of the group), then q 2^p split into two E4M3 parts,
-// written with the layout of q, and the segment's score factor.
+// Grid (key segment s = (b, g), part y): every CTA finds the largest |q| over
+// the segment's rows (nodes x heads of the group; eight 16-byte loads in
+// flight per thread), then splits its own part of the rows: q 2^p into two
+// E4M3 parts written with the layout of q.  Part 0 also writes the segment's
+// score factor.
+constexpr int kSplitItems = 4;  // 8-value items per thread in the split pass
+
 __global__ void __launch_bounds__(kSplitThreads) q_split_kernel(const __nv_bfloat16* __restrict__ q, int N, int Hq,
                                                                 int G, int D, float scale_log2,
                                                                 uint8_t* __restrict__ q_hi,
@@ -70,11 +74,20 @@ __global__ void __launch_bounds__(kSplitThreads) q_split_kernel(const __nv_bfloa
         return (((size_t)b * N + i) * Hq + h) * D + (size_t)u * 8;
     };
     float m = 0.f;
-    for (int it = threadIdx.x; it < items; it += kSplitThreads) {
-        float v[8];
-        load8_f32<__nv_bfloat16>(q + row_of(it), v);
+    for (int it0 = threadIdx.x; it0 < items; it0 += 8 * kSplitThreads) {
+        uint4 raw[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
+        for (int u = 0; u < 8; ++u) {
+            const int it = it0 + u * kSplitThreads;
+            raw[u] = it < items ? *reinterpret_cast<const uint4*>(q + row_of(it)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float v[8];
+            load8_f32<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16*>(&raw[u]), v);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -84,8 +97,12 @@ __global__ void __launch_bounds__(kSplitThreads) q_split_kernel(const __nv_bfloa
 #pragma unroll
     for (int w = 0; w < kSplitThreads / 32; ++w) m = fmaxf(m, red[w]);
     const int p = scale_exponent(m);
-    if (threadIdx.x == 0) q_scale[s] = ldexpf(scale_log2, -p);
-    for (int it = threadIdx.x; it < items; it += kSplitThreads) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) q_scale[s] = ldexpf(scale_log2, -p);
+    const int it_base = blockIdx.y * kSplitThreads * kSplitItems + threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < kSplitItems; ++u) {
+        const int it = it_base + u * kSplitThreads;
+        if (it >= items) break;
         const size_t off = row_of(it);
         float v[8];
         load8_f32<__nv_bfloat16>(q + off, v);
@@ -251,7 +268,9 @@ extern "C" lucetree_status lucetree_verify_attn_kq(const lucetree_attn_args* a, 
     L.q_lo = reinterpret_cast<uint8_t*>(ws + w.lo);
     L.q_scale = reinterpret_cast<float*>(ws + w.scale);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_pdl(q_split_kernel, dim3(L.plan.S), dim3(kSplitThreads), 0, s,
+    const int items = a->N * L.plan.G * a->D / 8;
+    const int parts = (items + kSplitThreads * kSplitItems - 1) / (kSplitThreads * kSplitItems);
+    if (launch_pdl(q_split_kernel, dim3(L.plan.S, parts), dim3(kSplitThreads), 0, s,
                    reinterpret_cast<const __nv_bfloat16*>(a->q), a->N, a->Hq, L.plan.G, a->D, L.scale_log2,
                    const_cast<uint8_t*>(L.q_hi), const_cast<uint8_t*>(L.q_lo), const_cast<float*>(L.q_scale)) !=
         cudaSuccess)
