@@ -518,9 +518,9 @@ def run_ours(args, cfg):
     host = dict(q=h16(inp["q"], True), k_tree=h16(inp["k_tree"], True), v_tree=h16(inp["v_tree"], True),
                 parent=torch.from_numpy(inp["parent"]).pin_memory(), draft=torch.from_numpy(inp["draft"]).pin_memory(),
                 logits=torch.from_numpy(inp["logits"]).pin_memory())
-    res = dict(acc_nodes=torch.empty_like(step.acc_nodes, device="cpu").pin_memory(),
-               acc_len=torch.empty_like(step.acc_len, device="cpu").pin_memory(),
-               bonus=torch.empty_like(step.bonus, device="cpu").pin_memory())
+    # the step's result (accepted path, count, bonus token, new length) is one
+    # contiguous device buffer: one copy reads it back
+    res = dict(results=torch.empty_like(step.results, device="cpu").pin_memory())
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in res.values())
     e2e_steps = min(args.steps, 500)
@@ -557,10 +557,7 @@ def run_ours(args, cfg):
             stream.wait_event(ev_in[i % 2])
             one(dd=bufs[i % 2])
             ev_used[i % 2].record(stream)
-            rr = results[i % 2]
-            rr["acc_nodes"].copy_(step.acc_nodes, non_blocking=True)
-            rr["acc_len"].copy_(step.acc_len, non_blocking=True)
-            rr["bonus"].copy_(step.bonus, non_blocking=True)
+            results[i % 2]["results"].copy_(step.results, non_blocking=True)
             ev_res[i % 2].record(stream)
         if i >= 1:
             ev_res[(i - 1) % 2].synchronize()  # the host has step i-1's result
@@ -821,7 +818,7 @@ def measure_kq(args, dev, stream, rank, d, step, cfg):
     """The headline attention call with K stored as FP8 E4M3 codes (one
     power-of-two exponent per token and head) and V in bf16 or as int8 codes,
     timed with CUDA events on the stream over resident inputs.  The codes
-    are drawn on the device as uniform finite E4M3 codes with exponents in
+    are drawn on the device from N(0, 160^2) values, the exponents uniform in
     [120, 124] (the generator's distribution for this format)."""
     import torch
     from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
@@ -831,8 +828,14 @@ def measure_kq(args, dev, stream, rank, d, step, cfg):
     peak, peak_kind = peak_hbm()
     g = torch.Generator(device=dev)
     g.manual_seed(99 + rank)
-    kc = torch.randint(0, 254, (P, cfg.Hkv, W.PAGE, cfg.D), generator=g, device=dev, dtype=torch.int32)
-    kc = (kc + (kc >= 127).int()).to(torch.uint8)  # skip 0x7F; 0xFF is never drawn
+    # codes of N(0, 160^2) values (a row's largest magnitude near the top of E4M3's range, as a per-token
+    # scale puts it), the distribution of the generator's default
+    kc = torch.empty((P, cfg.Hkv, W.PAGE, cfg.D), dtype=torch.uint8, device=dev)
+    flat = kc.view(-1)
+    for i in range(0, flat.numel(), 1 << 26):
+        j = min(flat.numel(), i + (1 << 26))
+        x = (torch.randn(j - i, generator=g, device=dev) * 160.0).clamp_(-448.0, 448.0)
+        flat[i:j] = x.to(torch.float8_e4m3fn).view(torch.uint8)
     ke = torch.randint(120, 125, (P, cfg.Hkv, W.PAGE), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
     vq = W.generate_vq(cfg, W.V_INT8, seed=rank)
     vcodes = torch.from_numpy(vq["v_codes"]).to(dev)

@@ -506,10 +506,14 @@ class VerifyStep:
         self.out = torch.empty(B, N, Hq, D, dtype=torch.float32, device=dev)
         self.lse = torch.empty(B, N, Hq, dtype=torch.float32, device=dev)
         self.argmax = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
-        self.acc_nodes = torch.empty(B, N, dtype=torch.int32, device=dev)
-        self.acc_len = torch.empty(B, dtype=torch.int32, device=dev)
-        self.bonus = torch.empty(B, dtype=torch.int32, device=dev)
-        self.ctx_out = torch.empty(B, dtype=torch.int32, device=dev)
+        # the step's result in one contiguous int32 buffer (one copy reads it
+        # back): accepted path [B][N], accepted count [B], bonus token [B],
+        # new committed length [B]
+        self.results = torch.empty(B * N + 3 * B, dtype=torch.int32, device=dev)
+        self.acc_nodes = self.results[:B * N].view(B, N)
+        self.acc_len = self.results[B * N:B * N + B]
+        self.bonus = self.results[B * N + B:B * N + 2 * B]
+        self.ctx_out = self.results[B * N + 2 * B:]
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self._packed = {}
 

@@ -52,9 +52,9 @@ def _reference(cfg, inp, kq, v_format=0, vq=None):
     return oracle.verify_attn(ref, oracle.BF16)
 
 
-def _check(cfg, seed, v_format=0, lse=True):
+def _check(cfg, seed, v_format=0, lse=True, dist="normal"):
     inp = W.generate(cfg, seed=seed, with_logits=False)
-    kq = W.generate_kq(cfg, seed=seed)
+    kq = W.generate_kq(cfg, seed=seed, dist=dist)
     vq = W.generate_vq(cfg, v_format, seed=seed) if v_format else None
     got, got_lse, status = _run_kq(cfg, inp, kq, v_format, vq, lse=lse)
     assert status == 0
@@ -66,12 +66,14 @@ def _check(cfg, seed, v_format=0, lse=True):
         assert np.abs(got_lse - ref_lse).max() <= 1e-3 * np.maximum(1.0, np.abs(ref_lse)).max()
 
 
+@pytest.mark.parametrize("dist", ["normal", "uniform"])
 @pytest.mark.parametrize("v_format", [0, W.V_INT8, W.V_INT4], ids=["bf16v", "int8v", "int4v"])
-def test_kq_ragged_batch(cuda_dev, v_format):
-    # committed lengths straddle tile (128) and page (64) boundaries, one is empty
+def test_kq_ragged_batch(cuda_dev, v_format, dist):
+    # committed lengths straddle tile (128) and page (64) boundaries, one is empty; codes spread over the
+    # whole E4M3 range ("uniform") move the running maxima on most tiles
     cfg = W.VerifyConfig("kq-ragged", ctx=(0, 1, 63, 65, 127, 129, 1000, 2049), Hq=12, Hkv=3, D=256, dtype=W.BF16,
                          N=9, tree="random", branch_cap=3, vocab=512, paged="permuted", spare_pages=5)
-    _check(cfg, 21, v_format)
+    _check(cfg, 21, v_format, dist=dist)
 
 
 @pytest.mark.parametrize("v_format", [0, W.V_INT8], ids=["bf16v", "int8v"])

@@ -122,10 +122,15 @@ def test_quantised_storage_inputs_follow_their_recipe():
     nib = np.stack([v4["v_codes"] & 0xF, v4["v_codes"] >> 4]).astype(np.int64)
     signed = np.where(nib >= 8, nib - 16, nib)
     assert signed.min() == -7 and signed.max() == 7  # the code -8 is never drawn
-    kq = W.generate_kq(cfg, seed=0)
+    kq = W.generate_kq(cfg, seed=0, dist="uniform")
     assert kq["k_codes"].shape == pools and not ((kq["k_codes"] & 0x7F) == 0x7F).any()  # no NaN codes
     assert kq["k_exp"].min() >= 120 and kq["k_exp"].max() <= 124
     assert len(np.unique(kq["k_codes"])) == 254
+    import oracle
+    kn = W.generate_kq(cfg, seed=0)  # the "normal" draw: N(0, 160^2) values toward zero
+    assert kn["k_codes"].shape == pools and not ((kn["k_codes"] & 0x7F) == 0x7F).any()
+    v = oracle.decode_e4m3(kn["k_codes"])
+    assert abs(v.std() - 160.0) < 8.0 and np.abs(v).max() == 448.0
 
 
 def test_lmhead_inputs_follow_their_recipe():
@@ -135,3 +140,22 @@ def test_lmhead_inputs_follow_their_recipe():
     assert a["hidden"].dtype == a["weight"].dtype == np.uint16
     assert abs(float(_f64(a["hidden"], cfg.dtype).std()) - 1.0) < 0.05
     assert abs(float(_f64(a["weight"], cfg.dtype).std()) - cfg.w_std) < 0.001
+
+
+def test_e4m3_code_toward_zero_bit_construction():
+    """The generator's code draw: the code's value never exceeds |x| and the
+    next larger code does (values below 448), signs follow x, no NaN codes."""
+    import oracle
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(50000) * 160.0, rng.standard_normal(5000) * 1e-3, [0.0, -0.0, 448.0,
+                                                                                                 -600.0, 2.0 ** -9]])
+    c = W.e4m3_code_toward_zero(x)
+    assert not ((c & 0x7F) == 0x7F).any()
+    v = oracle.decode_e4m3(c)
+    a = np.minimum(np.abs(x), 448.0)
+    assert (np.abs(v) <= a).all()
+    vals = oracle.decode_e4m3(np.arange(0x7F, dtype=np.uint8))
+    up = vals[np.minimum(np.searchsorted(vals, np.abs(v)) + 1, len(vals) - 1)]
+    assert ((up > a) | (np.abs(v) == 448.0)).all()
+    assert (np.signbit(v) == np.signbit(x)).all()
+    assert W.e4m3_code_toward_zero(np.array([1.0, 448.0, 2.0 ** -9])).tolist() == [0x38, 0x7E, 0x01]

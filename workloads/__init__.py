@@ -410,16 +410,48 @@ def generate_vq(cfg: VerifyConfig, v_format: int, seed: int = 0) -> dict:
     return dict(v_codes=codes, v_exp=v_exp)
 
 
-def generate_kq(cfg: VerifyConfig, seed: int = 0) -> dict:
+def e4m3_code_toward_zero(x: np.ndarray) -> np.ndarray:
+    """Bit construction of the FP8 E4M3 code whose value is the largest
+    magnitude not above |x| (|x| <= 448; sign from x): exponent field
+    floor(log2|x|) + 7 and the significand's top three fraction bits, or a
+    subnormal code below 2^-6.  Used to draw stored codes from a value
+    distribution."""
+    a = np.minimum(np.abs(np.asarray(x, np.float64)), 448.0)
+    e = np.clip(np.floor(np.log2(np.maximum(a, 2.0 ** -40))) + 7, 0, 15).astype(np.int64)
+    normal = a >= 2.0 ** -6
+    m_norm = np.floor((a / np.ldexp(1.0, e - 7) - 1.0) * 8.0).astype(np.int64)
+    m_sub = np.floor(a / 2.0 ** -9).astype(np.int64)
+    m = np.clip(np.where(normal, m_norm, m_sub), 0, 7)
+    e = np.where(normal, e, 0)
+    m = np.where((e == 15) & (m == 7), 6, m)          # 0x7F / 0xFF are NaN: 448 is the top
+    return ((np.signbit(x).astype(np.int64) << 7) | (e << 3) | m).astype(np.uint8)
+
+
+def generate_kq(cfg: VerifyConfig, seed: int = 0, dist: str = "normal") -> dict:
     """Quantised K pool for ``cfg``'s page geometry, drawn as storage: k_codes
-    uint8 [num_pages][Hkv][64][D], FP8 E4M3 codes uniform over the finite ones
-    (NaN codes 0x7F / 0xFF excluded), k_exp uint8 [num_pages][Hkv][64] uniform in
-    [120, 124]."""
+    uint8 [num_pages][Hkv][64][D] FP8 E4M3 codes and k_exp uint8
+    [num_pages][Hkv][64] uniform in [120, 124].
+      dist "normal": the codes of N(0, 1) values times 160 (so a row's largest
+        magnitude is near the top of E4M3's range, as a per-token scale puts
+        it), taken toward zero to a representable value;
+      dist "uniform": uniform over the 254 finite codes (NaN codes 0x7F / 0xFF
+        excluded) -- magnitudes spread over E4M3's whole range, so a key
+        segment meets new score maxima often."""
     rng = np.random.default_rng(np.random.SeedSequence([seed, _name_key(cfg.name), 0x4B51]))
     need = [pages_needed(L, cfg.N) for L in cfg.ctx]
     num_pages = sum(need) + cfg.spare_pages
     shape = (num_pages, cfg.Hkv, PAGE, cfg.D)
-    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
-    codes = finite[rng.integers(0, len(finite), size=shape)]
+    if dist == "uniform":
+        finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+        codes = finite[rng.integers(0, len(finite), size=shape)]
+    elif dist == "normal":
+        codes = np.empty(shape, np.uint8)
+        flat = codes.reshape(-1)
+        step = 1 << 24
+        for i in range(0, flat.size, step):
+            j = min(flat.size, i + step)
+            flat[i:j] = e4m3_code_toward_zero(rng.standard_normal(j - i) * 160.0)
+    else:
+        raise ValueError(dist)
     k_exp = rng.integers(120, 125, size=shape[:3]).astype(np.uint8)
     return dict(k_codes=codes, k_exp=k_exp)
