@@ -819,7 +819,7 @@ def measure_kq(args, dev, stream, rank, d, step, cfg):
     power-of-two exponent per token and head) and V in bf16 or as int8 codes,
     timed with CUDA events on the stream over resident inputs.  The codes
     are drawn on the device from N(0, 160^2) values, the exponents uniform in
-    [120, 124] (the generator's distribution for this format)."""
+    [119, 120] (keys of about unit spread: the generator's default)."""
     import torch
     from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
     res = {}
@@ -836,7 +836,7 @@ def measure_kq(args, dev, stream, rank, d, step, cfg):
         j = min(flat.numel(), i + (1 << 26))
         x = (torch.randn(j - i, generator=g, device=dev) * 160.0).clamp_(-448.0, 448.0)
         flat[i:j] = x.to(torch.float8_e4m3fn).view(torch.uint8)
-    ke = torch.randint(120, 125, (P, cfg.Hkv, W.PAGE), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    ke = torch.randint(119, 121, (P, cfg.Hkv, W.PAGE), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
     vq = W.generate_vq(cfg, W.V_INT8, seed=rank)
     vcodes = torch.from_numpy(vq["v_codes"]).to(dev)
     vexp = torch.from_numpy(vq["v_exp"]).to(dev)

@@ -131,6 +131,7 @@ def test_quantised_storage_inputs_follow_their_recipe():
     assert kn["k_codes"].shape == pools and not ((kn["k_codes"] & 0x7F) == 0x7F).any()
     v = oracle.decode_e4m3(kn["k_codes"])
     assert abs(v.std() - 160.0) < 8.0 and np.abs(v).max() == 448.0
+    assert kn["k_exp"].min() == 119 and kn["k_exp"].max() == 120
 
 
 def test_lmhead_inputs_follow_their_recipe():

@@ -430,13 +430,16 @@ def e4m3_code_toward_zero(x: np.ndarray) -> np.ndarray:
 def generate_kq(cfg: VerifyConfig, seed: int = 0, dist: str = "normal") -> dict:
     """Quantised K pool for ``cfg``'s page geometry, drawn as storage: k_codes
     uint8 [num_pages][Hkv][64][D] FP8 E4M3 codes and k_exp uint8
-    [num_pages][Hkv][64] uniform in [120, 124].
+    [num_pages][Hkv][64].
       dist "normal": the codes of N(0, 1) values times 160 (so a row's largest
         magnitude is near the top of E4M3's range, as a per-token scale puts
-        it), taken toward zero to a representable value;
-      dist "uniform": uniform over the 254 finite codes (NaN codes 0x7F / 0xFF
-        excluded) -- magnitudes spread over E4M3's whole range, so a key
-        segment meets new score maxima often."""
+        it), taken toward zero to a representable value, with exponents
+        uniform in [119, 120]: stored keys of about unit spread, like the
+        16-bit workloads' N(0, 1) keys;
+      dist "uniform": codes uniform over the 254 finite codes (NaN codes
+        0x7F / 0xFF excluded) and exponents uniform in [120, 124] --
+        magnitudes spread over E4M3's whole range and 16x between tokens, so
+        a key segment meets new score maxima often (a stress case)."""
     rng = np.random.default_rng(np.random.SeedSequence([seed, _name_key(cfg.name), 0x4B51]))
     need = [pages_needed(L, cfg.N) for L in cfg.ctx]
     num_pages = sum(need) + cfg.spare_pages
@@ -453,5 +456,6 @@ def generate_kq(cfg: VerifyConfig, seed: int = 0, dist: str = "normal") -> dict:
             flat[i:j] = e4m3_code_toward_zero(rng.standard_normal(j - i) * 160.0)
     else:
         raise ValueError(dist)
-    k_exp = rng.integers(120, 125, size=shape[:3]).astype(np.uint8)
+    lo, hi = (119, 120) if dist == "normal" else (120, 124)
+    k_exp = rng.integers(lo, hi + 1, size=shape[:3]).astype(np.uint8)
     return dict(k_codes=codes, k_exp=k_exp)
