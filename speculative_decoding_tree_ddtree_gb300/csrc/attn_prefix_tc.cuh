@@ -64,6 +64,7 @@ namespace prefix_tc {
 using namespace tc;
 
 constexpr int kSmGroups = 3;                        // softmax warps per TMEM lane quarter
+constexpr int kConvWarps = 2;                       // warps 2, 3: 16-bit V conversion
 constexpr int kSmWarps = 4 * kSmGroups;             // 12 softmax warps
 constexpr int kSoftmaxThreads = 32 * kSmWarps;      // 384
 constexpr int kThreads = 128 + kSoftmaxThreads;     // + warpgroup 0 (producer, MMA, two idle warps)
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kMaxSlots; ++i) {
             mbar_init(&ms->vfull[i], 1);
-            mbar_init(&ms->vready[i], kSmWarps);
+            mbar_init(&ms->vready[i], VQ == 0 ? kConvWarps : kSmWarps);
         }
         mbar_init(&ms->s_full, 1);
         mbar_init(&ms->s_free, kSmWarps);
@@ -574,6 +575,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (VQ == 0) {
+        // ============================================================ V conversion (warps 2, 3)
+        // Each 16-bit V chunk, once landed: bf16 -> fp16 in place (exact below
+        // 65536; a larger magnitude becomes inf and the merge flags the row),
+        // and the rows of keys at or past L in a partial page zeroed (the pool
+        // holds arbitrary data there and 0 * NaN would poison O^T); then
+        // vready.  Doing this here rather than in the softmax warps keeps a
+        // late V tile from holding up the next tile's exponents.  Thread ct
+        // owns 16-byte units ct + 64 i of a chunk; unit u holds 8 dims of key
+        // 64 * (c & 1) + (u % 512) / 8 (each 8 KB box is [64 keys][128 B]; the
+        // swizzle permutes units only within a key's row).
+        const int ct = threadIdx.x - 64;  // 0 .. 63
+        TileCursor cur;
+        cur.start(t0, t1, p, a.ctx_len);
+        uint32_t j = 0;
+        bool ok = true;
+        while (ok && cur.live) {
+            const int nvalid = min(kTileKeys, cur.pc.L - cur.t * kTileKeys);
+            // ring position of V(j)'s first chunk: the K operands before it
+            // (K(0) .. K(j+1), or .. K(j) for the last tile) and V(0) .. V(j-1)
+            const uint32_t vbase = (j + 1 < n_tiles ? j + 2 : j + 1) * kChunksK + j * kChunksV;
+            for (int c = 0; c < kChunksV; ++c) {
+                const uint32_t vn = j * kChunksV + c;
+                const bool landed = mbar_wait(&ms->vfull[vn % kMaxSlots], (vn / kMaxSlots) & 1);
+                if (!__all_sync(0xffffffffu, landed) || aborted(ms)) {
+                    ok = false;
+                    break;
+                }
+                uint4* base = reinterpret_cast<uint4*>(sSlots + ((vbase + c) % kNS) * kChunkBytes);
+                const int nv = nvalid - 64 * (c & 1);  // valid keys of this chunk's page
+                if (BF16 || nv < 64) {
+                    constexpr int kUnits = kChunkBytes / 16 / (32 * kConvWarps);  // 16 per thread
+                    constexpr int kBatch = 4;                                      // loads in flight
+#pragma unroll 1
+                    for (int i0 = 0; i0 < kUnits; i0 += kBatch) {
+                        uint4 x[kBatch];
+                        bool kv[kBatch];
+#pragma unroll
+                        for (int k = 0; k < kBatch; ++k) {
+                            const int u = ct + 32 * kConvWarps * (i0 + k);
+                            kv[k] = ((u & 511) >> 3) < nv;
+                            x[k] = kv[k] ? base[u] : make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                        for (int k = 0; k < kBatch; ++k) {
+                            const int u = ct + 32 * kConvWarps * (i0 + k);
+                            if constexpr (BF16) {
+                                x[k].x = bf16x2_to_f16x2(x[k].x);
+                                x[k].y = bf16x2_to_f16x2(x[k].y);
+                                x[k].z = bf16x2_to_f16x2(x[k].z);
+                                x[k].w = bf16x2_to_f16x2(x[k].w);
+                            }
+                            if (BF16 || !kv[k]) base[u] = x[k];
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ms->vready[vn % kMaxSlots]);
+            }
+            ++j;
+            cur.step(p, a.ctx_len);
+        }
+        if (!ok) set_abort(ms, a.status);
     }
     } else {
         regs_inc<kRegsSoftmax>();
@@ -820,13 +885,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();              // every lane's stores and fence come before lane 0's arrive
                 if (!bad && lane == 0) mbar_arrive(&ms->p_full);
 
-                // V(j), chunk by chunk as it lands: bf16 -> fp16 in place, rows of
-                // keys at or past L zeroed (the pool holds arbitrary data there and
-                // 0 * NaN would poison O^T).  Thread st owns the 16-byte units
-                // st, st + 384, st + 768 of a chunk; unit u holds 8 dims of key
-                // 64 * (c & 1) + (u % 512) / 8 (each 8 KB box is [64 keys][128 B];
-                // the swizzle permutes units only within a key's row).
-                if (!bad) {
+                // Quantised V(j), chunk by chunk as it lands: the codes expanded in
+                // place to the fp16 operand, rows of keys at or past L zeroed (the
+                // pool holds arbitrary data there and 0 * NaN would poison O^T).
+                // (16-bit V is converted by warps 2 and 3.)  Unit u of a chunk holds
+                // 8 dims of key 64 * (c & 1) + (u % 512) / 8 (each 8 KB box is
+                // [64 keys][128 B]; the swizzle permutes units only within a key's row).
+                if (!bad && VQ != 0) {
                     // ring position of V(j)'s first chunk: the K operands before it
                     // (K(0) .. K(j+1), or .. K(j) for the last tile) and V(0) .. V(j-1)
                     const uint32_t vbase = (j + 1 < n_tiles ? j + 2 : j + 1) * kChunksK + j * kChunksV;
@@ -916,25 +981,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     }
                                     base[u] = make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]),
                                                          pack_half2(f[4], f[5]), pack_half2(f[6], f[7]));
-                                }
-                            }
-                        } else if (BF16 || nv < 64) {
-#pragma unroll
-                            for (int i = 0; i < 3; ++i) {
-                                const int u = st + kSoftmaxThreads * i;
-                                if (u < 1024) {
-                                    const bool kv = ((u & 511) >> 3) < nv;
-                                    uint4 x = make_uint4(0, 0, 0, 0);
-                                    if (kv) {
-                                        x = base[u];
-                                        if constexpr (BF16) {
-                                            x.x = bf16x2_to_f16x2(x.x);
-                                            x.y = bf16x2_to_f16x2(x.y);
-                                            x.z = bf16x2_to_f16x2(x.z);
-                                            x.w = bf16x2_to_f16x2(x.w);
-                                        }
-                                    }
-                                    if (BF16 || !kv) base[u] = x;
                                 }
                             }
                         }
