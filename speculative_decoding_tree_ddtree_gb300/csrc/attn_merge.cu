@@ -6,21 +6,24 @@ namespace lucetree {
 
 namespace {
 
+constexpr int kWarps = 4;  // per CTA = per output row; up to four CTAs per SM
+constexpr int kThreads = 32 * kWarps;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(merge::kThreads, 3) merge_kernel(AttnLaunch L) {
-    __shared__ float s_o[merge::kWarps][D];
-    __shared__ float s_red[merge::kWarps];
+__global__ void __launch_bounds__(kThreads, 4) merge_kernel(AttnLaunch L) {
+    __shared__ float s_o[kWarps][D];
+    __shared__ float s_red[kWarps];
     if (threadIdx.x == 0) pdl_trigger();
     const long long row = blockIdx.x;
     const int i = (int)((row / L.plan.Hq) % L.plan.N);
     const int b = (int)(row / ((long long)L.plan.Hq * L.plan.N));
-    merge::merge_row<T, D>(L, row, L.a.anc_mask[(size_t)b * L.plan.N + i], s_o, s_red);
+    merge::merge_row<T, D, kWarps>(L, row, L.a.anc_mask[(size_t)b * L.plan.N + i], s_o, s_red);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_merge(const AttnLaunch& L, cudaStream_t stream) {
-    const dim3 grid((unsigned)((long long)L.plan.B * L.plan.N * L.plan.Hq)), block(merge::kThreads);
+    const dim3 grid((unsigned)((long long)L.plan.B * L.plan.N * L.plan.Hq)), block(kThreads);
     if (L.a.dtype == LUCETREE_BF16) {
         if (L.a.D == 256) return launch_pdl(merge_kernel<__nv_bfloat16, 256>, grid, block, 0, stream, L);
         return launch_pdl(merge_kernel<__nv_bfloat16, 128>, grid, block, 0, stream, L);

@@ -34,9 +34,14 @@ __device__ inline float warp_max(float v) {
     return v;
 }
 
-constexpr int kWarps = 8;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kRound = 5;  // partial rows per warp per round, all loads in flight together
+// Warps per output row: 4 in the merge launch (one 128-thread CTA per row, up
+// to four CTAs per SM, so a 528-row call fits in one wave), 8 in the fused
+// step's finish kernel (256-thread CTAs shared with the argmax).  Each warp
+// folds its partials in rounds of kRound<W> rows, all loads of a round in
+// flight together.
+template <int W>
+constexpr int kRound = W >= 8 ? 5 : 10;
+constexpr int kMaxTreeBatch = 4;  // ancestors whose K/V a warp loads before using any
 
 template <typename T, int D>
 __device__ inline void load_slice(const T* p, float (&out)[D / 32]) {
@@ -55,14 +60,15 @@ __device__ inline void load_partial(const float* op, float (&v)[DPL]) {
 }
 
 
-// One output row (b, node i, head h) by the whole CTA (kThreads threads).
-// anc: the node's ancestor-or-self mask.  s_o: kWarps x D floats and s_red:
-// kWarps floats of shared memory.  Runs the tree block, then pdl_wait(), then
-// the log-sum-exp merge of the prefix partials.
-template <typename T, int D>
+// One output row (b, node i, head h) by the whole CTA (W warps).  anc: the
+// node's ancestor-or-self mask.  s_o: W x D floats and s_red: W floats of
+// shared memory.  Runs the tree block, then pdl_wait(), then the log-sum-exp
+// merge of the prefix partials.
+template <typename T, int D, int W>
 __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, uint64_t anc, float (*s_o)[D],
                                           float* s_red) {
     constexpr int DPL = D / 32;
+    constexpr int kR = kRound<W>;
     const lucetree_attn_args& a = L.a;
     const PlanDims& p = L.plan;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -75,8 +81,9 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
     const int s = b * p.Hkv + g;
 
     // ---- tree block: keys of the node's ancestors and itself, the k-th such
-    // key (in node order) handled by warp k % kWarps with its own running
-    // max, sum and output slice
+    // key (in node order) handled by warp k % W with its own running max, sum
+    // and output slice; a warp loads the K/V slices of up to kMaxTreeBatch of
+    // its keys before using any
     float o[DPL];
 #pragma unroll
     for (int x = 0; x < DPL; ++x) o[x] = 0.f;
@@ -86,27 +93,54 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
         load_slice<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)row * D + lane * DPL, qf);
         if (p.N < 64) anc &= (1ull << p.N) - 1ull;
         if (!((anc >> i) & 1ull) && threadIdx.x == 0) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
+        // this warp's keys: every W-th set bit of anc, starting at rank `warp`
+        uint64_t mine = 0;
+        {
+            uint64_t rest = anc;
+            int rank = 0;
+            while (rest) {
+                const int j = __ffsll((long long)rest) - 1;
+                rest &= rest - 1ull;
+                if ((rank++ % W) == warp) mine |= 1ull << j;
+            }
+        }
         const T* kt = reinterpret_cast<const T*>(a.k_tree);
         const T* vt = reinterpret_cast<const T*>(a.v_tree);
-        int rank = 0;
-        while (anc) {
-            const int j = __ffsll((long long)anc) - 1;
-            anc &= anc - 1ull;
-            if ((rank++ % kWarps) != warp) continue;
-            const size_t base = (((size_t)b * p.N + j) * p.Hkv + g) * D + lane * DPL;
-            float kf[DPL], vf[DPL];
-            load_slice<T, D>(kt + base, kf);
-            load_slice<T, D>(vt + base, vf);
-            float dot = 0.f;
+        while (mine) {
+            int js[kMaxTreeBatch];
+            int nb = 0;
 #pragma unroll
-            for (int x = 0; x < DPL; ++x) dot = fmaf(qf[x], kf[x], dot);
-            const float sc = warp_sum(dot) * L.scale_log2;
-            const float mn = fmaxf(m_t, sc);
-            const float alpha = exp2f(m_t - mn), pj = exp2f(sc - mn);
-            l_t = l_t * alpha + pj;
+            for (int u = 0; u < kMaxTreeBatch; ++u) {
+                js[u] = -1;
+                if (mine) {
+                    js[u] = __ffsll((long long)mine) - 1;
+                    mine &= mine - 1ull;
+                    ++nb;
+                }
+            }
+            float kf[kMaxTreeBatch][DPL], vf[kMaxTreeBatch][DPL];
 #pragma unroll
-            for (int x = 0; x < DPL; ++x) o[x] = fmaf(o[x], alpha, pj * vf[x]);
-            m_t = mn;
+            for (int u = 0; u < kMaxTreeBatch; ++u) {
+                if (u < nb) {
+                    const size_t base = (((size_t)b * p.N + js[u]) * p.Hkv + g) * D + lane * DPL;
+                    load_slice<T, D>(kt + base, kf[u]);
+                    load_slice<T, D>(vt + base, vf[u]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kMaxTreeBatch; ++u) {
+                if (u >= nb) continue;
+                float dot = 0.f;
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) dot = fmaf(qf[x], kf[u][x], dot);
+                const float sc = warp_sum(dot) * L.scale_log2;
+                const float mn = fmaxf(m_t, sc);
+                const float alpha = exp2f(m_t - mn), pj = exp2f(sc - mn);
+                l_t = l_t * alpha + pj;
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) o[x] = fmaf(o[x], alpha, pj * vf[u][x]);
+                m_t = mn;
+            }
         }
     }
 
@@ -135,22 +169,24 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
     const size_t sf = slot_floats(p);
     const float* ws = L.ws + slot_index(p, rg, c_lo, s) * sf;
     // with fewer tiles than CTAs some CTAs own no tile and write no partial
+    const bool every_cta_owns = nT >= p.Cg;
     auto has_partial = [&](int k) {
-        return k < count && cta_begin(c_lo + k, nT, p.Cg) != cta_begin(c_lo + k + 1, nT, p.Cg);
+        return k < count &&
+               (every_cta_owns || cta_begin(c_lo + k, nT, p.Cg) != cta_begin(c_lo + k + 1, nT, p.Cg));
     };
 
-    // Each warp folds partials w, w + kWarps, w + 2 kWarps, ... into its own
-    // running (max, sum, output slice), which starts from its share of the
-    // tree block.  All of a round's loads (up to kRound partials per warp:
-    // maxima, sums and the row slices) are issued before any is used, so a
-    // round costs one trip to L2; the headline shapes need one round.
+    // Each warp folds partials w, w + W, w + 2 W, ... into its own running
+    // (max, sum, output slice), which starts from its share of the tree block.
+    // All of a round's loads (up to kR partials per warp: maxima, sums and
+    // the row slices) are issued before any is used, so a round costs one trip
+    // to L2; the headline shapes need one round.
     float m_w = m_t, l_w = l_t;
-    for (int k0 = warp; k0 < count; k0 += kWarps * kRound) {
-        float mk[kRound], lk[kRound];
-        float part[kRound][DPL];
+    for (int k0 = warp; k0 < count; k0 += W * kR) {
+        float mk[kR], lk[kR];
+        float part[kR][DPL];
 #pragma unroll
-        for (int u = 0; u < kRound; ++u) {
-            const int k = k0 + u * kWarps;
+        for (int u = 0; u < kR; ++u) {
+            const int k = k0 + u * W;
             mk[u] = -INFINITY;
             lk[u] = 0.f;
             if (has_partial(k)) {
@@ -165,14 +201,14 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
         }
         float mr = m_w;
 #pragma unroll
-        for (int u = 0; u < kRound; ++u) mr = fmaxf(mr, mk[u]);
+        for (int u = 0; u < kR; ++u) mr = fmaxf(mr, mk[u]);
         if (mr > -INFINITY) {
             const float a0 = m_w > -INFINITY ? exp2f(m_w - mr) : 0.f;
             l_w *= a0;
 #pragma unroll
             for (int x = 0; x < DPL; ++x) o[x] *= a0;
 #pragma unroll
-            for (int u = 0; u < kRound; ++u) {
+            for (int u = 0; u < kR; ++u) {
                 const float w = mk[u] > -INFINITY ? exp2f(mk[u] - mr) : 0.f;
                 l_w = fmaf(w, lk[u], l_w);
 #pragma unroll
@@ -187,7 +223,7 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
     __syncthreads();
     float mmax = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, s_red[w]);
+    for (int w = 0; w < W; ++w) mmax = fmaxf(mmax, s_red[w]);
     const float aw = m_w > -INFINITY ? exp2f(m_w - mmax) : 0.f;
 #pragma unroll
     for (int x = 0; x < DPL; ++x) s_o[warp][lane * DPL + x] = o[x] * aw;
@@ -199,13 +235,13 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
     // ---- combine the warps' sums and write the row
     float l = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) l += s_red[w];
+    for (int w = 0; w < W; ++w) l += s_red[w];
     const float inv = 1.f / l;
     float* orow = a.out + (size_t)row * D;
-    for (int d = threadIdx.x; d < D; d += kThreads) {
+    for (int d = threadIdx.x; d < D; d += 32 * W) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += s_o[w][d];
+        for (int w = 0; w < W; ++w) v += s_o[w][d];
         v *= inv;
         orow[d] = v;
         if (!isfinite(v)) atomicOr(a.status, LUCETREE_DEV_NONFINITE);

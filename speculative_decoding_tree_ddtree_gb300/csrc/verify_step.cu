@@ -44,12 +44,13 @@ struct StepLaunch {
 };
 
 constexpr int kThreads = 256;
-static_assert(kThreads == am::kThreads && kThreads == merge::kThreads, "one CTA size for every part");
+constexpr int kMergeWarps = kThreads / 32;  // a merge CTA's warps all work on its row
+static_assert(kThreads == am::kThreads, "one CTA size for every part");
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) finish_kernel(const StepLaunch S) {
-    __shared__ float s_o[merge::kWarps][D];
-    __shared__ float s_red[merge::kWarps];
+    __shared__ float s_o[kMergeWarps][D];
+    __shared__ float s_red[kMergeWarps];
     __shared__ unsigned long long s_key[kThreads / 32];
     __shared__ int32_t s_par[LUCETREE_MAX_NODES];
     __shared__ int s_flag, s_good;
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StepLaunch S) {
     bool bad = false;
     const uint64_t anc = tree::anc_walk(s_par, i, &bad);
     if (bad && threadIdx.x == 0 && (row % p.Hq) == 0) atomicOr(S.attn.a.status, LUCETREE_DEV_BAD_PARENT);
-    merge::merge_row<T, D>(S.attn, row, anc, s_o, s_red);
+    merge::merge_row<T, D, kMergeWarps>(S.attn, row, anc, s_o, s_red);
 }
 
 template <typename T, int D>
