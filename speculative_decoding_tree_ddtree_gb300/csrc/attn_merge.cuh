@@ -1,19 +1,19 @@
 // attn_merge.cuh -- tree block + log-sum-exp merge of tree-verify attention,
 // as a CTA device routine shared by the merge kernel and the fused step.
 //
-// One block per output row (b, node i, head h).  The warps share the softmax
+// One group of four warps per output row (b, node i, head h).  The warps share the softmax
 // over the tree keys j with bit j of anc_mask[b][i] set (the node's ancestors
 // and itself) and the prefix partials (O, max, sum) that the split-K prefix
 // kernel left for this row's key segment; the block writes out = O / sum and
 // lse = ln(sum) + max.  Maxima are kept in the log2 domain
 // (scores pre-multiplied by log2 e), so every rescale is one exp2.
 //
-// The partials are independent: warp w folds partials w, w + 8, ... into a
+// The partials are independent: warp w folds partials w, w + 4, ... into a
 // running (max, sum, output slice) of its own, issuing all of a round's
-// loads before using any, and the eight warps' parts are combined through
-// shared memory on their common maximum.  A block reads about 40 partial
-// rows of D floats, so spreading them over eight warps, five rows each, gets
-// the whole row in about one L2 round trip instead of one dependent row at a
+// loads before using any, and the four warps' parts are combined through
+// shared memory on their common maximum.  A row reads about 40 partial rows
+// of D floats, so spreading them over four warps, five rows a round, gets the
+// whole row in about two L2 round trips instead of one dependent row at a
 // time.
 #pragma once
 
@@ -34,13 +34,12 @@ __device__ inline float warp_max(float v) {
     return v;
 }
 
-// Warps per output row: 4 in the merge launch (one 128-thread CTA per row, up
-// to four CTAs per SM, so a 528-row call fits in one wave), 8 in the fused
-// step's finish kernel (256-thread CTAs shared with the argmax).  Each warp
-// folds its partials in rounds of kRound<W> rows, all loads of a round in
-// flight together.
-template <int W>
-constexpr int kRound = W >= 8 ? 5 : 10;
+// Four warps per output row, in the merge launch (one 128-thread CTA per row,
+// up to four CTAs per SM, so a 528-row call fits in one wave) and in the fused
+// step's finish kernel (two rows per 256-thread CTA), so both give the same
+// bits.  Each warp folds its partials in rounds of kRound rows, all loads of a
+// round in flight together.
+constexpr int kRound = 5;
 constexpr int kMaxTreeBatch = 4;  // ancestors whose K/V a warp loads before using any
 
 template <typename T, int D>
@@ -60,18 +59,26 @@ __device__ inline void load_partial(const float* op, float (&v)[DPL]) {
 }
 
 
-// One output row (b, node i, head h) by the whole CTA (W warps).  anc: the
-// node's ancestor-or-self mask.  s_o: W x D floats and s_red: W floats of
-// shared memory.  Runs the tree block, then pdl_wait(), then the log-sum-exp
-// merge of the prefix partials.
-template <typename T, int D, int W>
+__device__ __forceinline__ void group_sync(int bar_id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(threads) : "memory");
+}
+
+// One output row (b, node i, head h) by a group of W warps starting at warp
+// wbase of the CTA, which synchronise on named barrier bar_id (so several
+// groups of a CTA can each merge a row).  anc: the node's ancestor-or-self
+// mask.  s_o: W x D floats and s_red: W floats of shared memory (the
+// group's own).  Runs the tree block, then pdl_wait(), then the log-sum-exp
+// merge of the prefix partials.  The arithmetic depends only on W.
+template <typename T, int D, int W, int kBar = 1>
 __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, uint64_t anc, float (*s_o)[D],
-                                          float* s_red) {
+                                          float* s_red, int wbase = 0) {
+    constexpr int bar_id = kBar;
     constexpr int DPL = D / 32;
-    constexpr int kR = kRound<W>;
+    constexpr int kR = kRound;
     const lucetree_attn_args& a = L.a;
     const PlanDims& p = L.plan;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gt = threadIdx.x - 32 * wbase;  // thread index within the group
+    const int warp = gt >> 5, lane = threadIdx.x & 31;
     const int h = (int)(row % p.Hq);
     const int i = (int)((row / p.Hq) % p.N);
     const int b = (int)(row / ((long long)p.Hq * p.N));
@@ -92,7 +99,7 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
         float qf[DPL];
         load_slice<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)row * D + lane * DPL, qf);
         if (p.N < 64) anc &= (1ull << p.N) - 1ull;
-        if (!((anc >> i) & 1ull) && threadIdx.x == 0) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
+        if (!((anc >> i) & 1ull) && gt == 0) atomicOr(a.status, LUCETREE_DEV_BAD_NODE);
         // this warp's keys: every W-th set bit of anc, starting at rank `warp`
         uint64_t mine = 0;
         {
@@ -156,7 +163,7 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
     // once any block of this kernel runs, those inputs are final.  This holds
     // only while the prefix kernel keeps pdl_trigger() after pdl_wait().
     pdl_wait();
-    const int Lb = seq_len(a.ctx_len, b, p.max_pages, (i == 0 && h == 0 && threadIdx.x == 0) ? a.status : nullptr);
+    const int Lb = seq_len(a.ctx_len, b, p.max_pages, (i == 0 && h == 0 && gt == 0) ? a.status : nullptr);
     int count = 0, c_lo = 0;
     long long nT = 0;
     if (Lb > 0) {
@@ -179,7 +186,7 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
     // (max, sum, output slice), which starts from its share of the tree block.
     // All of a round's loads (up to kR partials per warp: maxima, sums and
     // the row slices) are issued before any is used, so a round costs one trip
-    // to L2; the headline shapes need one round.
+    // to L2.
     float m_w = m_t, l_w = l_t;
     for (int k0 = warp; k0 < count; k0 += W * kR) {
         float mk[kR], lk[kR];
@@ -220,7 +227,7 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
 
     // ---- the warps' parts on the common shift
     if (lane == 0) s_red[warp] = m_w;
-    __syncthreads();
+    group_sync(bar_id, 32 * W);
     float mmax = -INFINITY;
 #pragma unroll
     for (int w = 0; w < W; ++w) mmax = fmaxf(mmax, s_red[w]);
@@ -228,9 +235,9 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
 #pragma unroll
     for (int x = 0; x < DPL; ++x) s_o[warp][lane * DPL + x] = o[x] * aw;
     const float lsum = l_w * aw;  // the same in every lane of the warp
-    __syncthreads();              // every warp has read the maxima in s_red
+    group_sync(bar_id, 32 * W);   // every warp has read the maxima in s_red
     if (lane == 0) s_red[warp] = lsum;
-    __syncthreads();
+    group_sync(bar_id, 32 * W);
 
     // ---- combine the warps' sums and write the row
     float l = 0.f;
@@ -238,7 +245,7 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
     for (int w = 0; w < W; ++w) l += s_red[w];
     const float inv = 1.f / l;
     float* orow = a.out + (size_t)row * D;
-    for (int d = threadIdx.x; d < D; d += 32 * W) {
+    for (int d = gt; d < D; d += 32 * W) {
         float v = 0.f;
 #pragma unroll
         for (int w = 0; w < W; ++w) v += s_o[w][d];
@@ -246,7 +253,7 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
         orow[d] = v;
         if (!isfinite(v)) atomicOr(a.status, LUCETREE_DEV_NONFINITE);
     }
-    if (a.lse && threadIdx.x == 0) a.lse[row] = (mmax + log2f(l)) * kLn2;
+    if (a.lse && gt == 0) a.lse[row] = (mmax + log2f(l)) * kLn2;
 }
 
 }  // namespace merge

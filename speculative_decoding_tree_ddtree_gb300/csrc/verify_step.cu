@@ -44,15 +44,16 @@ struct StepLaunch {
 };
 
 constexpr int kThreads = 256;
-constexpr int kMergeWarps = kThreads / 32;  // a merge CTA's warps all work on its row
+constexpr int kMergeWarps = 4;                         // warps per output row, as in the merge launch
+constexpr int kRowsPerCta = kThreads / 32 / kMergeWarps;  // a merge CTA merges two rows side by side
 static_assert(kThreads == am::kThreads, "one CTA size for every part");
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) finish_kernel(const StepLaunch S) {
-    __shared__ float s_o[kMergeWarps][D];
-    __shared__ float s_red[kMergeWarps];
+    __shared__ float s_o[kRowsPerCta][kMergeWarps][D];
+    __shared__ float s_red[kRowsPerCta][kMergeWarps];
     __shared__ unsigned long long s_key[kThreads / 32];
-    __shared__ int32_t s_par[LUCETREE_MAX_NODES];
+    __shared__ int32_t s_par[kRowsPerCta][LUCETREE_MAX_NODES];
     __shared__ int s_flag, s_good;
     if (threadIdx.x == 0) pdl_trigger();
 
@@ -87,22 +88,30 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StepLaunch S) {
         tree::commit_block(S.commit, b, (int)sizeof(T), &s_good);
         return;
     }
-    // -------------------------------------------------------------------- merge row
-    const long long row = (long long)blockIdx.x - n_am;
+    // -------------------------------------------------------------------- merge rows
+    // warp group grp (kMergeWarps warps, named barrier 1 + grp) merges one row
+    const int grp = (threadIdx.x >> 5) / kMergeWarps;
+    const int gt = threadIdx.x - 32 * kMergeWarps * grp;
+    const long long row = ((long long)blockIdx.x - n_am) * kRowsPerCta + grp;
+    if (row >= (long long)p.B * N * p.Hq) return;  // (the group's barriers involve only its own warps)
     const int i = (int)((row / p.Hq) % N);
     const int b = (int)(row / ((long long)p.Hq * N));
-    if (threadIdx.x < N) s_par[threadIdx.x] = __ldcg(S.parent + (size_t)b * N + threadIdx.x);
-    __syncthreads();
+    if (gt < N) s_par[grp][gt] = __ldcg(S.parent + (size_t)b * N + gt);
+    static_assert(kRowsPerCta == 2, "two warp groups: named barriers 1 and 2");
+    if (grp == 0) merge::group_sync(1, 32 * kMergeWarps);
+    else merge::group_sync(2, 32 * kMergeWarps);
     bool bad = false;
-    const uint64_t anc = tree::anc_walk(s_par, i, &bad);
-    if (bad && threadIdx.x == 0 && (row % p.Hq) == 0) atomicOr(S.attn.a.status, LUCETREE_DEV_BAD_PARENT);
-    merge::merge_row<T, D, kMergeWarps>(S.attn, row, anc, s_o, s_red);
+    const uint64_t anc = tree::anc_walk(s_par[grp], i, &bad);
+    if (bad && gt == 0 && (row % p.Hq) == 0) atomicOr(S.attn.a.status, LUCETREE_DEV_BAD_PARENT);
+    if (grp == 0) merge::merge_row<T, D, kMergeWarps, 1>(S.attn, row, anc, s_o[0], s_red[0], 0);
+    else merge::merge_row<T, D, kMergeWarps, 2>(S.attn, row, anc, s_o[1], s_red[1], kMergeWarps);
 }
 
 template <typename T, int D>
 cudaError_t launch_finish(const StepLaunch& S, cudaStream_t stream) {
+    const long long rows = (long long)S.attn.plan.B * S.attn.plan.N * S.attn.plan.Hq;
     const long long blocks = (long long)S.attn.plan.B * (S.attn.plan.N + 1) * S.chunks +
-                             (long long)S.attn.plan.B * S.attn.plan.N * S.attn.plan.Hq;
+                             (rows + kRowsPerCta - 1) / kRowsPerCta;
     return launch_pdl(finish_kernel<T, D>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, S);
 }
 
