@@ -155,14 +155,14 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
     // (this kernel is launched as a programmatic dependent of the prefix
     // kernel: everything above overlaps its tail, nothing below may)
     //
-    // The reads above (q, anc_mask, tree K/V) and the status OR come before
-    // this kernel's own wait.  They are safe by transitivity: the prefix
-    // kernel triggers its dependents only after its own pdl_wait() has
+    // The reads above (q, anc_mask, tree K/V), those of ctx_len just below
+    // (which CTAs' partials cover this segment) and the status ORs come
+    // before this kernel's own wait.  They are safe by transitivity: the
+    // prefix kernel triggers its dependents only after its own pdl_wait() has
     // returned, i.e. after every kernel before it on the stream (the one that
     // wrote the masks, the caller's uploads) has completed and flushed.  So
     // once any block of this kernel runs, those inputs are final.  This holds
     // only while the prefix kernel keeps pdl_trigger() after pdl_wait().
-    pdl_wait();
     const int Lb = seq_len(a.ctx_len, b, p.max_pages, (i == 0 && h == 0 && gt == 0) ? a.status : nullptr);
     int count = 0, c_lo = 0;
     long long nT = 0;
@@ -173,6 +173,7 @@ __device__ __forceinline__ void merge_row(const AttnLaunch& L, long long row, ui
         c_lo = cta_of_tile(first, nT, p.Cg);
         count = cta_of_tile(last, nT, p.Cg) - c_lo + 1;
     }
+    pdl_wait();
     const size_t sf = slot_floats(p);
     const float* ws = L.ws + slot_index(p, rg, c_lo, s) * sf;
     // with fewer tiles than CTAs some CTAs own no tile and write no partial
