@@ -994,15 +994,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             // ---------------------------------------------------------- epilogue
-            // (also the consensus point for a timeout in the piece's last tile)
-            const bool got = !bad && mbar_wait(&ms->pv_done, (j - 1) & 1);
-            if (bar_sync_or(1, kSoftmaxThreads, bad || !got || aborted(ms))) {
-                bad = true;
-                break;
-            }
-            tc_fence_after();
-            // row sums: the warp's 32 key lanes by a butterfly reduce-scatter,
-            // then the four lane quarters through shared memory
+            // Row sums and shifts first: they are final once the last tile's
+            // exponent pass is done, so they are written while the last PV
+            // (which waits for the last V tile to land) is still running.
+            // Row sums: the warp's 32 key lanes by a butterfly reduce-scatter,
+            // then the four lane quarters through shared memory.
 #pragma unroll
             for (int cc = 0; cc < kNa; ++cc) {
                 if (cc >= nch) continue;
@@ -1020,6 +1016,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 slot_l[col] = (ms->col_red[0][col] + ms->col_red[1][col]) + (ms->col_red[2][col] + ms->col_red[3][col]);
                 slot_m[col] = ms->m_ref[col];
             }
+            // the consensus point for a timeout in the piece's last tile (a
+            // piece that failed has written garbage sums; the call reports the
+            // failure through the status word)
+            const bool got = !bad && mbar_wait(&ms->pv_done, (j - 1) & 1);
+            if (bar_sync_or(1, kSoftmaxThreads, bad || !got || aborted(ms))) {
+                bad = true;
+                break;
+            }
+            tc_fence_after();
 #pragma unroll
             for (int cc = 0; cc < kNa; ++cc) {
                 if (cc >= nch) continue;
@@ -1027,8 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < Lay::kDh; ++h) {
                     uint32_t r[16];
-                    const uint32_t addr = tl + (h ? Lay::kColO1 : Lay::kColO0) + 16 * c;
-                    tmem_ld16(addr, r);
+                    tmem_ld16(tl + (h ? Lay::kColO1 : Lay::kColO0) + 16 * c, r);
                     tmem_wait_ld_regs16(r);
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
