@@ -547,50 +547,75 @@ def run_ours(args, cfg):
 
     for k, v in views(host_pack).items():
         v.copy_(src[k])
-    dev_packs = [torch.empty(pos, dtype=torch.uint8, device=dev) for _ in range(2)]
+    n_buf = 3
+    dev_packs = [torch.empty(pos, dtype=torch.uint8, device=dev) for _ in range(n_buf)]
     res = dict(results=torch.empty_like(step.results, device="cpu").pin_memory())
     h2d = sum(src[k].numel() * src[k].element_size() for k in up_keys)
     d2h = sum(t.numel() * t.element_size() for t in res.values())
     e2e_steps = min(args.steps, 500)
     # Every step copies its own inputs from pinned host memory and the host
-    # reads every step's result back.  The inputs go into two alternating
-    # device buffers, copied on a second stream, so step i+1's upload overlaps
-    # step i's kernels; the host enqueues step i before it waits for step
-    # i-1's result (two result buffers), so launching overlaps too.
+    # reads every step's result back.  The inputs go into three rotating
+    # device buffers, copied on a second stream two steps ahead, so a step's
+    # upload overlaps the two steps before it.  Two VerifyStep objects take
+    # turns, so step i's result is read back on a third stream while step i+1
+    # runs (a copy on the compute stream would sit between two steps and keep
+    # the next step's programmatic launch from overlapping this one's tail);
+    # the host enqueues step i before it waits for step i-1's result.
     copy_stream = torch.cuda.Stream(device=dev)
+    rb_stream = torch.cuda.Stream(device=dev)
+    steps2 = [step, LT.VerifyStep(cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, device=dev)]
+    stream.wait_stream(torch.cuda.current_stream(dev))  # the second step's zeroed counters
     bufs = []
     for pk in dev_packs:
         b = dict(d)
         b.update(views(pk))
         bufs.append(b)
-    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
-    ev_used = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_in = [torch.cuda.Event() for _ in range(n_buf)]
+    ev_used = [torch.cuda.Event() for _ in range(n_buf)]
     ev_res = [torch.cuda.Event(), torch.cuda.Event()]
+    for e in ev_res:
+        e.record(rb_stream)
+    # every tenth upload is timed (its own event pair, read after the loop)
+    ev_copy = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(-(-e2e_steps // 10))]
     results = [res, {k: torch.empty_like(t).pin_memory() for k, t in res.items()}]
 
     def upload(i):
+        b = i % n_buf
         with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(ev_used[i % 2])  # the step that last read this buffer has finished
-            dev_packs[i % 2].copy_(host_pack, non_blocking=True)
-            ev_in[i % 2].record(copy_stream)
+            copy_stream.wait_event(ev_used[b])  # the step that last read this buffer has finished
+            if i % 10 == 0:
+                ev_copy[i // 10][0].record(copy_stream)
+            dev_packs[b].copy_(host_pack, non_blocking=True)
+            if i % 10 == 0:
+                ev_copy[i // 10][1].record(copy_stream)
+            ev_in[b].record(copy_stream)
 
     barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     upload(0)
+    if e2e_steps > 1:
+        upload(1)
     for i in range(e2e_steps):
-        if i + 1 < e2e_steps:
-            upload(i + 1)
+        if i + 2 < e2e_steps:
+            upload(i + 2)
+        st = steps2[i % 2]
         with torch.cuda.stream(stream):
-            stream.wait_event(ev_in[i % 2])
-            one(dd=bufs[i % 2])
-            ev_used[i % 2].record(stream)
-            results[i % 2]["results"].copy_(step.results, non_blocking=True)
-            ev_res[i % 2].record(stream)
+            stream.wait_event(ev_in[i % n_buf])
+            stream.wait_event(ev_res[i % 2])  # step i-2's result (same object) has been read back
+            issue_step(st, bufs[i % n_buf], stream)
+            ev_used[i % n_buf].record(stream)
+        with torch.cuda.stream(rb_stream):
+            rb_stream.wait_event(ev_used[i % n_buf])
+            results[i % 2]["results"].copy_(st.results, non_blocking=True)
+            ev_res[i % 2].record(rb_stream)
         if i >= 1:
             ev_res[(i - 1) % 2].synchronize()  # the host has step i-1's result
     ev_res[(e2e_steps - 1) % 2].synchronize()  # and the last step's
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev) / e2e_steps
+    torch.cuda.synchronize(dev)
+    copy_ms = [a.elapsed_time(b) for a, b in ev_copy]
     barrier()
 
     sb = step_bytes(cfg, acc_total)
@@ -611,8 +636,10 @@ def run_ours(args, cfg):
         "clocks": clocks,
         "e2e": {"value": world * sb / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
-                "pipeline": "step i+1's inputs (one packed pinned buffer, one copy) upload on a second stream "
-                            "while step i runs; every step's result (one copy) is read by the host one step later"},
+                "h2d_ms_per_copy_p50": float(np.median(copy_ms)) if copy_ms else None,
+                "pipeline": "each step's inputs (one packed pinned buffer, one copy) upload on a second stream two "
+                            "steps ahead into one of three device buffers; two VerifyStep objects take turns and "
+                            "each step's result (one copy, on a third stream) is read by the host one step later"},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "roofline": {"bound": "hbm", "kernel": "lucetree_verify_attn (split-K prefix + tree/merge launch)",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
@@ -634,8 +661,10 @@ def run_ours(args, cfg):
         line["quantised_v"] = measure_vq(args, dev, stream, rank, d, step, cfg)
         line["quantised_k"] = measure_kq(args, dev, stream, rank, d, step, cfg)
     if not args.no_configs:
-        for held in (d, host, bufs[1]):
+        for held in (d, bufs[0], bufs[1]):
             held.clear()  # the other workloads need the device memory
+        dev_packs.clear()
+        del steps2[1:]
         torch.cuda.empty_cache()
         line["configs"] = measure_configs(args, dev, stream, rank)
     print(json.dumps(line), flush=True)
