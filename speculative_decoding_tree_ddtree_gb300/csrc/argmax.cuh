@@ -111,8 +111,8 @@ __device__ inline bool argmax_chunk(const float* __restrict__ logits, int vocab,
 
 // Chunks per row: about four CTAs per SM over all rows, and no chunk smaller
 // than one round of loads.
-inline int argmax_chunks(int rows, int vocab, int sms) {
-    int chunks = (4 * sms + rows - 1) / rows;
+inline int argmax_chunks(int rows, int vocab, int sms, int ctas_per_sm = 4) {
+    int chunks = (ctas_per_sm * sms + rows - 1) / rows;
     const int max_by_size = (vocab + 4 * kThreads - 1) / (4 * kThreads);
     if (chunks > max_by_size) chunks = max_by_size;
     if (chunks < 1) chunks = 1;

@@ -44,6 +44,10 @@ struct StepLaunch {
 };
 
 constexpr int kThreads = 256;
+// Argmax CTAs per SM's worth of logits.  They are blocks of this kernel, so
+// they take a merge block's registers (two blocks per SM): the fewer they
+// are, the sooner the merge blocks are resident.
+constexpr int kArgmaxCtasPerSm = 2;
 constexpr int kMergeWarps = 4;                         // warps per output row, as in the merge launch
 constexpr int kRowsPerCta = kThreads / 32 / kMergeWarps;  // a merge CTA merges two rows side by side
 static_assert(kThreads == am::kThreads, "one CTA size for every part");
@@ -123,7 +127,7 @@ struct StepWs {
 
 StepWs step_ws(const PlanDims& p, int vocab, int sms) {
     const int rows = p.B * (p.N + 1);
-    const int chunks = am::argmax_chunks(rows, vocab, sms);
+    const int chunks = am::argmax_chunks(rows, vocab, sms, kArgmaxCtasPerSm);
     StepWs w;
     w.attn = (attn_workspace_bytes(p) + 255) / 256 * 256;
     w.row_t = w.attn;
@@ -178,7 +182,7 @@ extern "C" lucetree_status lucetree_verify_step(const lucetree_step_args* s, voi
     S.draft = s->draft;
     S.logits = s->logits;
     S.vocab = s->vocab;
-    S.chunks = am::argmax_chunks(a.B * (a.N + 1), s->vocab, device_sm_count(dev));
+    S.chunks = am::argmax_chunks(a.B * (a.N + 1), s->vocab, device_sm_count(dev), kArgmaxCtasPerSm);
     S.argmax = s->argmax;
     S.acc_nodes = s->acc_nodes;
     S.acc_len = s->acc_len;
