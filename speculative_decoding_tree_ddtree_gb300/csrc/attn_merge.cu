@@ -6,11 +6,15 @@ namespace lucetree {
 
 namespace {
 
-constexpr int kWarps = 4;  // per CTA = per output row; up to four CTAs per SM
+// Four warps per CTA = per output row, five CTAs per SM (at most 102
+// registers a thread): a 528-row call then fits on the first 106 SMs that the
+// prefix kernel frees, so its last blocks start early enough for their tree
+// block to finish before the prefix kernel does.
+constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 4) merge_kernel(AttnLaunch L) {
+__global__ void __launch_bounds__(kThreads, 5) merge_kernel(AttnLaunch L) {
     __shared__ float s_o[kWarps][D];
     __shared__ float s_red[kWarps];
     if (threadIdx.x == 0) pdl_trigger();

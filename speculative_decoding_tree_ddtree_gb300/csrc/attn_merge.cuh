@@ -35,12 +35,12 @@ __device__ inline float warp_max(float v) {
 }
 
 // Four warps per output row, in the merge launch (one 128-thread CTA per row,
-// up to four CTAs per SM, so a 528-row call fits in one wave) and in the fused
+// up to five CTAs per SM, so a 528-row call fits in one wave) and in the fused
 // step's finish kernel (two rows per 256-thread CTA), so both give the same
 // bits.  Each warp folds its partials in rounds of kRound rows, all loads of a
 // round in flight together.
 constexpr int kRound = 5;
-constexpr int kMaxTreeBatch = 4;  // ancestors whose K/V a warp loads before using any
+constexpr int kMaxTreeBatch = 2;  // ancestors whose K/V a warp loads before using any (registers)
 
 template <typename T, int D>
 __device__ inline void load_slice(const T* p, float (&out)[D / 32]) {
