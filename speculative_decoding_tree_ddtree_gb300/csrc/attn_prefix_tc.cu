@@ -48,23 +48,12 @@ cudaError_t launch_attn_prefix(const AttnLaunch& L, cudaStream_t stream) {
     const cuuint64_t q_dims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.N};
     const cuuint64_t q_strides[2] = {(cuuint64_t)a.D * 2, (cuuint64_t)a.Hq * a.D * 2};
     const cuuint32_t q_box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)p.rg.NPG};
-    if (!kq && enc(&tq, dt, 3, const_cast<void*>(a.q), q_dims, q_strides, q_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    // (E4M3 K too: the kernel splits the bf16 queries into their two E4M3 parts on chip)
+    if (enc(&tq, dt, 3, const_cast<void*>(a.q), q_dims, q_strides, q_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     tq2 = tv;
-    if (kq) {
-        // the two E4M3 parts of the scaled queries, bytes with the layout of q; box = 128 dims x G x NPG
-        const cuuint64_t qb_strides[2] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq * a.D};
-        const cuuint32_t qb_box[3] = {128, (cuuint32_t)p.G, (cuuint32_t)p.rg.NPG};
-        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(L.q_hi), q_dims, qb_strides, qb_box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-            enc(&tq2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(L.q_lo), q_dims, qb_strides, qb_box,
-                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
 
     // quantised V: codes as bytes [rows][D or D/2] (one 64-token page x 128 dims per box, no
     // swizzle: the softmax warps expand them), exponents [num_pages * Hkv][64] one page per box

@@ -55,6 +55,7 @@
 // copies and MMAs and returns.
 #pragma once
 
+#include "e4m3.cuh"
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -123,6 +124,7 @@ struct Misc {
     uint64_t vfull[kMaxSlots];
     uint64_t vready[kMaxSlots];
     uint64_t s_full, s_free, q_full, q_empty, p_full, pv_done, drain;
+    uint64_t q_ready;  // E4M3 K: the piece's queries split into their two E4M3 parts
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -308,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ms->p_full, kSmWarps);
         mbar_init(&ms->pv_done, 1);
         mbar_init(&ms->drain, 1);
+        mbar_init(&ms->q_ready, kSmWarps);
         ms->abort_flag = 0;
         mbar_fence_init();
     }
@@ -423,6 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rel = cur.t - cur.pc.ta;
             if (rel == 0) {
                 // a new key segment: its queries replace the previous ones once their last QK is done
+                if (KQ && cur.piece_no > 0 && have_v) {
+                    // E4M3 K: the previous piece's last V goes first, because the next
+                    // piece's first QK waits for the softmax warps to split its queries,
+                    // which they do only after that V's PV (the MMA warp keeps this order)
+                    if (!(ok = issue(true, v_row0, v_row1))) break;
+                    have_v = false;
+                }
                 if (cur.piece_no > 0) {
                     const bool w = mbar_wait(&ms->q_empty, (cur.piece_no - 1) & 1);
                     if (!(ok = __all_sync(0xffffffffu, w))) break;
@@ -430,17 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&ms->q_full, kChunks * RG * 128);
                     const int b = cur.pc.s / p.Hkv, g = cur.pc.s % p.Hkv;
-                    if constexpr (KQ) {
-                        // high parts, then low parts: [RGP rows][128 dims] bytes per chunk
-                        for (int c = 0; c < D / 128; ++c) {
-                            tma_load_3d(sQ + c * RGP * 128, &tm_q, 128 * c, g * p.G, b * p.N + i0, &ms->q_full);
-                            tma_load_3d(sQ + (D / 128 + c) * RGP * 128, &tm_q2, 128 * c, g * p.G, b * p.N + i0,
-                                        &ms->q_full);
-                        }
-                    } else {
-                        for (int c = 0; c < kChunks; ++c)
-                            tma_load_3d(sQ + c * RGP * 128, &tm_q, 64 * c, g * p.G, b * p.N + i0, &ms->q_full);
-                    }
+                    // (E4M3 K: the bf16 queries too; the softmax warps split them in place)
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(sQ + c * RGP * 128, &tm_q, 64 * c, g * p.G, b * p.N + i0, &ms->q_full);
                 }
                 __syncwarp();
                 ++q_loads;
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                 }
                 if (qk.first()) {
-                    if (!mbar_wait(&ms->q_full, qk.piece_no & 1)) return false;
+                    if (!mbar_wait(KQ ? &ms->q_ready : &ms->q_full, qk.piece_no & 1)) return false;
                     tc_fence_after();
                 }
                 for (int c = 0; c < kChunksK; ++c) {
@@ -513,9 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int sub = 0; sub < 4; ++sub) {
                         const uint64_t ad = make_desc(hi_k, aS + slot * kChunkBytes + sub * 32);
                         if constexpr (KQ) {
-                            // 32 dims per step: K codes times the high, then the low query part
-                            const uint64_t bh = make_desc(hi_k, aQ + c * RGP * 128 + sub * 32);
-                            const uint64_t bl = make_desc(hi_k, aQ + (kChunksK + c) * RGP * 128 + sub * 32);
+                            // 32 dims per step (dims 128 c + 32 sub): K codes times the high,
+                            // then the low query part; the split queries keep each 32-dim
+                            // span's hi codes in the first 32 bytes of the span's 64 and lo
+                            // in the next 32, the spans at the bf16 layout's places
+                            const uint32_t qspan = aQ + (2 * c + (sub >> 1)) * RGP * 128 + (sub & 1) * 64;
+                            const uint64_t bh = make_desc(hi_k, qspan);
+                            const uint64_t bl = make_desc(hi_k, qspan + 32);
                             mma_f8f6f4_ss(tmem, ad, bh, id_qk, (c | sub) != 0);
                             mma_f8f6f4_ss(tmem, ad, bl, id_qk, 1u);
                         } else {
@@ -538,35 +544,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (qk.live && !(ok = issue_qk())) break;  // QK(j+1)
-                // O^T += V^T . P^T once the softmax has written P^T(j)
-                if (!(ok = mbar_wait(&ms->p_full, j & 1))) break;
-                tc_fence_after();
-                const bool first = pv.first();
-                // output dims 128h..128h+127: chunk 2h holds keys 0..63, chunk
-                // 2h+1 keys 64..127 (four 16-key steps each)
-                for (int h = 0; h < kChunksV / 2 && ok; ++h) {
-                    const uint32_t dO = tmem + (h ? Lay::kColO1 : Lay::kColO0);
-                    for (int kh = 0; kh < 2 && ok; ++kh) {
-                        const int slot = chunk % kNS;
-                        // landed and converted by the softmax warps
-                        const uint32_t vn = j * kChunksV + 2 * h + kh;
-                        if (!(ok = mbar_wait(&ms->vready[vn % kMaxSlots], (vn / kMaxSlots) & 1))) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t ad = make_desc(hi_v, aS + slot * kChunkBytes + ks * 2048);
-                            const uint64_t bd = make_desc(hi_p, aP + (4 * kh + ks) * 256);
-                            mma_f16_ss(dO, ad, bd, id_pv, !(first && kh == 0 && ks == 0));
-                        }
-                        mma_commit(&ms->empty[slot]);
-                        ++chunk;
+                // QK(j+1), then PV(j); with E4M3 K, QK(j+1) after PV(j) when it opens a
+                // new piece (its queries are split by the softmax warps once they are
+                // done with tile j).  One loop over the two steps keeps a single copy
+                // of each in this 56-register warp.
+                const bool defer_qk = KQ && qk.live && qk.first() && qk.piece_no > 0;
+#pragma unroll 1
+                for (int step = 0; step < 2 && ok; ++step) {
+                    if ((step == 0) != defer_qk) {
+                        if (qk.live) ok = issue_qk();
+                        continue;
                     }
+                    // O^T += V^T . P^T once the softmax has written P^T(j)
+                    if (!(ok = mbar_wait(&ms->p_full, j & 1))) break;
+                    tc_fence_after();
+                    const bool first = pv.first();
+                    // output dims 128h..128h+127: chunk 2h holds keys 0..63, chunk
+                    // 2h+1 keys 64..127 (four 16-key steps each)
+                    for (int h = 0; h < kChunksV / 2 && ok; ++h) {
+                        const uint32_t dO = tmem + (h ? Lay::kColO1 : Lay::kColO0);
+                        for (int kh = 0; kh < 2 && ok; ++kh) {
+                            const int slot = chunk % kNS;
+                            // landed and converted by the softmax warps
+                            const uint32_t vn = j * kChunksV + 2 * h + kh;
+                            if (!(ok = mbar_wait(&ms->vready[vn % kMaxSlots], (vn / kMaxSlots) & 1))) break;
+                            tc_fence_after();
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks) {
+                                const uint64_t ad = make_desc(hi_v, aS + slot * kChunkBytes + ks * 2048);
+                                const uint64_t bd = make_desc(hi_p, aP + (4 * kh + ks) * 256);
+                                mma_f16_ss(dO, ad, bd, id_pv, !(first && kh == 0 && ks == 0));
+                            }
+                            mma_commit(&ms->empty[slot]);
+                            ++chunk;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&ms->pv_done);
+                    ++j;
+                    pv.step(p, a.ctx_len);
                 }
-                if (!ok) break;
-                mma_commit(&ms->pv_done);
-                ++j;
-                pv.step(p, a.ctx_len);
             }
             if (!ok || aborted(ms)) {
                 set_abort(ms, a.status);
@@ -595,7 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nvalid = min(kTileKeys, cur.pc.L - cur.t * kTileKeys);
             // ring position of V(j)'s first chunk: the K operands before it
             // (K(0) .. K(j+1), or .. K(j) for the last tile) and V(0) .. V(j-1)
-            const uint32_t vbase = (j + 1 < n_tiles ? j + 2 : j + 1) * kChunksK + j * kChunksV;
+            // (E4M3 K: the next piece's first K comes after this V)
+            const bool k_after = j + 1 < n_tiles && !(KQ && cur.t == cur.pc.te - 1);
+            const uint32_t vbase = (k_after ? j + 2 : j + 1) * kChunksK + j * kChunksV;
             for (int c = 0; c < kChunksV; ++c) {
                 const uint32_t vn = j * kChunksV + c;
                 const bool landed = mbar_wait(&ms->vfull[vn % kMaxSlots], (vn / kMaxSlots) & 1);
@@ -748,7 +767,85 @@ __global__ void __launch_bounds__(kThreads, 1)
             float qs = 0.f;
             if constexpr (KQ) {
                 ek_next = k_exp_of(page_of(cur.pc.ta));
-                qs = L.q_scale[seg];
+                // The piece's bf16 queries (four 64-dim chunks of [RGP rows][128 B],
+                // 128-byte swizzled) become two E4M3 parts in place, scaled by 2^p so
+                // that their largest magnitude lies in (224, 448]: hi = e4m3(q 2^p),
+                // lo = e4m3(q 2^p - hi).  The 64 bytes of each 32-dim span of a row
+                // (four 16-byte units) are rewritten as hi's 32 codes in the first
+                // two units and lo's in the last two, so every thread rewrites only
+                // what it read, and a 32-dim K step of the FP8 MMA finds its hi (and,
+                // 32 bytes on, its lo) operand rows contiguous.  One pass for the
+                // CTA's largest |q| (one barrier, which also carries a timed-out
+                // wait), one to convert.
+                constexpr int kSpans = RGP * 8;
+                constexpr int kPer = (kSpans + kSoftmaxThreads - 1) / kSoftmaxThreads;
+                const bool qw = !bad && wait_all(&ms->q_full, piece_no & 1);
+                auto span_unit = [&](int sid, int k) -> uint4* {
+                    const int r = sid >> 3, v = sid & 7;
+                    return reinterpret_cast<uint4*>(sQ + (v >> 1) * RGP * 128 + r * 128 +
+                                                    (((4 * (v & 1) + k) ^ (r & 7)) << 4));
+                };
+                float qm = 0.f;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int sid = st + kSoftmaxThreads * i;
+                    if (sid >= kSpans || !qw) continue;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float v[8];
+                        const uint4 w4 = *span_unit(sid, k);
+                        load8_f32<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16*>(&w4), v);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) qm = fmaxf(qm, fabsf(v[e]));
+                    }
+                }
+                qm = warp_max(qm);
+                if (lane == 0) ms->col_red[0][warp - 4] = qm;
+                if (bar_sync_or(1, kSoftmaxThreads, !qw)) bad = true;
+                if (!bad) {
+                    qm = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kSmWarps; ++w) qm = fmaxf(qm, ms->col_red[0][w]);
+                    const int pe = e4m3::scale_exponent(qm);
+                    qs = ldexpf(L.scale_log2, -pe);
+                    const float s2p = ldexpf(1.f, pe);  // 2^p: scaling by it is exact here
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i) {
+                        const int sid = st + kSoftmaxThreads * i;
+                        if (sid >= kSpans) continue;
+                        uint4 w4[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) w4[k] = *span_unit(sid, k);
+                        uint32_t hw[8], lw[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            float v[8];
+                            load8_f32<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16*>(&w4[k]), v);
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2) {
+                                const float y0 = v[e] * s2p, y1 = v[e + 1] * s2p;  // exact: |y| <= 448
+                                const uint16_t hc = e4m3::e4m3x2(y0, y1);
+                                const float2 hf = e4m3::e4m3x2_to_f32(hc);
+                                const uint16_t lc = e4m3::e4m3x2(y0 - hf.x, y1 - hf.y);  // exact differences
+                                const int wi = 2 * k + (e >> 2);  // dims 8k + e, 8k + e + 1
+                                if ((e & 2) == 0) {
+                                    hw[wi] = hc;
+                                    lw[wi] = lc;
+                                } else {
+                                    hw[wi] |= (uint32_t)hc << 16;
+                                    lw[wi] |= (uint32_t)lc << 16;
+                                }
+                            }
+                        }
+                        *span_unit(sid, 0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *span_unit(sid, 1) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                        *span_unit(sid, 2) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        *span_unit(sid, 3) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ms->q_ready);
+                }
             }
 
             while (cur.live && cur.piece_no == piece_no) {
@@ -894,7 +991,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!bad && VQ != 0) {
                     // ring position of V(j)'s first chunk: the K operands before it
                     // (K(0) .. K(j+1), or .. K(j) for the last tile) and V(0) .. V(j-1)
-                    const uint32_t vbase = (j + 1 < n_tiles ? j + 2 : j + 1) * kChunksK + j * kChunksV;
+                    const bool k_after = j + 1 < n_tiles && !(KQ && t == cur.pc.te - 1);
+                    const uint32_t vbase = (k_after ? j + 2 : j + 1) * kChunksK + j * kChunksV;
                     for (int c = 0; c < kChunksV; ++c) {
                         const uint32_t vn = j * kChunksV + c;
                         const bool landed = wait_all(&ms->vfull[vn % kMaxSlots], (vn / kMaxSlots) & 1);

@@ -186,9 +186,6 @@ struct AttnLaunch {
     const uint8_t* v_exp;  // per-token exponents of quantised V [num_pages][Hkv][64]
     int k_format;          // LUCETREE_K_SAME, or LUCETREE_K_E4M3 (k_pool holds E4M3 codes)
     const uint8_t* k_exp;  // per-token exponents of E4M3 K [num_pages][Hkv][64]
-    const uint8_t* q_hi;   // E4M3 K: the two parts of the scaled queries [B][N][Hq][D] (workspace)
-    const uint8_t* q_lo;
-    const float* q_scale;  // E4M3 K: per key segment, scale * log2(e) / 2^p of its query parts (workspace)
 };
 
 int prefix_grid_ctas(int device);  // persistent grid size of the prefix kernel

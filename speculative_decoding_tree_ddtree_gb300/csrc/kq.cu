@@ -9,117 +9,26 @@
 // e = 127 - p and rounds each k * 2^p to the nearest E4M3 value, ties to the
 // even code.
 //
-// QK runs on the FP8 tensor cores.  The queries of one key segment (sequence,
-// KV head) are scaled by one power of two 2^p so that their largest magnitude
-// lies in (224, 448], then split into two E4M3 parts, hi = e4m3(q 2^p) and
+// QK runs on the FP8 tensor cores.  The prefix kernel loads each piece's
+// bf16 queries (one row group of one key segment) and splits them in shared
+// memory: scaled by one power of two 2^p so that their largest magnitude lies
+// in (224, 448], then two E4M3 parts, hi = e4m3(q 2^p) and
 // lo = e4m3(q 2^p - hi).  A bf16 query has 8 significant bits and hi keeps
 // the top 4, so the residual fits lo exactly wherever it stays in E4M3's
 // normal range (|q 2^p| >= 1/4); two FP8 MMAs (hi, then lo, into one fp32
 // accumulator) cost one bf16 MMA.  The softmax multiplies each key's
 // accumulated score by 2^(e - 127) and by scale * log2(e) / 2^p.
 #include "attn_prefix_tc.cuh"
+#include "e4m3.cuh"
 #include "tree_ops.cuh"
 
 namespace lucetree {
 
 namespace {
 
-constexpr int kSplitThreads = 256;
-
-// two fp32 values -> two E4M3 codes, round to nearest even, saturating to
-// +-448 (the callers keep |x| <= 448): lo -> low byte, hi -> high byte
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-// two E4M3 codes (low byte first) -> two fp32 values (exact)
-__device__ __forceinline__ float2 e4m3x2_to_f32(uint16_t c) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
-    return __half22float2(*reinterpret_cast<__half2*>(&h2));
-}
-
-// p with max * 2^p in (224, 448] (the quantised-K scale rule); 0 for max = 0
-__device__ __forceinline__ int scale_exponent(float m) {
-    if (!(m > 0.f)) return 0;
-    int ex;
-    const float mant = frexpf(m, &ex);  // m = mant * 2^ex, mant in [0.5, 1)
-    return mant <= 0.875f ? 9 - ex : 8 - ex;
-}
-
-// Grid (key segment s = (b, g), part y): every CTA finds the largest |q| over
-// the segment's rows (nodes x heads of the group; eight 16-byte loads in
-// flight per thread), then splits its own part of the rows: q 2^p into two
-// E4M3 parts written with the layout of q.  Part 0 also writes the segment's
-// score factor.
-constexpr int kSplitItems = 4;  // 8-value items per thread in the split pass
-
-__global__ void __launch_bounds__(kSplitThreads) q_split_kernel(const __nv_bfloat16* __restrict__ q, int N, int Hq,
-                                                                int G, int D, float scale_log2,
-                                                                uint8_t* __restrict__ q_hi,
-                                                                uint8_t* __restrict__ q_lo,
-                                                                float* __restrict__ q_scale) {
-    __shared__ float red[kSplitThreads / 32];
-    pdl_wait();
-    pdl_trigger();
-    const int s = blockIdx.x;
-    const int Hkv = Hq / G;
-    const int b = s / Hkv, g = s % Hkv;
-    const int per_row = D / 8;               // 8 values (16 bytes) per item
-    const int items = N * G * per_row;
-    auto row_of = [&](int it) {              // flat element offset of item it
-        const int r = it / per_row, u = it % per_row;
-        const int i = r / G, h = g * G + r % G;
-        return (((size_t)b * N + i) * Hq + h) * D + (size_t)u * 8;
-    };
-    float m = 0.f;
-    for (int it0 = threadIdx.x; it0 < items; it0 += 8 * kSplitThreads) {
-        uint4 raw[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int it = it0 + u * kSplitThreads;
-            raw[u] = it < items ? *reinterpret_cast<const uint4*>(q + row_of(it)) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            float v[8];
-            load8_f32<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16*>(&raw[u]), v);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    m = 0.f;
-#pragma unroll
-    for (int w = 0; w < kSplitThreads / 32; ++w) m = fmaxf(m, red[w]);
-    const int p = scale_exponent(m);
-    if (threadIdx.x == 0 && blockIdx.y == 0) q_scale[s] = ldexpf(scale_log2, -p);
-    const int it_base = blockIdx.y * kSplitThreads * kSplitItems + threadIdx.x;
-#pragma unroll
-    for (int u = 0; u < kSplitItems; ++u) {
-        const int it = it_base + u * kSplitThreads;
-        if (it >= items) break;
-        const size_t off = row_of(it);
-        float v[8];
-        load8_f32<__nv_bfloat16>(q + off, v);
-        uint32_t hw[2] = {0, 0}, lw[2] = {0, 0};
-#pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-            const float y0 = ldexpf(v[k], p), y1 = ldexpf(v[k + 1], p);  // exact: a power-of-two scale
-            const uint16_t h = e4m3x2(y0, y1);
-            const float2 hf = e4m3x2_to_f32(h);
-            const uint16_t l = e4m3x2(y0 - hf.x, y1 - hf.y);                 // exact differences
-            hw[k / 4] |= (uint32_t)h << (16 * ((k / 2) & 1));
-            lw[k / 4] |= (uint32_t)l << (16 * ((k / 2) & 1));
-        }
-        *reinterpret_cast<uint2*>(q_hi + off) = make_uint2(hw[0], hw[1]);
-        *reinterpret_cast<uint2*>(q_lo + off) = make_uint2(lw[0], lw[1]);
-    }
-}
+using e4m3::e4m3x2;
+using e4m3::e4m3x2_to_f32;
+using e4m3::scale_exponent;
 
 // One CTA per sequence: every accepted node's K rows (all KV heads) stored as
 // E4M3 codes and exponent at logical position L_b + k, its V rows copied as
@@ -206,23 +115,6 @@ __global__ void __launch_bounds__(256) commit_kq_kernel(lucetree_commit_args c, 
     if (threadIdx.x == 0) c.ctx_len_out[b] = L < 0 ? L : L + count;
 }
 
-// workspace after the attention partials: the two query parts (B N Hq D bytes
-// each) and the segments' score factors, each 256-byte aligned
-struct KqWs {
-    size_t attn, hi, lo, scale, total;
-};
-
-KqWs kq_ws(const PlanDims& p) {
-    KqWs w;
-    const size_t qbytes = ((size_t)p.B * p.N * p.Hq * p.D + 255) / 256 * 256;
-    w.attn = 0;
-    w.hi = (attn_workspace_bytes(p) + 255) / 256 * 256;
-    w.lo = w.hi + qbytes;
-    w.scale = w.lo + qbytes;
-    w.total = w.scale + ((size_t)p.S * 4 + 255) / 256 * 256;
-    return w;
-}
-
 }  // namespace
 
 lucetree_status verify_attn_check(const lucetree_attn_args* a, bool need_mask, int v_format, AttnLaunch* L);
@@ -239,7 +131,7 @@ extern "C" lucetree_status lucetree_verify_attn_kq_workspace(int B, int N, int H
     if (D != 256) return LUCETREE_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LUCETREE_ERR_CUDA;
-    *bytes = kq_ws(make_plan(B, N, Hq, Hkv, D, prefix_grid_ctas(dev), 1)).total;
+    *bytes = attn_workspace_bytes(make_plan(B, N, Hq, Hkv, D, prefix_grid_ctas(dev), 1));
     return LUCETREE_OK;
 }
 
@@ -256,25 +148,14 @@ extern "C" lucetree_status lucetree_verify_attn_kq(const lucetree_attn_args* a, 
     AttnLaunch L;
     lucetree_status st = verify_attn_check(a, true, v_format, &L);
     if (st != LUCETREE_OK) return st;
-    const KqWs w = kq_ws(L.plan);
-    if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    if (!workspace || workspace_bytes < attn_workspace_bytes(L.plan) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return LUCETREE_ERR_WORKSPACE;
-    char* ws = reinterpret_cast<char*>(workspace);
-    L.ws = reinterpret_cast<float*>(ws + w.attn);
+    L.ws = reinterpret_cast<float*>(workspace);
     L.v_exp = v_format != LUCETREE_V_SAME ? v_exp : nullptr;
     L.k_format = LUCETREE_K_E4M3;
     L.k_exp = k_exp;
-    L.q_hi = reinterpret_cast<uint8_t*>(ws + w.hi);
-    L.q_lo = reinterpret_cast<uint8_t*>(ws + w.lo);
-    L.q_scale = reinterpret_cast<float*>(ws + w.scale);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int items = a->N * L.plan.G * a->D / 8;
-    const int parts = (items + kSplitThreads * kSplitItems - 1) / (kSplitThreads * kSplitItems);
-    if (launch_pdl(q_split_kernel, dim3(L.plan.S, parts), dim3(kSplitThreads), 0, s,
-                   reinterpret_cast<const __nv_bfloat16*>(a->q), a->N, a->Hq, L.plan.G, a->D, L.scale_log2,
-                   const_cast<uint8_t*>(L.q_hi), const_cast<uint8_t*>(L.q_lo), const_cast<float*>(L.q_scale)) !=
-        cudaSuccess)
-        return LUCETREE_ERR_CUDA;
     if (launch_attn_prefix(L, s) != cudaSuccess) return LUCETREE_ERR_CUDA;
     if (launch_attn_merge(L, s) != cudaSuccess) return LUCETREE_ERR_CUDA;
     return LUCETREE_OK;

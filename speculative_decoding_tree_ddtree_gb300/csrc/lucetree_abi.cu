@@ -178,8 +178,6 @@ lucetree_status verify_attn_check(const lucetree_attn_args* a, bool need_mask, i
     L->v_exp = nullptr;
     L->k_format = LUCETREE_K_SAME;
     L->k_exp = nullptr;
-    L->q_hi = L->q_lo = nullptr;
-    L->q_scale = nullptr;
     return LUCETREE_OK;
 }
 
