@@ -624,9 +624,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint4* base = reinterpret_cast<uint4*>(sSlots + ((vbase + c) % kNS) * kChunkBytes);
                 const int nv = nvalid - 64 * (c & 1);  // valid keys of this chunk's page
-                if (BF16 || nv < 64) {
-                    constexpr int kUnits = kChunkBytes / 16 / (32 * kConvWarps);  // 16 per thread
-                    constexpr int kBatch = 4;                                      // loads in flight
+                constexpr int kUnits = kChunkBytes / 16 / (32 * kConvWarps);  // 16 per thread
+                constexpr int kBatch = 4;                                      // loads in flight
+                if (BF16 && nv >= 64) {
+                    // a full page (every chunk but a segment's last few): no per-key test
+#pragma unroll 1
+                    for (int i0 = 0; i0 < kUnits; i0 += kBatch) {
+                        uint4 x[kBatch];
+#pragma unroll
+                        for (int k = 0; k < kBatch; ++k) x[k] = base[ct + 32 * kConvWarps * (i0 + k)];
+#pragma unroll
+                        for (int k = 0; k < kBatch; ++k) {
+                            x[k].x = bf16x2_to_f16x2(x[k].x);
+                            x[k].y = bf16x2_to_f16x2(x[k].y);
+                            x[k].z = bf16x2_to_f16x2(x[k].z);
+                            x[k].w = bf16x2_to_f16x2(x[k].w);
+                            base[ct + 32 * kConvWarps * (i0 + k)] = x[k];
+                        }
+                    }
+                } else if (BF16 || nv < 64) {
 #pragma unroll 1
                     for (int i0 = 0; i0 < kUnits; i0 += kBatch) {
                         uint4 x[kBatch];
@@ -765,8 +781,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             uint32_t ek_next = 0;
             float qs = 0.f;
+            int pg0 = -1;  // E4M3 K: my key's page for the piece's first tile (its exponent is read after the split)
             if constexpr (KQ) {
-                ek_next = k_exp_of(page_of(cur.pc.ta));
+                pg0 = page_of(cur.pc.ta);
                 // The piece's bf16 queries (four 64-dim chunks of [RGP rows][128 B],
                 // 128-byte swizzled) become two E4M3 parts in place, scaled by 2^p so
                 // that their largest magnitude lies in (224, 448]: hi = e4m3(q 2^p),
@@ -848,6 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
 
+            if constexpr (KQ) ek_next = k_exp_of(pg0);
             while (cur.live && cur.piece_no == piece_no) {
                 const int t = cur.t;
                 // validity of my page for 32 tiles at a time (one load per lane)
