@@ -308,6 +308,27 @@ def time_attention(LT, step, dd, stream, n, flush=None, group=10):
     return [a.elapsed_time(b) / span for a, b in ev]
 
 
+def time_spans(call, stream, dev, n, group=10):
+    """ms per call of `call` on `stream`, one value per span of `group` calls
+    run back to back between CUDA events (as the headline call is timed: an
+    event between two calls would stop the next call's programmatic launch
+    from overlapping this one's tail), after five untimed calls."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(max(1, n // group))]
+        torch.cuda.synchronize(dev)
+        for e0, e1 in ev:
+            e0.record(stream)
+            for _ in range(group):
+                call()
+            e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return [a.elapsed_time(b) / group for a, b in ev]
+
+
 def attn_flops(cfg: W.VerifyConfig) -> int:
     """Algorithmic flops of one attention call: Q.K^T and P.V over the
     committed prefix, 4 * N * Hq * L * D per sequence."""
@@ -830,7 +851,8 @@ def measure_delta(args, dev, stream, rank, with_cpu=True):
 def measure_vq(args, dev, stream, rank, d, step, cfg):
     """The headline attention call with V stored quantised (int8 and int4 codes,
     one power-of-two exponent per token and head; K stays bf16), timed with
-    CUDA events on the stream over the same resident inputs as the step."""
+    CUDA events on the stream over the same resident inputs as the step, in
+    spans of ten back-to-back calls like the 16-bit call."""
     import torch
     from speculative_decoding_tree_ddtree_gb300 import lucetree as LT
     res = {}
@@ -847,18 +869,7 @@ def measure_vq(args, dev, stream, rank, d, step, cfg):
                                        d["k_tree"], d["v_tree"], step.anc, step.out, step.status, step.ws_attn,
                                        stream=stream)
 
-        with torch.cuda.stream(stream):
-            for _ in range(5):
-                call()
-            n = max(20, min(200, args.steps // 10))
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-            torch.cuda.synchronize(dev)
-            for e0, e1 in evs:
-                e0.record(stream)
-                call()
-                e1.record(stream)
-        torch.cuda.synchronize(dev)
-        st_ms = ms_stats([e0.elapsed_time(e1) for e0, e1 in evs])
+        st_ms = ms_stats(time_spans(call, stream, dev, max(20, min(200, args.steps // 10))))
         ms = st_ms["mean"]
         nbytes = int(L * cfg.Hkv * cfg.D * (2 + vbytes) + L * cfg.Hkv
                      + cfg.B * cfg.N * cfg.Hq * cfg.D * 2 + cfg.B * cfg.N * cfg.Hq * cfg.D * 4 + 4 * L // 64)
@@ -874,7 +885,8 @@ def measure_vq(args, dev, stream, rank, d, step, cfg):
 def measure_kq(args, dev, stream, rank, d, step, cfg):
     """The headline attention call with K stored as FP8 E4M3 codes (one
     power-of-two exponent per token and head) and V in bf16 or as int8 codes,
-    timed with CUDA events on the stream over resident inputs.  The codes
+    timed with CUDA events on the stream over resident inputs, in spans of ten
+    back-to-back calls like the 16-bit call.  The codes
     are drawn on the device from N(0, 160^2) values, the exponents uniform in
     [119, 120] (keys of about unit spread: the generator's default)."""
     import torch
@@ -907,18 +919,7 @@ def measure_kq(args, dev, stream, rank, d, step, cfg):
             LT.lucetree_verify_attn_kq(d["q"], kc, ke, vp, d["page_table"], d["ctx_len"], d["k_tree"], d["v_tree"],
                                        step.anc, step.out, step.status, ws, v_format=fmt, v_exp=vx, stream=stream)
 
-        with torch.cuda.stream(stream):
-            for _ in range(5):
-                call()
-            n = max(20, min(200, args.steps // 10))
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-            torch.cuda.synchronize(dev)
-            for e0, e1 in evs:
-                e0.record(stream)
-                call()
-                e1.record(stream)
-        torch.cuda.synchronize(dev)
-        st_ms = ms_stats([e0.elapsed_time(e1) for e0, e1 in evs])
+        st_ms = ms_stats(time_spans(call, stream, dev, max(20, min(200, args.steps // 10))))
         per_tok = cfg.Hkv * (cfg.D * (1 + vbytes) + 1 + (1 if fmt != LT.LUCETREE_V_SAME else 0))
         nbytes = int(L * per_tok + cfg.B * cfg.N * cfg.Hq * cfg.D * 2 + cfg.B * cfg.N * cfg.Hq * cfg.D * 4
                      + 4 * L // 64)

@@ -700,47 +700,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with the current shifts; lpart += P (sign +1) or -= P (sign -1, the
         // exact undo of a pass made with the same shifts); optionally keeps
         // P (fp16 pairs) in registers `ph` and tracks the largest exponent.
-        // Invalid keys and padding columns give P = 0.  (A separate unmasked
-        // copy of this pass for interior tiles measured slower: the extra code
-        // costs more in instruction fetch than the selects it saves.)
+        // Invalid keys and padding columns give P = 0.
         // P stays in registers so that the pass can run while PV of the
         // previous tile still reads the shared P^T buffer; store_p writes it
         // once that PV has completed.
         auto exp_pass = [&](float (&lpart)[kNa * 16], bool valid, float sign, bool keep_p, float& ex,
                             uint32_t (&ph)[kNa * 8]) {
-            // 8-column blocks b = 2*cc + hb; the TMEM load of block b+1 is in
-            // flight while block b is computed
-            constexpr int kBlocks = 2 * kNa;
-            const int nblk = 2 * nch;
-            uint32_t rn[8];
-            tmem_ld8(tl + 16 * cb, rn);
+            // 16-column chunks, each in two 8-column blocks b = 2*cc + hb; the
+            // TMEM load of chunk cc+1 is in flight while chunk cc is computed.
+            // An invalid key's exponents are -inf, and so are a padding
+            // column's (its shift is +inf), so neither needs a column test.
+            uint32_t rn[16];
+            tmem_ld16(tl + 16 * cb, rn);
 #pragma unroll
-            for (int bi = 0; bi < kBlocks; ++bi) {
-                if (bi >= nblk) continue;
-                uint32_t r[8];
-                tmem_wait_ld_regs(rn);
+            for (int cc = 0; cc < kNa; ++cc) {
+                if (cc >= nch) continue;
+                uint32_t r[16];
+                tmem_wait_ld_regs16(rn);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) r[k] = rn[k];
-                if (bi + 1 < nblk) tmem_ld8(tl + 16 * cb + 8 * (bi + 1), rn);
-                const int cc = bi >> 1, hb = bi & 1;
+                for (int k = 0; k < 16; ++k) r[k] = rn[k];
+                if (cc + 1 < nch) tmem_ld16(tl + 16 * (cb + cc + 1), rn);
                 const int c = cb + cc;
-                const int lim = valid ? R_seg - 16 * c : 0;
-                const float4* m4 = reinterpret_cast<const float4*>(ms->m_ref + 16 * c + 8 * hb);
-                const float4 ma = m4[0], mb = m4[1];
-                const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-                float pv[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float x = fmaf(__uint_as_float(r[k]), sl2, -mv[k]);
-                    const bool ok = 8 * hb + k < lim;
-                    if (ok) ex = fmaxf(ex, x);
-                    pv[k] = ok ? ex2(x) : 0.f;
-                    float& acc = lpart[cc * 16 + 8 * hb + k];
-                    acc = fmaf(sign, pv[k], acc);
-                }
-                if (keep_p) {
+                for (int hb = 0; hb < 2; ++hb) {
+                    const int bi = 2 * cc + hb;
+                    const float4* m4 = reinterpret_cast<const float4*>(ms->m_ref + 16 * c + 8 * hb);
+                    const float4 ma = m4[0], mb = m4[1];
+                    const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                    float pv[8];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) ph[4 * bi + k] = pack_half2(pv[2 * k], pv[2 * k + 1]);
+                    for (int k = 0; k < 8; ++k) {
+                        const float x = valid ? fmaf(__uint_as_float(r[8 * hb + k]), sl2, -mv[k]) : -INFINITY;
+                        ex = fmaxf(ex, x);
+                        pv[k] = ex2(x);
+                        float& acc = lpart[cc * 16 + 8 * hb + k];
+                        acc = fmaf(sign, pv[k], acc);
+                    }
+                    if (keep_p) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) ph[4 * bi + k] = pack_half2(pv[2 * k], pv[2 * k + 1]);
+                    }
                 }
             }
         };
@@ -762,7 +761,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int piece_no = cur.piece_no;
             const int seg = cur.pc.s;
             bar_sync(1, kSoftmaxThreads);
-            for (int col = st; col < RGP; col += kSoftmaxThreads) ms->m_ref[col] = -INFINITY;
+            // padding columns keep a shift of +inf, so their exponents are -inf and P = 0
+            for (int col = st; col < RGP; col += kSoftmaxThreads) ms->m_ref[col] = col < R_seg ? -INFINITY : INFINITY;
             bar_sync(1, kSoftmaxThreads);
             float lpart[kNa * 16];
 #pragma unroll
