@@ -245,6 +245,16 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 // Two bf16 (one 32-bit word) -> two fp16 (round to nearest), exact for
 // magnitudes below 65536; larger magnitudes become inf.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return pack_half2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
@@ -1024,31 +1034,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // int8: the fp16 output of key row r covers bytes [128 r, 128 r + 128) of
                             // each 8 KB box; the second box's lands exactly on row r's own 128 code
                             // bytes and nowhere else.  So one half-warp expands one row (lane l of
-                            // 16: box l / 8, swizzled unit l % 8), all 16 lanes reading before any
-                            // writes: a __syncwarp suffices, no CTA barrier.  Both halves of a warp
+                            // 16: box l / 8, swizzled unit l % 8), its three rows' codes all read
+                            // before any write: a __syncwarp suffices, no CTA barrier.  Both halves of a warp
                             // always get the same number of rows (rows hw, hw + 24, hw + 48).
                             const uint8_t* codes = reinterpret_cast<const uint8_t*>(base) + VCodes<1>::kOff;
                             const uint8_t* ex = ms->vexp[vn % kMaxSlots];
                             const int hw = 2 * (warp - 4) + (lane >> 4), l = lane & 15;
+                            uint2 cws[3];
+                            uint32_t ebs[3];
+#pragma unroll
+                            for (int it = 0; it < 3; ++it) {  // every row's codes read before any write
+                                const int r = hw + 24 * it;
+                                const int d0 = 64 * (l >> 3) + 8 * ((l & 7) ^ (r & 7));
+                                cws[it] = make_uint2(0, 0);
+                                ebs[it] = 0;
+                                if (r < 64 && r < nv) {
+                                    cws[it] = *reinterpret_cast<const uint2*>(codes + r * 128 + d0);
+                                    ebs[it] = ex[r];
+                                }
+                            }
+                            __syncwarp();
 #pragma unroll
                             for (int it = 0; it < 3; ++it) {
                                 const int r = hw + 24 * it;
                                 const int u = (l >> 3) * 512 + r * 8 + (l & 7);
-                                const int d0 = 64 * (l >> 3) + 8 * ((l & 7) ^ (r & 7));
-                                uint2 cw = make_uint2(0, 0);
-                                float sc = 0.f;
-                                if (r < 64 && r < nv) {
-                                    cw = *reinterpret_cast<const uint2*>(codes + r * 128 + d0);
-                                    sc = __uint_as_float((uint32_t)ex[r] << 23);  // 2^(e - 127)
-                                }
-                                __syncwarp();
+                                const uint2 cw = cws[it];
+                                const uint32_t eb = ebs[it];
                                 if (r < 64) {
-                                    float f[8];
+                                    const float sc = __uint_as_float(eb << 23);  // 2^(e - 127)
+                                    // (with E4M3 K the fp32 route below measured faster in this kernel)
+                                    if (!KQ && eb >= 103 && eb <= 132) {
+                                        // 2^(e-127) and 1152 * 2^(e-127) are fp16 numbers: each code c
+                                        // becomes the fp16 1024 + (c + 128) (its byte under an exponent
+                                        // of 2^10), and one fused (x - 1152) * 2^(e-127) per pair is exact
+                                        const uint32_t s2 = pack_half2(sc, sc), n2 = pack_half2(-1152.f * sc, -1152.f * sc);
+                                        const uint32_t ux = cw.x ^ 0x80808080u, uy = cw.y ^ 0x80808080u;
+                                        base[u] = make_uint4(hfma2(prmt(ux, 0x64646464u, 0x5140u), s2, n2),
+                                                             hfma2(prmt(ux, 0x64646464u, 0x5342u), s2, n2),
+                                                             hfma2(prmt(uy, 0x64646464u, 0x5140u), s2, n2),
+                                                             hfma2(prmt(uy, 0x64646464u, 0x5342u), s2, n2));
+                                    } else {
+                                        float f[8];
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e)
-                                        f[e] = (float)(int)(int8_t)(((e < 4 ? cw.x : cw.y) >> (8 * (e & 3))) & 0xFFu) * sc;
-                                    base[u] = make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]),
-                                                         pack_half2(f[4], f[5]), pack_half2(f[6], f[7]));
+                                        for (int e = 0; e < 8; ++e)
+                                            f[e] = (float)(int)(int8_t)(((e < 4 ? cw.x : cw.y) >> (8 * (e & 3))) & 0xFFu) * sc;
+                                        base[u] = make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]),
+                                                             pack_half2(f[4], f[5]), pack_half2(f[6], f[7]));
+                                    }
                                 }
                             }
                         } else if constexpr (VQ == 2) {
@@ -1058,12 +1090,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint8_t* codes = reinterpret_cast<const uint8_t*>(base) + VCodes<VQ>::kOff;
                             const uint8_t* ex = ms->vexp[vn % kMaxSlots];
                             uint2 cw[3];
-                            float sc[3];
+                            uint32_t eb[3];
 #pragma unroll
                             for (int i = 0; i < 3; ++i) {
                                 const int u = st + kSoftmaxThreads * i;
                                 cw[i] = make_uint2(0, 0);
-                                sc[i] = 0.f;
+                                eb[i] = 0;
                                 if (landed && u < 1024) {
                                     const int r = (u & 511) >> 3, d0 = 64 * (u >> 9) + 8 * ((u & 7) ^ (r & 7));
                                     if (r < nv) {
@@ -1071,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             cw[i] = *reinterpret_cast<const uint2*>(codes + r * 128 + d0);
                                         else
                                             cw[i].x = *reinterpret_cast<const uint32_t*>(codes + r * 64 + d0 / 2);
-                                        sc[i] = __uint_as_float((uint32_t)ex[r] << 23);  // 2^(e - 127)
+                                        eb[i] = ex[r];
                                     }
                                 }
                             }
@@ -1085,18 +1117,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int i = 0; i < 3; ++i) {
                                 const int u = st + kSoftmaxThreads * i;
                                 if (u < 1024) {
-                                    float f[8];
+                                    const float sc = __uint_as_float(eb[i] << 23);  // 2^(e - 127)
+                                    if (eb[i] >= 103 && eb[i] <= 132) {
+                                        // as for int8: nibbles with their sign bit flipped (c + 8) go
+                                        // into bytes in dimension order, each byte under an fp16
+                                        // exponent of 2^10, then one exact fused (x - 1032) * 2^(e-127)
+                                        const uint32_t s2 = pack_half2(sc, sc), n2 = pack_half2(-1032.f * sc, -1032.f * sc);
+                                        const uint32_t w = cw[i].x ^ 0x88888888u;
+                                        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+                                        const uint32_t p0 = prmt(lo, hi, 0x5140u), p1 = prmt(lo, hi, 0x7362u);
+                                        base[u] = make_uint4(hfma2(prmt(p0, 0x64646464u, 0x5140u), s2, n2),
+                                                             hfma2(prmt(p0, 0x64646464u, 0x5342u), s2, n2),
+                                                             hfma2(prmt(p1, 0x64646464u, 0x5140u), s2, n2),
+                                                             hfma2(prmt(p1, 0x64646464u, 0x5342u), s2, n2));
+                                    } else {
+                                        float f[8];
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) {
-                                        int q;
-                                        if constexpr (VQ == 1)
-                                            q = (int)(int8_t)(((e < 4 ? cw[i].x : cw[i].y) >> (8 * (e & 3))) & 0xFFu);
-                                        else
-                                            q = ((int)(cw[i].x << (28 - 4 * e))) >> 28;
-                                        f[e] = (float)q * sc[i];
+                                        for (int e = 0; e < 8; ++e) f[e] = (float)(((int)(cw[i].x << (28 - 4 * e))) >> 28) * sc;
+                                        base[u] = make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]),
+                                                             pack_half2(f[4], f[5]), pack_half2(f[6], f[7]));
                                     }
-                                    base[u] = make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]),
-                                                         pack_half2(f[4], f[5]), pack_half2(f[6], f[7]));
                                 }
                             }
                         }

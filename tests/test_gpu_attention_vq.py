@@ -92,6 +92,25 @@ def test_quantised_v_zero_exponents_read_as_zero(cuda_dev):
     assert status == 0 and row_error(got, ref.reshape(got.shape)).max() <= ATTN_TOL
 
 
+@pytest.mark.parametrize("v_format", [W.V_INT8, W.V_INT4], ids=["int8", "int4"])
+def test_quantised_v_exponents_across_fp16_range(cuda_dev, v_format):
+    # per-token exponents from 2^-31 to 2^9 (every code times its power of two stays an fp16
+    # number or underflows to an fp16 subnormal), some zero: rows whose scale and 1152 (1032)
+    # times it are fp16 numbers and rows whose are not expand by different routes on chip
+    cfg = W.VerifyConfig("vq-exprange", ctx=(3000, 130, 1025), Hq=12, Hkv=3, D=256, dtype=W.BF16, N=9,
+                         tree="random", branch_cap=3, vocab=512, paged="permuted", spare_pages=3)
+    inp = W.generate(cfg, seed=41)
+    vq = W.generate_vq(cfg, v_format, seed=41)
+    rng = np.random.default_rng(41)
+    e = rng.integers(96, 137, size=vq["v_exp"].shape)
+    e[rng.random(e.shape) < 0.05] = 0
+    vq["v_exp"][:] = e.astype(np.uint8)
+    got, status = _run_vq(cfg, inp, vq, v_format)
+    assert status == 0
+    ref = _reference(cfg, inp, vq, v_format)
+    assert row_error(got, ref.reshape(got.shape)).max() <= ATTN_TOL
+
+
 def test_quantised_v_refuses_head_dim_128(cuda_dev):
     import torch
     LT = _lt()
