@@ -33,17 +33,19 @@
 // Softmax over keys runs across TMEM lanes.  Each softmax thread owns one key
 // lane and keeps per-column partial sums in registers; the shift m[r] per
 // query row is stale on purpose.  A tile is first exponentiated with the
-// current shifts (one streaming pass: P^T written, sums accumulated, largest
-// exponent tracked); if any exponent exceeds 8 (log2 domain) the pass is taken
+// current shifts (one streaming pass: P kept in registers, sums accumulated,
+// largest exponent tracked; padding columns carry a shift of +inf, so they give
+// P = 0 without a column test); if any exponent exceeds 8 (log2 domain) the pass is taken
 // back out exactly, the tile's column maxima are found (warp shuffles +
 // shared memory) and the partial sums and already-accumulated O^T columns are
 // rescaled before the tile is redone.  The first tile of every range goes
 // straight to that path.  Sums are reduced across lanes once per range.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2..3 idle (they
-// complete warpgroup 0, which hands most of its registers to the others),
-// 4..15 = softmax, V conversion and epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and
-// handles one third of the row tile's column chunks.  K and V stream through
+// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2..3 = bf16 -> fp16
+// conversion of 16-bit V chunks (warpgroup 0 hands most of its registers to the
+// others), 4..15 = softmax, expansion of quantised V codes, and epilogue: warp w
+// reads TMEM lanes 32*(w%4) .. +31 and handles one third of the row tile's
+// column chunks.  K and V stream through
 // a ring of 16 KB chunk slots, two TMA boxes of [64 keys][64 d] (128-byte
 // swizzle) per slot; an operand (one tile's K or V) is D/64 consecutive
 // chunks.  A K chunk is [128 keys][64 d] (one box per 64-token page: the
@@ -118,7 +120,8 @@ struct Misc {
     uint64_t empty[kMaxSlots];
     // V chunks have their own barriers, indexed by V chunk number n (in V
     // order) modulo kMaxSlots >= kNS: vfull[n % kMaxSlots] = landed,
-    // vready[n % kMaxSlots] = converted by the softmax warps.  full[slot] still
+    // vready[n % kMaxSlots] = made the fp16 operand (16-bit V by warps 2 and 3,
+    // quantised V by the softmax warps).  full[slot] still
     // completes one phase per fill (a plain arrive for V fills), so the K
     // waits' parities keep counting fills.
     uint64_t vfull[kMaxSlots];
@@ -575,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t dO = tmem + (h ? Lay::kColO1 : Lay::kColO0);
                         for (int kh = 0; kh < 2 && ok; ++kh) {
                             const int slot = chunk % kNS;
-                            // landed and converted by the softmax warps
+                            // landed and made the fp16 operand
                             const uint32_t vn = j * kChunksV + 2 * h + kh;
                             if (!(ok = mbar_wait(&ms->vready[vn % kMaxSlots], (vn / kMaxSlots) & 1))) break;
                             tc_fence_after();
