@@ -57,7 +57,8 @@ cudaError_t launch_lmhead(const lucetree_lmhead_args& a, void* ws, cudaStream_t 
     int dev = 0;
     cudaGetDevice(&dev);
     const int n_tiles = (a.vocab + lmhead::kVT - 1) / lmhead::kVT;
-    const int ctas = n_tiles < device_sm_count(dev) ? n_tiles : device_sm_count(dev);
+    const int slots = device_sm_count(dev) * lmhead::ctas_per_sm(rp);
+    const int ctas = n_tiles < slots ? n_tiles : slots;
     return a.dtype == LUCETREE_BF16 ? launch_lmhead_bf16(rp, tw, th, k, ctas, stream)
                                     : launch_lmhead_f16(rp, tw, th, k, ctas, stream);
 }

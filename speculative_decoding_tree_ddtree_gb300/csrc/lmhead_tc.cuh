@@ -39,6 +39,12 @@ constexpr int kMaxW = 16;
 constexpr int kHS = 4;                  // hidden-state chunk slots
 constexpr uint32_t kTmemCols = 512;
 
+// Two CTAs per SM for up to 64 padded rows (the verify budgets): each keeps its
+// own weight ring and half the tensor memory, so an SM streams two independent
+// in-order rings, which keeps more of the weight in flight than one deeper ring.
+// Larger row counts need the whole shared memory for their hidden-state ring.
+__host__ __device__ constexpr int ctas_per_sm(int rp) { return rp <= 64 ? 2 : 1; }
+
 struct Args {
     int rows, d_model, vocab;
     unsigned long long* keys;  // [rows] workspace, zero between calls
@@ -50,17 +56,20 @@ struct Args {
 
 template <int RP>
 struct Layout {
+    static constexpr int kCps = ctas_per_sm(RP);
+    static constexpr uint32_t kTmem = kTmemCols / kCps;                         // columns this CTA owns
+    static constexpr int kBudget = kCps == 1 ? kSmemLimit : 113 * 1024;        // per CTA
     static constexpr int kHBytes = RP * 128;  // one hidden-state chunk [RP rows][64 d]
-    static constexpr int kTPG = (int)kTmemCols / RP < 16 ? (int)kTmemCols / RP : 16;  // tiles per TMEM fill
+    static constexpr int kTPG = (int)kTmem / RP < 16 ? (int)kTmem / RP : 16;  // tiles per TMEM fill
     static constexpr int kMiscBytes = 4096;
     static constexpr int kHOff = 0;
     static constexpr int kWOff = ((kHS * kHBytes + 1023) / 1024) * 1024;
-    static constexpr int kWRaw = (kSmemLimit - 1024 - kWOff - kMiscBytes) / kWChunk;
+    static constexpr int kWRaw = (kBudget - 1024 - kWOff - kMiscBytes) / kWChunk;
     static constexpr int kNW = kWRaw > kMaxW ? kMaxW : kWRaw;
     static constexpr int kMiscOff = kWOff + kNW * kWChunk;
     static constexpr int kBytes = kMiscOff + kMiscBytes + 1024;
     static_assert(kNW >= 4, "weight ring");
-    static_assert(kBytes <= kSmemLimit, "shared memory budget");
+    static_assert(kBytes <= kBudget, "shared memory budget");
 };
 
 struct Misc {
@@ -114,7 +123,7 @@ __device__ __forceinline__ void set_abort(Misc* ms, uint32_t* status) {
 __device__ __forceinline__ bool aborted(Misc* ms) { return *(volatile int*)&ms->abort_flag != 0; }
 
 template <bool BF16, int RP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(RP))
     lmhead_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h, const Args a) {
     using Lay = Layout<RP>;
     constexpr int kTPG = Lay::kTPG;
@@ -154,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_fence_init();
     }
     if (warp == 1) {
-        tmem_alloc(&ms->tmem_base, kTmemCols);
+        tmem_alloc(&ms->tmem_base, Lay::kTmem);
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc(tmem, Lay::kTmem);
     for (int r = threadIdx.x; r < a.rows; r += kThreads)
         if (ms->row_key[r]) atomicMax(a.keys + r, ms->row_key[r]);
     __threadfence();
